@@ -1,0 +1,191 @@
+/*
+ * lynx.h -- C ABI of the GB300 (sm_103a) Lynx hot path.
+ *
+ * Lynx ("Lynx: Progressive Speculative Quantization for accelerating KV
+ * Transfer in Long-Context Inference") splits each KV-cache value into an
+ * 8-bit code and ships it as two 4-bit streams: an Anchor (most significant
+ * nibble) that is enough for speculative draft decoding, and a Residual
+ * (least significant nibble) that restores the full code for verification.
+ * This library implements, as CUDA kernels for one GB300 GPU:
+ *
+ *   lynx_encode_pages     Algorithm 1 of the paper (§4.1): BF16 pages ->
+ *                         packed Anchor plane, packed Residual plane, fp32
+ *                         metadata.
+ *   lynx_reconstruct      the two dequantisation phases of §4.2 (Anchor only:
+ *                         draft KV; Anchor + Residual: verification KV).
+ *   lynx_decode_attn      softmax(Q K^T * scale) V (§2.1) over the packed
+ *                         planes, dequantised in registers; 1 query token
+ *                         (draft decode) or T tokens (the parallel
+ *                         verification pass of §4.3).
+ *   lynx_decode_attn_bf16 the same attention over plain BF16 pages (the
+ *                         uncompressed baseline the paper compares against).
+ *
+ * ---------------------------------------------------------------------------
+ * Data layout (all sizes for H = 128 channels, P = 256 tokens, C = 32):
+ *
+ *   KV page      One KV head's 128 channels x 256 consecutive tokens, BF16,
+ *                channel-major: element (c, t) at index c*256 + t.  65536 B.
+ *   Anchor plane Per page uint8[128][128]: byte j of channel row c holds the
+ *                4-bit two's-complement anchor of token 2j in its low nibble
+ *                and of token 2j+1 in its high nibble (paper §5: two 4-bit
+ *                segments per byte).  16384 B per page.
+ *   Residual     Same layout, 4-bit two's-complement residual.  16384 B.
+ *   Metadata     Per page float32[2304] = gamma_min[128], gamma_scale[128],
+ *                mu[128][8], sigma[128][8] (Algorithm 1's metadata).  9216 B.
+ *
+ * Code definition (per channel c of a page, per token t, chunk b = t / 32):
+ *   x_n = (x - gamma_min) / (gamma_scale + eps)              (Stage 1)
+ *   mu  = (x_n[32b] + ... + x_n[32b+31]) / 32, summed left to right
+ *   sigma = max |x_n - mu| over the chunk
+ *   x_f = (x_n - mu) / (sigma + eps)                           (Stage 2)
+ *   I   = round(127 ln(1 + alpha |x_f|) / ln(1 + alpha))       (Stage 3, Eq. 3)
+ *   S   = -1 if x_f < 0 else +1
+ *   anchor   = (S > 0 ? I : -I - 1) >> 4   (arithmetic shift), in [-8, 7]
+ *   residual = 16 * (I >> 4) + 7 - I,                          in [-8, 7]
+ * Every step of Stages 1-2 is one correctly rounded IEEE float32 operation;
+ * the rounding of Stage 3 is decided exactly for the float32 x_f.  The anchor
+ * equals Stage 4's sign-aware two's-complement map applied to V = I >> 4; the
+ * Round-Half-Down bias (+7) sits at the anchor's reconstruction point 16 V + 7,
+ * which keeps both streams within 4 bits (as printed, Stage 4 gives an anchor
+ * with 18 levels).
+ *
+ * Reconstruction:  I_hat = 16 V + 7 (anchor only) or 16 V + 7 - residual,
+ *   x_hat = gamma_min + (gamma_scale+eps) * (mu + (sigma+eps) * S * l(I_hat)),
+ *   l(y) = ((1 + alpha)^(y/127) - 1) / alpha   (Eq. 4; inverse of Eq. 3).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every entry point:
+ *   - Device pointers unless stated.  The caller owns and allocates every
+ *     buffer; the library allocates no device or host memory and keeps no
+ *     state beyond per-device constant tables.
+ *   - Pointers must be 16-byte aligned (LYNX_ERR_ALIGNMENT otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and never synchronise.  A non-zero return means nothing
+ *     was launched, except LYNX_ERR_CUDA, which reports a failed launch.
+ *   - Inputs must be finite; NaN or Inf give unspecified codes.
+ *   - Supported shapes: H = 128, P = 256, C = 32, head_dim = 128,
+ *     0.25 <= alpha <= 1e6, 0 < eps <= 1e-2.  Others return
+ *     LYNX_ERR_UNSUPPORTED.
+ *   - Thread safety: entry points may be called from several host threads;
+ *     lynx_last_error() is per host thread.
+ */
+#ifndef LYNX_H_
+#define LYNX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Method parameters.  Defaults {128, 256, 32, 100.0f, 1e-6f}. */
+typedef struct lynx_params {
+  int32_t H;      /* channels per page (block size of Algorithm 1); must be 128 */
+  int32_t P;      /* tokens per page; must be 256                               */
+  int32_t C;      /* tokens per chunk (Stage 2); must be 32                     */
+  float alpha;    /* alpha of the compander, Eq. (3)                            */
+  float eps;      /* epsilon of Algorithm 1, Stages 1 and 2                     */
+} lynx_params_t;
+
+enum {
+  LYNX_OK = 0,
+  LYNX_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad enum      */
+  LYNX_ERR_UNSUPPORTED = -2,   /* shape or parameter outside the supported set */
+  LYNX_ERR_ALIGNMENT = -3,     /* a pointer is not 16-byte aligned           */
+  LYNX_ERR_WORKSPACE = -4,     /* workspace missing or too small             */
+  LYNX_ERR_CUDA = -5,          /* CUDA runtime error (message in lynx_last_error) */
+  LYNX_ERR_DEVICE = -6         /* a kernel gave up a bounded wait (see lynx_device_status) */
+};
+
+/* Output element types of lynx_reconstruct. */
+enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 };
+
+/* Algorithm 1 (paper §4.1, all four stages) on n_pages BF16 pages.
+ *   x_bf16    [n_pages][128][256] BF16 (read only)
+ *   anchor    [n_pages][128][128] uint8, written
+ *   residual  [n_pages][128][128] uint8, written
+ *   meta      [n_pages][2304] float32, written
+ * n_pages == 0 is a no-op.  Errors: INVALID_ARG (null pointer with n_pages>0,
+ * n_pages<0, null params), UNSUPPORTED, ALIGNMENT, CUDA. */
+int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
+                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream);
+
+/* Dequantisation (paper §4.2: Anchor phase and Residual phase).
+ *   residual == NULL selects the anchor-only reconstruction (draft KV);
+ *   otherwise the full code is used (verification KV).
+ *   out       [n_pages][128][256], BF16 (out_dtype = LYNX_OUT_BF16, rounded
+ *             to nearest even from the float32 result) or float32
+ *             (LYNX_OUT_F32).  The float32 value is
+ *             fmaf(fmaf(S*l(I_hat), sigma+eps, mu), gamma_scale+eps, gamma_min)
+ *             with S*l(I_hat) rounded to float32.
+ * Errors as for lynx_encode_pages; INVALID_ARG for an unknown out_dtype. */
+int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
+                     int64_t n_pages, const lynx_params_t* params, void* out, int out_dtype,
+                     void* stream);
+
+/* Split-K decode / verification attention over packed planes (paper §2.1 and
+ * §4.2-4.3), dequantising in registers.
+ *   q_bf16      [B][T][Hq][128] BF16.  Query head hq attends KV head hq / (Hq/Hkv).
+ *   k_anc, v_anc, k_meta, v_meta   page pools (layouts above), indexed by page id.
+ *   k_res, v_res  NULL for the draft (anchor-only) KV; both non-NULL for the
+ *               full codes.  Mixing is INVALID_ARG.
+ *   n_pool_pages  pages in each pool; a page id outside 0..n_pool_pages-1
+ *               is not dereferenced: page 0 is read instead and the device
+ *               error word is set (see lynx_device_status).
+ *   page_table  [B][Hkv][max_pages] int32 page ids (device).  Entries past a
+ *               sequence's last page are never read.
+ *   ctx_len     [B] int32 (device): keys in each sequence, 0..max_pages*256
+ *               (values outside are clamped and set the device error word).
+ *   causal      0: every query row sees all ctx_len keys.  1: query token i
+ *               (0-based, of T) sees keys 0 .. ctx_len - T + i; a row with no
+ *               visible key outputs zeros and lse = -inf.
+ *   sm_scale    logit scale (1/sqrt(128) in the paper's formula).
+ *   out         [B][T][Hq][128] float32;  lse [B][T][Hq] float32 = natural
+ *               log of sum_j exp(sm_scale * q.k_j) (NULL to skip).
+ *   workspace   device scratch of at least lynx_decode_attn_workspace_size()
+ *               bytes (LYNX_ERR_WORKSPACE otherwise); contents need no
+ *               initialisation and are clobbered.
+ * All values of every page a sequence touches must be finite, including the
+ * positions past ctx_len in its last page.
+ * Limits: 1 <= T <= 32, Hq % Hkv == 0, T * (Hq/Hkv) <= 256, max_pages >= 1,
+ * B <= 65535, Hkv * ceil(T*(Hq/Hkv)/4) <= 65535. */
+int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                     const uint8_t* k_anc, const uint8_t* k_res, const float* k_meta,
+                     const uint8_t* v_anc, const uint8_t* v_res, const float* v_meta,
+                     int64_t n_pool_pages, const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len,
+                     const lynx_params_t* params, float sm_scale, int causal,
+                     float* out, float* lse, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Same attention over plain BF16 page pools k_pages / v_pages ([id][128][256]). */
+int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                          const void* k_pages, const void* v_pages, int64_t n_pool_pages,
+                          const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                          float sm_scale, int causal, float* out, float* lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes needed by lynx_decode_attn / lynx_decode_attn_bf16 for the
+ * given shape on the current device (0 for invalid shapes). */
+size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages);
+
+/* Reads and clears the current device's error word, which kernels set when a
+ * bounded wait on a TMA transfer gives up.  Synchronises the device.
+ * Returns LYNX_OK, LYNX_ERR_DEVICE, or LYNX_ERR_CUDA. */
+int lynx_device_status(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* lynx_status_string(int status);
+
+/* Detail of the last error returned on this host thread ("" if none). */
+const char* lynx_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int lynx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LYNX_H_ */

@@ -25,19 +25,28 @@ def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
 
     ``n_visible[r]`` (optional) limits row r to keys 0 .. n_visible[r]-1.
     Returns (o[R, D], lse[R]) in float64.
+    A row that sees no key has no softmax: its output is NaN (undefined) and
+    its log-sum-exp is -inf (the log of an empty sum).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
+    R, L = q.shape[0], k.shape[0]
+    if L == 0:
+        return np.full((R, v.shape[1]), np.nan), np.full(R, -np.inf)
     s = (q @ k.T) * float(scale)
     if n_visible is not None:
-        cols = np.arange(k.shape[0])[None, :]
+        cols = np.arange(L)[None, :]
         s = np.where(cols < np.asarray(n_visible)[:, None], s, -np.inf)
     m = s.max(axis=1, keepdims=True)
-    p = np.exp(s - m)
-    l = p.sum(axis=1, keepdims=True)
-    o = (p @ v) / l
-    lse = (m + np.log(l))[:, 0]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        o = (p @ v) / l
+        lse = (m + np.log(l))[:, 0]
+    empty = ~np.isfinite(m[:, 0])
+    o[empty] = np.nan
+    lse[empty] = -np.inf
     return o, lse
 
 

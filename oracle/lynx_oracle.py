@@ -22,16 +22,16 @@ reconstruction are evaluated in float64.
 
 Readings of the pages where they are silent, garbled or inconsistent (all of
 them listed in the design notes):
-  * Anchor/Residual split ("reading B").  As printed, lines 14-18 of
-    Algorithm 1 give an anchor magnitude (I+7)>>4 in 0..8, i.e. 18 signed
+  * Anchor/Residual split ("reading B").  As printed, Stage 4 of
+    Algorithm 1 gives an anchor magnitude (I+7)>>4 in 0..8, i.e. 18 signed
     levels, which cannot be the 4-bit anchor the paper ships two per byte.
     Here the anchor magnitude is V = I >> 4 (the top 3 magnitude bits), the
-    anchor is line 18's sign-aware map of V, which equals the int8 code
+    anchor is Stage 4's sign-aware two's-complement map of V, which equals the int8 code
     (S>0 ? I : -I-1) shifted right by 4, and the Round-Half-Down +7 bias moves
     to the reconstruction point V_recon = 16*V + 7, so the residual
     Q_res = V_recon - I is a centred signed 4-bit correction in [-8, 7].
     ``split_stream_literal`` keeps the printed lines for the worked example.
-  * Sign source: line 12 prints Sign(X_view), but X_view lies in [0, 1]; the
+  * Sign source: Stage 3 prints Sign(X_view), but X_view lies in [0, 1]; the
     sign is taken from X_final, and zero counts as positive.
   * Mean over a chunk: the C values are summed left to right in float32 and the
     sum is divided by C.
@@ -50,7 +50,7 @@ from dataclasses import dataclass
 import numpy as np
 
 MAG_MAX = 127          # 2^7 - 1, Eq. (3)
-NIBBLE_BIAS = 7        # Round-Half-Down bias of Algorithm 1, line 14
+NIBBLE_BIAS = 7        # Round-Half-Down bias of Algorithm 1, Stage 4
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -77,24 +77,24 @@ def expander(y, alpha):
 @dataclass
 class Stages:
     """Every intermediate of Algorithm 1 for a batch of pages [N, H, P]."""
-    gmin: np.ndarray      # [N, H]       float32  (line 2)
-    gscale: np.ndarray    # [N, H]       float32  (line 3)
-    xn: np.ndarray        # [N, H, P]    float32  (line 4)
-    mu: np.ndarray        # [N, H, P/C]  float32  (line 7)
-    xcent: np.ndarray     # [N, H, P/C, C] float32 (line 7)
-    sigma: np.ndarray     # [N, H, P/C]  float32  (line 8)
-    xfinal: np.ndarray    # [N, H, P/C, C] float32 (line 8)
-    Y: np.ndarray         # [N, H, P]    float64  (line 10)
-    I: np.ndarray         # [N, H, P]    int32    (line 11)
-    S: np.ndarray         # [N, H, P]    int32 +-1 (line 12)
+    gmin: np.ndarray      # [N, H]       float32  (Stage 1)
+    gscale: np.ndarray    # [N, H]       float32  (Stage 1)
+    xn: np.ndarray        # [N, H, P]    float32  (Stage 1)
+    mu: np.ndarray        # [N, H, P/C]  float32  (Stage 2)
+    xcent: np.ndarray     # [N, H, P/C, C] float32 (Stage 2)
+    sigma: np.ndarray     # [N, H, P/C]  float32  (Stage 2)
+    xfinal: np.ndarray    # [N, H, P/C, C] float32 (Stage 2)
+    Y: np.ndarray         # [N, H, P]    float64  (Stage 3)
+    I: np.ndarray         # [N, H, P]    int32    (Stage 3)
+    S: np.ndarray         # [N, H, P]    int32 +-1 (Stage 3)
 
 
 def normalise(x: np.ndarray, C: int, eps) -> tuple:
     """Stages 1 and 2 of Algorithm 1 on float32 pages x[N, H, P].
 
-    Stage 1 (lines 1-4): per channel (row) of a page, gamma_min = min over the
+    Stage 1: per channel (row) of a page, gamma_min = min over the
     P tokens, gamma_scale = max - gamma_min, X <- (X - gamma_min) / (gamma_scale + eps).
-    Stage 2 (lines 5-8): view each row as P/C chunks of C tokens; mu = mean of a
+    Stage 2: view each row as P/C chunks of C tokens; mu = mean of a
     chunk, X_cent = X - mu, sigma = max |X_cent| over the chunk,
     X_final = X_cent / (sigma + eps).
     """
@@ -117,7 +117,7 @@ def normalise(x: np.ndarray, C: int, eps) -> tuple:
 
 
 def quantise(xfinal: np.ndarray, alpha):
-    """Stage 3 (lines 9-12): Y = compander(|X_final|) in float64, I = Round(Y)
+    """Stage 3: Y = compander(|X_final|) in float64, I = Round(Y)
     (half to even), S = -1 where X_final < 0 else +1."""
     xf = np.asarray(xfinal, dtype=np.float32)
     Y = compander(np.abs(xf).astype(np.float64), np.float32(alpha))
@@ -127,12 +127,12 @@ def quantise(xfinal: np.ndarray, alpha):
 
 
 def split_stream(I: np.ndarray, S: np.ndarray):
-    """Stage 4 (lines 13-18) under reading B; returns (Q_anc, Q_res) as int8 in [-8, 7].
+    """Stage 4 under reading B; returns (Q_anc, Q_res) as int8 in [-8, 7].
 
     V_mag   = I >> 4                  anchor magnitude, 0..7
     V_recon = (V_mag << 4) + 7        Round-Half-Down bias at the reconstruction point
     Q_res   = V_recon - I             centred signed correction, -8..7
-    Q_anc   = V_mag * S + min(S, 0)   sign-aware two's-complement map (line 18)
+    Q_anc   = V_mag * S + min(S, 0)   sign-aware two's-complement map
     """
     I = np.asarray(I, dtype=np.int32)
     S = np.asarray(S, dtype=np.int32)
@@ -144,7 +144,7 @@ def split_stream(I: np.ndarray, S: np.ndarray):
 
 
 def split_stream_literal(I, S) -> dict:
-    """Algorithm 1, lines 14-18 exactly as printed (unpacked integers).  Kept
+    """Stage 4 of Algorithm 1 exactly as printed (unpacked integers).  Kept
     for the notes' worked example and to show that the printed anchor needs 18
     levels; the library does not use it."""
     I = np.asarray(I, dtype=np.int32)
@@ -238,7 +238,7 @@ def reconstruct(anchor: np.ndarray, residual, meta: np.ndarray, alpha, eps,
     q_anc = unpack_nibbles(anchor).astype(np.int32)
     N = q_anc.shape[0]
     S = np.where(q_anc < 0, -1, 1)
-    v_mag = np.where(S > 0, q_anc, -q_anc - 1)          # inverse of line 18
+    v_mag = np.where(S > 0, q_anc, -q_anc - 1)          # inverse of the two's-complement map
     idx = (v_mag << 4) + NIBBLE_BIAS
     if residual is not None:
         idx = idx - unpack_nibbles(residual).astype(np.int32)

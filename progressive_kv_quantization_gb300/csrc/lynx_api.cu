@@ -1,0 +1,337 @@
+// C ABI of the Lynx hot path: argument checks, per-(alpha, eps) tables,
+// the device error word, and kernel launches.  See include/lynx.h.
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "lynx_internal.cuh"
+
+namespace lynx {
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(LYNX_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int check_params(const lynx_params_t* p) {
+  if (p == nullptr) return fail(LYNX_ERR_INVALID_ARG, "params is NULL");
+  if (p->H != kH || p->P != kP || p->C != kC)
+    return fail(LYNX_ERR_UNSUPPORTED, "unsupported page shape H=%d P=%d C=%d (need 128, 256, 32)",
+                p->H, p->P, p->C);
+  if (!(p->alpha >= 0.25f && p->alpha <= 1e6f))
+    return fail(LYNX_ERR_UNSUPPORTED, "alpha=%g outside [0.25, 1e6]", (double)p->alpha);
+  if (!(p->eps > 0.0f && p->eps <= 1e-2f))
+    return fail(LYNX_ERR_UNSUPPORTED, "eps=%g outside (0, 1e-2]", (double)p->eps);
+  return LYNX_OK;
+}
+
+double ell(double y, double alpha) {  // inverse compander ((1+alpha)^(y/127) - 1)/alpha
+  return expm1(y / 127.0 * log1p(alpha)) / alpha;
+}
+
+__device__ int g_status;   // per-device error word set by kernels that give up a wait
+
+std::mutex g_dev_mutex;
+int g_sm_count[64];
+int* g_status_ptr[64];
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+}  // namespace
+
+const EncodeTables* encode_tables(float alpha, float eps) {
+  thread_local EncodeTables tab;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  if (alpha == cached_alpha && eps == cached_eps) return &tab;
+  const double a = alpha;
+  tab.thr[0] = 0.0f;
+  for (int k = 1; k <= 127; ++k) {
+    const double x = ell(k - 0.5, a);      // exact edge between codes k-1 and k
+    float f = (float)x;
+    if ((double)f < x) f = nextafterf(f, INFINITY);
+    tab.thr[k] = f;
+  }
+  tab.thr[128] = INFINITY;
+  const double c = 127.0 / log2(1.0 + a);
+  tab.c_lg2 = (float)c;
+  tab.alpha = alpha;
+  tab.eps = eps;
+  // Margin around a rounding edge inside which the code is decided from the
+  // table: far above the error of c * log2(1 + alpha a) evaluated with the
+  // hardware log2 and float32 rounding.
+  tab.edge = (float)(0.5 - (1e-3 + c * ldexp(1.0, -16)));
+  cached_alpha = alpha;
+  cached_eps = eps;
+  return &tab;
+}
+
+const LutTables* lut_tables(float alpha, float eps) {
+  thread_local LutTables lut;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  if (alpha == cached_alpha && eps == cached_eps) return &lut;
+  const double a = alpha;
+  for (int n = 0; n < 16; ++n) {
+    const int q = n >= 8 ? n - 16 : n;           // two's-complement anchor
+    const int S = q < 0 ? -1 : 1;
+    const int V = S > 0 ? q : -q - 1;
+    lut.anc16[n] = (float)(S * ell(16 * V + 7, a));
+  }
+  for (int c = 0; c < 256; ++c) {
+    const int na = c & 15, nr = c >> 4;
+    const int qa = na >= 8 ? na - 16 : na;
+    const int qr = nr >= 8 ? nr - 16 : nr;
+    const int S = qa < 0 ? -1 : 1;
+    const int V = S > 0 ? qa : -qa - 1;
+    lut.full[c] = (float)(S * ell(16 * V + 7 - qr, a));
+  }
+  for (int byte = 0; byte < 256; ++byte)
+    lut.anc_pair[byte] = make_float2(lut.anc16[byte & 15], lut.anc16[byte >> 4]);
+  lut.eps = eps;
+  cached_alpha = alpha;
+  cached_eps = eps;
+  return &lut;
+}
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n > 0 ? n : 1;
+  }
+  return g_sm_count[dev];
+}
+
+int* device_status_ptr() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace lynx
+
+using namespace lynx;
+
+extern "C" {
+
+int lynx_version(void) { return 100; }
+
+const char* lynx_last_error(void) { return g_last_error; }
+
+const char* lynx_status_string(int status) {
+  switch (status) {
+    case LYNX_OK: return "LYNX_OK";
+    case LYNX_ERR_INVALID_ARG: return "LYNX_ERR_INVALID_ARG";
+    case LYNX_ERR_UNSUPPORTED: return "LYNX_ERR_UNSUPPORTED";
+    case LYNX_ERR_ALIGNMENT: return "LYNX_ERR_ALIGNMENT";
+    case LYNX_ERR_WORKSPACE: return "LYNX_ERR_WORKSPACE";
+    case LYNX_ERR_CUDA: return "LYNX_ERR_CUDA";
+    case LYNX_ERR_DEVICE: return "LYNX_ERR_DEVICE";
+    default: return "LYNX_ERR_UNKNOWN";
+  }
+}
+
+int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
+                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!x_bf16 || !anchor || !residual || !meta)
+    return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(x_bf16) || misaligned(anchor) || misaligned(residual) || misaligned(meta))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  const EncodeTables* tab = encode_tables(params->alpha, params->eps);
+  cudaError_t e = launch_encode(x_bf16, n_pages, anchor, residual, meta, tab,
+                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_pages launch");
+  return LYNX_OK;
+}
+
+int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
+                     int64_t n_pages, const lynx_params_t* params, void* out, int out_dtype,
+                     void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_F32)
+    return fail(LYNX_ERR_INVALID_ARG, "out_dtype=%d (need 0 = BF16 or 1 = F32)", out_dtype);
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!anchor || !meta || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(anchor) || (residual && misaligned(residual)) || misaligned(meta) || misaligned(out))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  const LutTables* lut = lut_tables(params->alpha, params->eps);
+  cudaError_t e = launch_reconstruct(anchor, residual, meta, n_pages, out, out_dtype, lut,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct launch");
+  return LYNX_OK;
+}
+
+namespace {
+
+int check_decode_shape(int B, int T, int Hq, int Hkv, int head_dim, int max_pages) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || max_pages < 1)
+    return fail(LYNX_ERR_INVALID_ARG, "B=%d T=%d Hq=%d Hkv=%d max_pages=%d must be >= 1", B, T, Hq,
+                Hkv, max_pages);
+  if (head_dim != kH) return fail(LYNX_ERR_UNSUPPORTED, "head_dim=%d (need 128)", head_dim);
+  if (T > 32) return fail(LYNX_ERR_UNSUPPORTED, "T=%d > 32", T);
+  if (Hq % Hkv != 0) return fail(LYNX_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  const int G = Hq / Hkv;
+  if (T * G > 256) return fail(LYNX_ERR_UNSUPPORTED, "T*Hq/Hkv=%d > 256", T * G);
+  const int n_rg = (T * G + 3) / 4;
+  if (B > 65535 || (int64_t)Hkv * n_rg > 65535)
+    return fail(LYNX_ERR_UNSUPPORTED, "grid too large (B=%d, Hkv*row_groups=%lld)", B,
+                (long long)Hkv * n_rg);
+  if ((int64_t)max_pages * kP > 0x7fffffff) return fail(LYNX_ERR_UNSUPPORTED, "max_pages too large");
+  return LYNX_OK;
+}
+
+int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, int Hkv,
+                  int head_dim, int64_t n_pool, const int32_t* page_table, int max_pages,
+                  const int32_t* ctx_len, float sm_scale, int causal, float* out, float* lse,
+                  void* workspace, size_t ws_bytes, float alpha, float eps, void* stream) {
+  int st = check_decode_shape(B, T, Hq, Hkv, head_dim, max_pages);
+  if (st != LYNX_OK) return st;
+  if (!q || !page_table || !ctx_len || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (n_pool < 1) return fail(LYNX_ERR_INVALID_ARG, "n_pool_pages=%lld < 1", (long long)n_pool);
+  if (misaligned(q) || misaligned(page_table) || misaligned(ctx_len) || misaligned(out) ||
+      (lse && misaligned(lse)) || (workspace && misaligned(workspace)))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (causal != 0 && causal != 1) return fail(LYNX_ERR_INVALID_ARG, "causal=%d", causal);
+  if (!(sm_scale > 0.0f) || !isfinite(sm_scale))
+    return fail(LYNX_ERR_INVALID_ARG, "sm_scale=%g must be finite and > 0", (double)sm_scale);
+  const DecodePlan pl = plan_decode(B, T, Hq, Hkv, max_pages, mode);
+  if (workspace == nullptr || ws_bytes < pl.ws_bytes)
+    return fail(LYNX_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.ws_bytes,
+                workspace ? ws_bytes : (size_t)0);
+  int* status = device_status_ptr();
+  if (!status) return fail(LYNX_ERR_CUDA, "cannot resolve the device status word");
+  a.q = static_cast<const uint16_t*>(q);
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.out = out;
+  a.lse = lse;
+  a.ws = static_cast<float*>(workspace);
+  a.status = status;
+  a.n_pool = n_pool;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.max_pages = max_pages;
+  a.n_rg = pl.n_rg;
+  a.n_splits = pl.n_splits;
+  a.pages_per_split = pl.pages_per_split;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.causal = causal;
+  a.eps = eps;
+  const LutTables* lut = lut_tables(alpha, eps);
+  cudaError_t e = launch_decode(a, mode, lut, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_decode_attn launch");
+  return LYNX_OK;
+}
+
+}  // namespace
+
+size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages) {
+  if (check_decode_shape(B, T, Hq, Hkv, head_dim, max_pages) != LYNX_OK) return 0;
+  return plan_decode(B, T, Hq, Hkv, max_pages, kModeAnchor).ws_bytes;
+}
+
+int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                     const uint8_t* k_anc, const uint8_t* k_res, const float* k_meta,
+                     const uint8_t* v_anc, const uint8_t* v_res, const float* v_meta,
+                     int64_t n_pool_pages, const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len, const lynx_params_t* params, float sm_scale,
+                     int causal, float* out, float* lse, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (!k_anc || !k_meta || !v_anc || !v_meta) return fail(LYNX_ERR_INVALID_ARG, "NULL page pool");
+  if ((k_res == nullptr) != (v_res == nullptr))
+    return fail(LYNX_ERR_INVALID_ARG, "k_res and v_res must both be NULL or both be set");
+  if (misaligned(k_anc) || misaligned(k_meta) || misaligned(v_anc) || misaligned(v_meta) ||
+      (k_res && misaligned(k_res)) || (v_res && misaligned(v_res)))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.k_anc = k_anc;
+  a.k_res = k_res;
+  a.k_meta = k_meta;
+  a.v_anc = v_anc;
+  a.v_res = v_res;
+  a.v_meta = v_meta;
+  const int mode = k_res ? kModeFull : kModeAnchor;
+  return decode_common(a, mode, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table,
+                       max_pages, ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes,
+                       params->alpha, params->eps, stream);
+}
+
+int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                          const void* k_pages, const void* v_pages, int64_t n_pool_pages,
+                          const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                          float sm_scale, int causal, float* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  g_last_error[0] = '\0';
+  if (!k_pages || !v_pages) return fail(LYNX_ERR_INVALID_ARG, "NULL page pool");
+  if (misaligned(k_pages) || misaligned(v_pages))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.k_bf16 = static_cast<const uint16_t*>(k_pages);
+  a.v_bf16 = static_cast<const uint16_t*>(v_pages);
+  return decode_common(a, kModeBf16, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table,
+                       max_pages, ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes,
+                       100.0f, 1e-6f, stream);
+}
+
+int lynx_device_status(void) {
+  g_last_error[0] = '\0';
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_device_status synchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_device_status read");
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    return fail(LYNX_ERR_DEVICE, "device error word = %d (1: a bounded wait gave up, "
+                "2: page id outside the pool, 3: ctx_len outside 0..max_pages*256)", v);
+  }
+  return LYNX_OK;
+}
+
+}  // extern "C"

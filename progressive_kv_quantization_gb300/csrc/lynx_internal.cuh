@@ -1,0 +1,95 @@
+// Internal definitions shared by the Lynx CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lynx.h"
+
+namespace lynx {
+
+// Page geometry (H channels x P tokens, C-token chunks).
+constexpr int kH = 128;
+constexpr int kP = 256;
+constexpr int kC = 32;
+constexpr int kChunks = kP / kC;                       // 8
+constexpr int kPageElems = kH * kP;                    // 32768
+constexpr int kPlaneBytes = kH * kP / 2;               // 16384: one 4-bit plane
+constexpr int kMetaFloats = 2 * kH + 2 * kH * kChunks; // 2304
+constexpr int kMetaBytes = kMetaFloats * 4;            // 9216
+constexpr int kMetaMuOff = 2 * kH;                     // mu[128][8] starts here
+constexpr int kMetaSigmaOff = 2 * kH + kH * kChunks;   // sigma[128][8]
+
+// Quantiser tables for one (alpha, eps).  thr[k] (k = 1..127) is the smallest
+// float32 f with 127 ln(1 + alpha f)/ln(1 + alpha) >= k - 1/2, so that for a
+// float32 magnitude a the rounded code is #{k : a >= thr[k]}.  thr[0] = 0 and
+// thr[128] = +inf bracket the search.
+struct EncodeTables {
+  float thr[129];
+  float c_lg2;     // 127 / log2(1 + alpha)
+  float alpha;
+  float eps;
+  float edge;      // |y - rint(y)| above which the code is decided from thr[]
+};
+
+// Dequantisation tables: signed inverse-compander values S * l(I_hat),
+// rounded to float32.
+struct LutTables {
+  float2 anc_pair[256];  // anchor byte -> (value of low nibble, value of high nibble)
+  float full[256];       // (anchor nibble | residual nibble << 4) -> value
+  float anc16[16];       // anchor nibble -> value
+  float eps;
+};
+
+const EncodeTables* encode_tables(float alpha, float eps);
+const LutTables* lut_tables(float alpha, float eps);
+
+int device_sm_count();
+int* device_status_ptr();   // device address of this device's error word
+
+// Launchers (one per kernel family).  Return cudaGetLastError() of the launch.
+cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
+                          float* meta, const EncodeTables* tab, cudaStream_t s);
+cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
+                               int64_t n_pages, void* out, int out_dtype, const LutTables* lut,
+                               cudaStream_t s);
+
+enum DecodeMode { kModeAnchor = 0, kModeFull = 1, kModeBf16 = 2 };
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint8_t* k_anc;
+  const uint8_t* k_res;
+  const float* k_meta;
+  const uint8_t* v_anc;
+  const uint8_t* v_res;
+  const float* v_meta;
+  const uint16_t* k_bf16;
+  const uint16_t* v_bf16;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  float* out;
+  float* lse;
+  float* ws;
+  int* status;
+  int64_t n_pool;        // pages in each pool (valid page ids are 0 .. n_pool-1)
+  int B, T, Hq, Hkv, G, max_pages;
+  int n_rg;              // row groups of 4 query rows per (sequence, KV head)
+  int n_splits;
+  int pages_per_split;
+  float scale_log2;      // sm_scale * log2(e)
+  int causal;
+  float eps;
+};
+
+struct DecodePlan {
+  int n_rg;
+  int n_splits;
+  int pages_per_split;
+  size_t ws_bytes;
+};
+
+DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode);
+cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);
+
+}  // namespace lynx

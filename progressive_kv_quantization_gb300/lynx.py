@@ -1,0 +1,210 @@
+"""Thin Python binding of the Lynx C ABI (include/lynx.h).
+
+Argument marshalling only: every function checks tensor types, allocates the
+outputs the caller did not pass (torch device memory), and calls the entry
+point of the same name in ``_build/liblynx.so`` on the current CUDA stream.
+There is no fallback: if the library is missing or a call fails, a
+``LynxError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblynx.so")
+
+H, P, C = 128, 256, 32
+PLANE_BYTES = H * P // 2
+META_FLOATS = 2 * H + 2 * H * (P // C)
+OUT_BF16, OUT_F32 = 0, 1
+
+
+class LynxError(RuntimeError):
+    pass
+
+
+class lynx_params_t(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("P", ctypes.c_int32), ("C", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+@dataclass(frozen=True)
+class Params:
+    alpha: float = 100.0
+    eps: float = 1e-6
+    H: int = H
+    P: int = P
+    C: int = C
+
+    def c(self) -> lynx_params_t:
+        return lynx_params_t(self.H, self.P, self.C, self.alpha, self.eps)
+
+
+_lib = None
+
+# (name, restype, argtypes) of every exported entry point
+_VP, _I64, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_PP = ctypes.POINTER(lynx_params_t)
+SIGNATURES = {
+    "lynx_encode_pages": (_I32, [_VP, _I64, _PP, _VP, _VP, _VP, _VP]),
+    "lynx_reconstruct": (_I32, [_VP, _VP, _VP, _I64, _PP, _VP, _I32, _VP]),
+    "lynx_decode_attn": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "lynx_decode_attn_bf16": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I64, _VP, _I32,
+                                     _VP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "lynx_decode_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "lynx_device_status": (_I32, []),
+    "lynx_status_string": (ctypes.c_char_p, [_I32]),
+    "lynx_last_error": (ctypes.c_char_p, []),
+    "lynx_version": (_I32, []),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load liblynx.so (built by ``progressive_kv_quantization_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise LynxError(f"{path} is missing: build the CUDA library first "
+                        "(python -m progressive_kv_quantization_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        lib = load()
+        raise LynxError(f"{what}: {lib.lynx_status_string(status).decode()} "
+                        f"({lib.lynx_last_error().decode()})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, device=None):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_contiguous():
+        raise LynxError(f"{name} must be a contiguous {dtype} tensor")
+    if not t.is_cuda:
+        raise LynxError(f"{name} must live on a CUDA device")
+
+
+def lynx_encode_pages(x, params: Params = Params(), anchor=None, residual=None, meta=None,
+                      stream=None):
+    """Algorithm 1 on BF16 pages x[N, 128, 256] -> (anchor u8[N,128,128],
+    residual u8[N,128,128], meta f32[N, 2304])."""
+    _need(x, torch.bfloat16, "x")
+    n = x.numel() // (H * P)
+    if x.numel() != n * H * P:
+        raise LynxError("x must hold whole 128 x 256 pages")
+    dev = x.device
+    anchor = anchor if anchor is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=dev)
+    residual = residual if residual is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=dev)
+    meta = meta if meta is not None else torch.empty((n, META_FLOATS), dtype=torch.float32, device=dev)
+    for t, nm in ((anchor, "anchor"), (residual, "residual")):
+        _need(t, torch.uint8, nm)
+    _need(meta, torch.float32, "meta")
+    if anchor.numel() < n * PLANE_BYTES or residual.numel() < n * PLANE_BYTES or meta.numel() < n * META_FLOATS:
+        raise LynxError("output buffers too small")
+    p = params.c()
+    _check(load().lynx_encode_pages(_ptr(x), n, ctypes.byref(p), _ptr(anchor), _ptr(residual),
+                                    _ptr(meta), _stream(stream)), "lynx_encode_pages")
+    return anchor, residual, meta
+
+
+def lynx_reconstruct(anchor, residual, meta, params: Params = Params(), out=None,
+                     out_dtype=torch.bfloat16, stream=None):
+    """Anchor-only (residual=None) or full reconstruction -> out[N, 128, 256]."""
+    _need(anchor, torch.uint8, "anchor")
+    if residual is not None:
+        _need(residual, torch.uint8, "residual")
+    _need(meta, torch.float32, "meta")
+    n = anchor.numel() // PLANE_BYTES
+    code = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}.get(out_dtype)
+    if code is None:
+        raise LynxError("out_dtype must be torch.bfloat16 or torch.float32")
+    out = out if out is not None else torch.empty((n, H, P), dtype=out_dtype, device=anchor.device)
+    _need(out, out_dtype, "out")
+    p = params.c()
+    _check(load().lynx_reconstruct(_ptr(anchor), _ptr(residual), _ptr(meta), n, ctypes.byref(p),
+                                   _ptr(out), code, _stream(stream)), "lynx_reconstruct")
+    return out
+
+
+def lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages) -> int:
+    return int(load().lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages))
+
+
+def _decode_prep(q, page_table, ctx_len, n_kv_heads, out, lse, workspace):
+    _need(q, torch.bfloat16, "q")
+    if q.dim() != 4:
+        raise LynxError("q must be [B, T, Hq, 128]")
+    B, T, Hq, D = q.shape
+    _need(page_table, torch.int32, "page_table")
+    _need(ctx_len, torch.int32, "ctx_len")
+    if page_table.dim() != 3 or page_table.shape[0] != B or page_table.shape[1] != n_kv_heads:
+        raise LynxError("page_table must be [B, Hkv, max_pages]")
+    max_pages = page_table.shape[2]
+    dev = q.device
+    out = out if out is not None else torch.empty((B, T, Hq, D), dtype=torch.float32, device=dev)
+    lse = lse if lse is not None else torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+    _need(out, torch.float32, "out")
+    ws_bytes = lynx_decode_attn_workspace_size(B, T, Hq, n_kv_heads, D, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    return B, T, Hq, D, max_pages, out, lse, workspace
+
+
+def lynx_decode_attn(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page_table, ctx_len,
+                     n_kv_heads, params: Params = Params(), sm_scale=None, causal=False,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Attention of q[B, T, Hq, 128] over packed K/V page pools (k_res = v_res =
+    None: anchor-only draft KV).  Returns (out f32[B,T,Hq,128], lse f32[B,T,Hq])."""
+    B, T, Hq, D, max_pages, out, lse, workspace = _decode_prep(q, page_table, ctx_len, n_kv_heads,
+                                                               out, lse, workspace)
+    n_pool = k_anc.numel() // PLANE_BYTES
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
+    p = params.c()
+    _check(load().lynx_decode_attn(
+        _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_anc), _ptr(k_res), _ptr(k_meta), _ptr(v_anc),
+        _ptr(v_res), _ptr(v_meta), n_pool, _ptr(page_table), max_pages, _ptr(ctx_len),
+        ctypes.byref(p), scale, int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_decode_attn")
+    return out, lse
+
+
+def lynx_decode_attn_bf16(q, k_pages, v_pages, page_table, ctx_len, n_kv_heads, sm_scale=None,
+                          causal=False, out=None, lse=None, workspace=None, stream=None):
+    """The same attention over BF16 page pools k_pages/v_pages[n, 128, 256]."""
+    B, T, Hq, D, max_pages, out, lse, workspace = _decode_prep(q, page_table, ctx_len, n_kv_heads,
+                                                               out, lse, workspace)
+    _need(k_pages, torch.bfloat16, "k_pages")
+    _need(v_pages, torch.bfloat16, "v_pages")
+    n_pool = k_pages.numel() // (H * P)
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
+    _check(load().lynx_decode_attn_bf16(
+        _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_pages), _ptr(v_pages), n_pool, _ptr(page_table),
+        max_pages, _ptr(ctx_len), scale, int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_decode_attn_bf16")
+    return out, lse
+
+
+def lynx_device_status():
+    """Raise if a kernel recorded an error (synchronises the device)."""
+    _check(load().lynx_device_status(), "lynx_device_status")

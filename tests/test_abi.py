@@ -1,0 +1,86 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point include/lynx.h declares, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from progressive_kv_quantization_gb300 import lynx as L
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lynx.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lynx_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("lynx_encode_pages", "lynx_reconstruct", "lynx_decode_attn"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lynx_lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lynx_lib, n), f"{n} declared in lynx.h but not exported"
+        assert n in L.SIGNATURES, f"{n} has no binding signature"
+
+
+def _p(**kw):
+    d = dict(H=128, P=256, C=32, alpha=100.0, eps=1e-6)
+    d.update(kw)
+    return L.lynx_params_t(d["H"], d["P"], d["C"], d["alpha"], d["eps"])
+
+
+def test_encode_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    aligned = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(aligned.value + 1)
+    ok = _p()
+    assert lib.lynx_encode_pages(aligned, 1, None, aligned, aligned, aligned, None) == -1
+    assert lib.lynx_encode_pages(aligned, 1, ctypes.byref(_p(H=64)), aligned, aligned, aligned, None) == -2
+    assert lib.lynx_encode_pages(aligned, 1, ctypes.byref(_p(C=16)), aligned, aligned, aligned, None) == -2
+    assert lib.lynx_encode_pages(aligned, 1, ctypes.byref(_p(alpha=0.0)), aligned, aligned, aligned, None) == -2
+    assert lib.lynx_encode_pages(aligned, 1, ctypes.byref(_p(eps=0.0)), aligned, aligned, aligned, None) == -2
+    assert lib.lynx_encode_pages(aligned, -1, ctypes.byref(ok), aligned, aligned, aligned, None) == -1
+    assert lib.lynx_encode_pages(None, 1, ctypes.byref(ok), aligned, aligned, aligned, None) == -1
+    assert lib.lynx_encode_pages(odd, 1, ctypes.byref(ok), aligned, aligned, aligned, None) == -3
+    assert lib.lynx_encode_pages(None, 0, ctypes.byref(ok), None, None, None, None) == 0
+    assert b"16-byte" in (lib.lynx_encode_pages(odd, 1, ctypes.byref(ok), aligned, aligned, aligned, None)
+                          and lib.lynx_last_error())
+
+
+def test_reconstruct_and_decode_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    ok = ctypes.byref(_p())
+    assert lib.lynx_reconstruct(a, None, a, 1, ok, a, 7, None) == -1
+    assert lib.lynx_reconstruct(a, None, a, 0, ok, a, 0, None) == 0
+    # decode: T > 32, Hq not a multiple of Hkv, head_dim != 128, mixed residual pools
+    args = lambda **kw: dict(dict(q=a, B=1, T=1, Hq=32, Hkv=8, D=128, kr=None, vr=None,
+                                  ws=a, wsb=0), **kw)
+
+    def call(**kw):
+        x = args(**kw)
+        return lib.lynx_decode_attn(x["q"], x["B"], x["T"], x["Hq"], x["Hkv"], x["D"], a, x["kr"], a,
+                                    a, x["vr"], a, 4, a, 4, a, ok, 0.088, 0, a, a, x["ws"], x["wsb"], None)
+    assert call(T=33) == -2
+    assert call(Hq=30) == -1
+    assert call(D=64) == -2
+    assert call(kr=a) == -1
+    assert call(ws=None) == -4
+    assert lib.lynx_decode_attn_workspace_size(1, 1, 32, 8, 128, 64) > 0
+    assert lib.lynx_decode_attn_workspace_size(1, 40, 32, 8, 128, 64) == 0
+
+
+def test_status_strings(lynx_lib):
+    for code, name in ((0, b"LYNX_OK"), (-3, b"LYNX_ERR_ALIGNMENT"), (-6, b"LYNX_ERR_DEVICE")):
+        assert lynx_lib.lynx_status_string(code) == name
+    assert lynx_lib.lynx_version() >= 100

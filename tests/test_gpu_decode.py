@@ -1,0 +1,230 @@
+"""GPU parity of lynx_decode_attn / lynx_decode_attn_bf16 against the float64
+attention oracle over the oracle's own dequantised KV.
+
+The page pools fed to the GPU are the oracle's encoding of seeded BF16 pages
+(inputs flow oracle -> GPU only), so the comparison isolates the attention
+kernel.  Bar: |gpu - oracle| <= 2e-3 * max(1, |oracle|) for outputs and
+log-sum-exps.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as at
+from oracle import lynx_oracle as lo
+from progressive_kv_quantization_gb300 import inputs
+from progressive_kv_quantization_gb300 import lynx as L
+
+from lynx_testutil import EPS, check_attention, check_codes
+
+pytestmark = pytest.mark.gpu
+
+
+class Pools:
+    """K and V page pools encoded by the oracle, plus their dequantised float64
+    copies (anchor-only and full) and the BF16 originals."""
+
+    def __init__(self, n_heads, n_tokens, seed, alpha=100.0):
+        out = inputs.outlier_pairs(n_heads, seed)
+        self.alpha = alpha
+        self.kb = inputs.kv_pages_np(n_heads, n_tokens, seed * 10 + 1, out)
+        self.vb = inputs.kv_pages_np(n_heads, n_tokens, seed * 10 + 2, out)
+        self.n = self.kb.shape[0]
+        self.enc = {}
+        self.deq = {}
+        for name, bits in (("k", self.kb), ("v", self.vb)):
+            a, r, m = lo.encode_pages(bits, alpha, EPS)
+            self.enc[name] = (a, r, m)
+            self.deq[(name, "anchor")] = lo.reconstruct(a, None, m, alpha, EPS)
+            self.deq[(name, "full")] = lo.reconstruct(a, r, m, alpha, EPS)
+            self.deq[(name, "bf16")] = lo.bf16_to_f32(bits).astype(np.float64)
+        self.dev = {name: tuple(torch.from_numpy(t).cuda() for t in self.enc[name]) for name in ("k", "v")}
+        self.dev_bf16 = {name: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+                         for name, b in (("k", self.kb), ("v", self.vb))}
+
+    def fetch(self, mode):
+        return lambda ids: (self.deq[("k", mode)][ids], self.deq[("v", mode)][ids])
+
+
+def run(pools, mode, q_bits, table, ctx, Hkv, causal, scale=None):
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    pt = torch.from_numpy(table.astype(np.int32)).cuda()
+    cl = torch.from_numpy(ctx.astype(np.int32)).cuda()
+    if mode == "bf16":
+        o, lse = L.lynx_decode_attn_bf16(q, pools.dev_bf16["k"], pools.dev_bf16["v"], pt, cl, Hkv,
+                                         sm_scale=scale, causal=causal)
+    else:
+        ka, kr, km = pools.dev["k"]
+        va, vr, vm = pools.dev["v"]
+        full = mode == "full"
+        o, lse = L.lynx_decode_attn(q, ka, kr if full else None, km, va, vr if full else None, vm,
+                                    pt, cl, Hkv, L.Params(alpha=pools.alpha), sm_scale=scale,
+                                    causal=causal)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    return o.cpu().numpy(), lse.cpu().numpy()
+
+
+def reference(pools, mode, q_bits, table, ctx, Hkv, causal, scale=None, **kw):
+    q = lo.bf16_to_f32(q_bits).astype(np.float64)
+    s = scale if scale is not None else 1.0 / math.sqrt(128)
+    return at.decode_attention(q, pools.fetch(mode), table, ctx, Hkv, s, causal, **kw)
+
+
+def contiguous_table(B, Hkv, pages_per_head, pool_pages_per_head, offset=0):
+    t = np.zeros((B, Hkv, pages_per_head), dtype=np.int32)
+    for b in range(B):
+        for h in range(Hkv):
+            t[b, h] = (offset + h * pool_pages_per_head + np.arange(pages_per_head)) % (Hkv * pool_pages_per_head)
+    return t
+
+
+@pytest.fixture(scope="module")
+def llama_pools():
+    return Pools(8, 16384, 1)
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full", "bf16"])
+def test_llama8b_layer_draft_decode(cuda_device, llama_pools, mode):
+    """1-token decode, B=1, 8 KV heads, 32 query heads (GQA 4:1), 16,384 tokens."""
+    B, T, Hq, Hkv = 1, 1, 32, 8
+    table = contiguous_table(B, Hkv, 64, 64)
+    ctx = np.array([16384])
+    q = inputs.queries_np((B, T, Hq, 128), 7)
+    o, lse = run(llama_pools, mode, q, table, ctx, Hkv, False)
+    ro, rl = reference(llama_pools, mode, q, table, ctx, Hkv, False)
+    check_attention(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full", "bf16"])
+@pytest.mark.parametrize("T", [4, 8, 32])
+def test_verification_causal_ragged_batch(cuda_device, llama_pools, mode, T):
+    """T-token causal verification over sequences of different, ragged lengths."""
+    B, Hq, Hkv = 3, 32, 8
+    ctx = np.array([16384, 5000, 300])
+    table = np.stack([contiguous_table(1, Hkv, 64, 64, offset=17 * b)[0] for b in range(B)])
+    q = inputs.queries_np((B, T, Hq, 128), 100 + T)
+    o, lse = run(llama_pools, mode, q, table, ctx, Hkv, True)
+    ro, rl = reference(llama_pools, mode, q, table, ctx, Hkv, True)
+    check_attention(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full", "bf16"])
+def test_odd_group_sizes_and_tiny_contexts(cuda_device, llama_pools, mode):
+    """G = 3 query heads per KV head (rows not a multiple of 4), T = 3; contexts
+    of 1 key, T keys (the first causal row sees a single key) and 0 keys."""
+    B, T, Hkv = 4, 3, 2
+    Hq = 3 * Hkv
+    ctx = np.array([1, 3, 257, 0])
+    table = np.stack([contiguous_table(1, Hkv, 2, 64, offset=5 * b)[0] for b in range(B)])
+    q = inputs.queries_np((B, T, Hq, 128), 55)
+    for causal in (False, True):
+        o, lse = run(llama_pools, mode, q, table, ctx, Hkv, causal)
+        ro, rl = reference(llama_pools, mode, q, table, np.maximum(ctx, 0), Hkv, causal)
+        empty = np.isnan(ro[..., 0])          # rows with no visible key
+        assert np.all(o[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
+        check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
+
+
+def test_scale_and_shared_pages(cuda_device, llama_pools):
+    """Eight sequences whose page tables point at overlapping pages (as eight
+    sequences realised over a multi-layer cache), with a non-default scale."""
+    B, T, Hq, Hkv = 8, 1, 32, 8
+    table = np.stack([contiguous_table(1, Hkv, 32, 64, offset=4 * b)[0] for b in range(B)])
+    ctx = np.full(B, 32 * 256)
+    q = inputs.queries_np((B, T, Hq, 128), 9)
+    o, lse = run(llama_pools, "anchor", q, table, ctx, Hkv, False, scale=0.05)
+    ro, rl = reference(llama_pools, "anchor", q, table, ctx, Hkv, False, scale=0.05)
+    check_attention(o, lse, ro, rl)
+
+
+def test_invalid_page_id_and_context_are_reported(cuda_device, llama_pools):
+    """Out-of-pool page ids and out-of-range context lengths are not dereferenced:
+    the kernel reads page 0 / clamps and sets the device error word."""
+    B, T, Hq, Hkv = 1, 1, 32, 8
+    table = contiguous_table(B, Hkv, 4, 64)
+    table[0, 3, 1] = 10 ** 6
+    q = inputs.queries_np((B, T, Hq, 128), 3)
+    with pytest.raises(L.LynxError, match="error word = 2"):
+        run(llama_pools, "anchor", q, table, np.array([1024]), Hkv, False)
+    with pytest.raises(L.LynxError, match="error word = 3"):
+        run(llama_pools, "anchor", q, contiguous_table(B, Hkv, 4, 64), np.array([5000]), Hkv, False)
+    L.lynx_device_status()     # cleared by the previous read
+
+
+def test_end_to_end_encode_then_decode(cuda_device):
+    """GPU encode followed by GPU decode over the GPU's own planes, against the
+    oracle's encode + reconstruct + attention of the same BF16 pages."""
+    Hkv, Hq, n_tok = 4, 16, 4096
+    out = inputs.outlier_pairs(Hkv, 4)
+    kb = inputs.kv_pages_np(Hkv, n_tok, 41, out)
+    vb = inputs.kv_pages_np(Hkv, n_tok, 42, out)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+    ka, kr, km = L.lynx_encode_pages(dev(kb))
+    va, vr, vm = L.lynx_encode_pages(dev(vb))
+    oka, okr, okm, kst = lo.encode_pages(kb, 100.0, EPS, return_stages=True)
+    ova, ovr, ovm, vst = lo.encode_pages(vb, 100.0, EPS, return_stages=True)
+    check_codes(ka.cpu().numpy(), kr.cpu().numpy(), oka, okr, kst.Y)
+    check_codes(va.cpu().numpy(), vr.cpu().numpy(), ova, ovr, vst.Y)
+    T = 8
+    table = contiguous_table(1, Hkv, 16, 16)
+    ctx = np.array([n_tok])
+    qb = inputs.queries_np((1, T, Hq, 128), 77)
+    q = dev(qb)
+    pt = torch.from_numpy(table).cuda()
+    cl = torch.from_numpy(ctx.astype(np.int32)).cuda()
+    for full in (False, True):
+        o, lse = L.lynx_decode_attn(q, ka, kr if full else None, km, va, vr if full else None, vm, pt, cl, Hkv,
+                                    causal=True)
+        kd = lo.reconstruct(oka, okr if full else None, okm, 100.0, EPS)
+        vd = lo.reconstruct(ova, ovr if full else None, ovm, 100.0, EPS)
+        ro, rl = at.decode_attention(lo.bf16_to_f32(qb).astype(np.float64), lambda ids: (kd[ids], vd[ids]),
+                                     table, ctx, Hkv, 1 / math.sqrt(128), True)
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
+
+
+@pytest.mark.slow
+def test_qwen235b_layers_full_context_sampled(cuda_device):
+    """Qwen3-235B-A22B-shaped layers at the full 131,072-token context (4 KV
+    heads, 16 query heads): GPU encode of the layer's K and V, anchor-only
+    decode over the whole context; two query heads of every KV head are checked
+    against the oracle (which re-encodes the same BF16 pages)."""
+    w = inputs.QWEN235B_CACHE
+    outl = inputs.outlier_pairs(w.n_kv_heads, 0)
+    Hkv, Hq = w.n_kv_heads, w.n_q_heads
+    for layer in (0, 93):
+        k = inputs.kv_pages_torch(Hkv, w.n_tokens, inputs.layer_seed(0, layer, 0), outl, "cuda")
+        v = inputs.kv_pages_torch(Hkv, w.n_tokens, inputs.layer_seed(0, layer, 1), outl, "cuda")
+        ka, kr, km = L.lynx_encode_pages(k)
+        va, vr, vm = L.lynx_encode_pages(v)
+        npph = w.pages_per_head
+        table = contiguous_table(1, Hkv, npph, npph)
+        ctx = np.array([w.n_tokens])
+        qb = inputs.queries_np((1, 1, Hq, 128), 500 + layer)
+        q = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).cuda()
+        o, lse = L.lynx_decode_attn(q, ka, None, km, va, None, vm, torch.from_numpy(table).cuda(),
+                                    torch.from_numpy(ctx.astype(np.int32)).cuda(), Hkv)
+        torch.cuda.synchronize()
+        L.lynx_device_status()
+        kbits = k.view(torch.int16).cpu().numpy().view(np.uint16)
+        vbits = v.view(torch.int16).cpu().numpy().view(np.uint16)
+        heads = [0, 5, 10, 15]
+        cache = {}
+
+        def fetch(ids):
+            key = int(ids[0])
+            if key not in cache:
+                oa, _, om = lo.encode_pages(kbits[ids], 100.0, EPS)
+                ova, _, ovm = lo.encode_pages(vbits[ids], 100.0, EPS)
+                cache[key] = (lo.reconstruct(oa, None, om, 100.0, EPS), lo.reconstruct(ova, None, ovm, 100.0, EPS))
+            return cache[key]
+        ro, rl = at.decode_attention(lo.bf16_to_f32(qb).astype(np.float64), fetch, table, ctx, Hkv,
+                                     1 / math.sqrt(128), False, q_heads=heads)
+        sel = np.zeros(o.shape[:3], dtype=bool)
+        sel[:, :, heads] = True
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), np.nan_to_num(ro), np.nan_to_num(rl, nan=0.0),
+                        mask=sel)
+        del k, v, ka, kr, km, va, vr, vm
+        torch.cuda.empty_cache()

@@ -1,0 +1,159 @@
+"""GPU parity of lynx_encode_pages and lynx_reconstruct against the CPU oracle.
+
+Inputs are seeded BF16 pages; the oracle encodes the same bits on the CPU.
+Codes: bit-exact except +-1 within 1e-5 of a rounding edge (fraction < 1e-4).
+Metadata: within 1e-6 relative.  Reconstruction (fed with the oracle's own
+planes): within the float32 error bound of the float64 value, plus half a BF16
+ulp for BF16 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import lynx_oracle as lo
+from progressive_kv_quantization_gb300 import inputs
+from progressive_kv_quantization_gb300 import lynx as L
+
+from lynx_testutil import EPS, check_codes, check_meta, check_recon, recon_bound
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(bits: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def encode_and_compare(bits, alpha=100.0):
+    x = to_dev(bits)
+    a, r, m = L.lynx_encode_pages(x, L.Params(alpha=alpha))
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    oa, orr, om, st = lo.encode_pages(bits, alpha, EPS, return_stages=True)
+    frac = check_codes(a.cpu().numpy(), r.cpu().numpy(), oa, orr, st.Y)
+    exact = check_meta(m.cpu().numpy(), om)
+    return frac, exact
+
+
+@pytest.mark.parametrize("alpha", [100.0, 255.0])
+def test_single_page(cuda_device, alpha):
+    bits = inputs.kv_pages_np(1, 256, 0, inputs.outlier_pairs(1, 0, count=4))
+    frac, exact = encode_and_compare(bits, alpha)
+    assert exact == 1.0          # same IEEE float32 steps on both sides
+
+
+def test_llama8b_layer_k_and_v(cuda_device):
+    out = inputs.outlier_pairs(8, 0)
+    k = inputs.kv_pages_np(8, 16384, 1, out)
+    v = inputs.kv_pages_np(8, 16384, 2, out)
+    bits = np.concatenate([k, v])
+    assert bits.shape == (1024, 128, 256)
+    frac, exact = encode_and_compare(bits)
+    assert exact == 1.0
+
+
+@pytest.mark.parametrize("n_pages", [1, 3, 37, 301])
+def test_ragged_page_counts(cuda_device, n_pages):
+    bits = inputs.kv_pages_np(1, 256 * n_pages, 5 + n_pages, inputs.outlier_pairs(1, 5, count=2))
+    encode_and_compare(bits)
+
+
+def special_pages():
+    rng = np.random.default_rng(11)
+    pages = []
+    x = rng.standard_normal((128, 256)).astype(np.float32)
+    x[3] = 1.5                                           # constant channel
+    x[4] = np.where(np.arange(256) % 2 == 0, -2.0, 6.0)  # two-level channel
+    x[5] = np.arange(256)                                # ramp
+    x[6] = 0.0                                           # all zeros
+    x[7] = -0.0                                          # negative zeros
+    x[8, ::3] = -0.0                                     # mixed signed zeros
+    x[9] = rng.standard_normal(256) * 1e-30              # tiny values
+    x[10] = rng.standard_normal(256) * 3e4               # large values
+    x[11] = 1e-3 * np.round(rng.standard_normal(256) * 4)  # heavy ties
+    pages.append(x)
+    pages.append(np.full((128, 256), 7.25, dtype=np.float32))             # constant page
+    y = rng.laplace(0, 0.1, (128, 256)).astype(np.float32)
+    y[:, 100] = 50.0                                                       # single spike per row
+    pages.append(y)
+    return inputs.f32_to_bf16_bits(np.stack(pages))
+
+
+@pytest.mark.parametrize("alpha", [0.25, 100.0, 255.0, 1e4])
+def test_special_pages(cuda_device, alpha):
+    encode_and_compare(special_pages(), alpha)
+
+
+def test_zero_pages_is_a_noop(cuda_device):
+    x = torch.empty((0, 128, 256), dtype=torch.bfloat16, device="cuda")
+    a, r, m = L.lynx_encode_pages(x)
+    assert a.numel() == 0 and m.numel() == 0
+
+
+@pytest.mark.slow
+def test_qwen32b_cache_full_size_sampled(cuda_device):
+    """The 64-layer Qwen-32B-shaped cache (65,536 pages, 4.29e9 BF16 bytes) in one
+    launch, as the benchmark runs it; 256 seeded pages are checked against the oracle."""
+    w = inputs.QWEN32B_CACHE
+    outl = inputs.outlier_pairs(w.n_kv_heads, 0)
+    per = w.pages_per_tensor_layer
+    x = torch.empty((2 * w.n_layers * per, 128, 256), dtype=torch.bfloat16, device="cuda")
+    for layer in range(w.n_layers):
+        for t in range(2):
+            i = (2 * layer + t) * per
+            x[i:i + per] = inputs.kv_pages_torch(w.n_kv_heads, w.n_tokens, inputs.layer_seed(0, layer, t),
+                                                 outl, "cuda")
+    a, r, m = L.lynx_encode_pages(x)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    idx = np.sort(np.random.default_rng(3).choice(x.shape[0], 256, replace=False))
+    ti = torch.from_numpy(idx).cuda()
+    bits = x[ti].view(torch.int16).cpu().numpy().view(np.uint16)
+    oa, orr, om, st = lo.encode_pages(bits, 100.0, EPS, return_stages=True)
+    check_codes(a[ti].cpu().numpy(), r[ti].cpu().numpy(), oa, orr, st.Y)
+    check_meta(m[ti].cpu().numpy(), om)
+
+
+# ------------------------------------------------------------------ reconstruct
+
+def oracle_planes(bits, alpha=100.0):
+    oa, orr, om = lo.encode_pages(bits, alpha, EPS)
+    return oa, orr, om
+
+
+@pytest.mark.parametrize("full", [False, True])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("n_pages,alpha", [(1, 100.0), (37, 255.0), (512, 100.0)])
+def test_reconstruct_parity(cuda_device, full, out_dtype, n_pages, alpha):
+    bits = inputs.kv_pages_np(1, 256 * n_pages, 21, inputs.outlier_pairs(1, 21, count=3))
+    oa, orr, om = oracle_planes(bits, alpha)
+    out = L.lynx_reconstruct(torch.from_numpy(oa).cuda(), torch.from_numpy(orr).cuda() if full else None,
+                             torch.from_numpy(om).cuda(), L.Params(alpha=alpha), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref = lo.reconstruct(oa, orr if full else None, om, alpha, EPS)
+    check_recon(out.float().cpu().numpy(), ref, recon_bound(om), out_dtype == torch.bfloat16)
+
+
+def test_reconstruct_special_pages(cuda_device):
+    bits = special_pages()
+    oa, orr, om = oracle_planes(bits)
+    for full in (False, True):
+        out = L.lynx_reconstruct(torch.from_numpy(oa).cuda(), torch.from_numpy(orr).cuda() if full else None,
+                                 torch.from_numpy(om).cuda(), out_dtype=torch.float32)
+        ref = lo.reconstruct(oa, orr if full else None, om, 100.0, EPS)
+        check_recon(out.cpu().numpy(), ref, recon_bound(om), False)
+
+
+def test_encode_then_reconstruct_round_trip(cuda_device):
+    """The hot path end to end on the GPU: encode, then both reconstructions,
+    against the oracle's encode + reconstruct of the same BF16 bits."""
+    bits = inputs.kv_pages_np(2, 256 * 16, 31, inputs.outlier_pairs(2, 31, count=3))
+    x = to_dev(bits)
+    a, r, m = L.lynx_encode_pages(x)
+    oa, orr, om, st = lo.encode_pages(bits, 100.0, EPS, return_stages=True)
+    check_codes(a.cpu().numpy(), r.cpu().numpy(), oa, orr, st.Y)
+    for full in (False, True):
+        out = L.lynx_reconstruct(a, r if full else None, m, out_dtype=torch.float32)
+        ref = lo.reconstruct(oa, orr if full else None, om, 100.0, EPS)
+        # a code that differs by one at a rounding edge moves that element by one code step
+        err = np.abs(out.cpu().numpy() - ref) <= recon_bound(om)
+        assert err.mean() > 1 - 1e-4

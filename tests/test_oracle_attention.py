@@ -93,3 +93,13 @@ def test_paged_grouped_causal_indexing():
                     assert abs(o[b, t, hq, 0] - (nvis - 1) / 2) < 1e-9
                     assert abs(o[b, t, hq, 1] - (1000 * (hq // G) + b)) < 1e-9
                     assert abs(lse[b, t, hq] - np.log(nvis)) < 1e-9
+
+
+def test_rows_without_visible_keys():
+    q, k, v = _rand((3, 128), 11), _rand((5, 128), 12), _rand((5, 128), 13)
+    o, lse = at.attention_rows(q, k, v, 0.1, np.array([0, 2, 5]))
+    assert np.all(np.isnan(o[0])) and lse[0] == -np.inf
+    o2, l2 = at.attention_rows(q[1:], k[:2], v[:2], 0.1)
+    assert np.max(np.abs(o[1] - o2[0])) < 1e-12 and abs(lse[1] - l2[0]) < 1e-12
+    oe, le = at.attention_rows(q, k[:0], v[:0], 0.1)
+    assert np.all(np.isnan(oe)) and np.all(np.isneginf(le))

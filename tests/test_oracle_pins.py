@@ -133,7 +133,7 @@ def test_split_stream_identities_all_codes():
     assert np.array_equal(16 * V + 7 - q_res.astype(np.int32), I)
     assert q_anc.min() == -8 and q_anc.max() == 7
     assert q_res.min() == -8 and q_res.max() == 7
-    # the printed lines 14-18 need a ninth magnitude level once I + 7 >= 128
+    # Stage 4 as printed needs a ninth magnitude level once I + 7 >= 128
     lit = lo.split_stream_literal(I, S)
     assert np.array_equal(lit["V_mag"] == 8, I >= 121)
     assert lit["Q_anc"].min() == -9 and lit["Q_anc"].max() == 8
