@@ -1,0 +1,491 @@
+"""Benchmark of the Lynx hot path on one GB300 (or N, one process per GPU).
+
+One step = one pass of the whole hot path over a Qwen-32B-shaped KV cache
+(64 layers x 8 KV heads x 128 channels x 16,384 tokens, K and V: 65,536 pages,
+4.29e9 BF16 bytes, synthetic, seeded):
+
+  encode            lynx_encode_pages over all 65,536 pages (one launch)
+  reconstruct_anchor / reconstruct_full   lynx_reconstruct, BF16 out
+  decode_anchor_b1  1-token draft decode, 32 query heads (GQA 4:1), one
+                    sequence per layer (B = 64)
+  decode_anchor_b8  the same with 8 sequences per layer (B = 512; sequence b of
+                    layer l reads layer (l + b) mod 64)
+  verify_full_t8    8-token causal verification over the full codes (B = 64)
+  decode_bf16_b1    the BF16-page baseline kernel, B = 64, 1 token
+
+value = sum over the step's kernels of each kernel's headline bytes (encode:
+BF16 bytes in; reconstruct and decode: packed KV bytes read; BF16 baseline:
+BF16 KV bytes read) / step time, in GB/s.  The per-kernel numbers, including
+the two the metric names (encode GB/s of BF16 in, anchor decode GB/s of packed
+KV read), are under "kernels".
+
+--impl reference times the CPU oracle on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV encode GB/s (BF16 in) and Anchor-KV decode-attn GB/s, % of GB300 HBM peak"
+UNIT = "GB/s"
+WORKLOAD = ("Qwen-32B-shaped KV cache: 64 layers x 8 KV heads x 128 x 16384 tokens, K and V "
+            "(65536 pages of 128x256 BF16, 4.29e9 B); decode B=1 and B=8 (anchor), T=8 verify (full), "
+            "32 query heads")
+N_LAYERS, HKV, HQ, N_TOK = 64, 8, 32, 16384
+NPPH = N_TOK // 256                 # pages per head
+PER = HKV * NPPH                    # pages per tensor per layer (512)
+N_PAGES = 2 * N_LAYERS * PER        # 65536
+PLANE, META, PAGE = 16384, 9216, 65536
+
+# per-page byte counts (headline, moved) of each kernel
+BYTES = {
+    "encode": (PAGE, PAGE + 2 * PLANE + META),
+    "reconstruct_anchor": (PLANE + META, PLANE + META + PAGE),
+    "reconstruct_full": (2 * PLANE + META, 2 * PLANE + META + PAGE),
+    "decode_anchor": (PLANE + META, PLANE + META),
+    "decode_full": (2 * PLANE + META, 2 * PLANE + META),
+    "decode_bf16": (PAGE, PAGE),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def build_buffers(torch, L, inputs, dev, seed=0):
+    outl = inputs.outlier_pairs(HKV, seed)
+    x = torch.empty((N_PAGES, 128, 256), dtype=torch.bfloat16, device=dev)
+    for layer in range(N_LAYERS):
+        for t in range(2):
+            i = (2 * layer + t) * PER
+            x[i:i + PER] = inputs.kv_pages_torch(HKV, N_TOK, inputs.layer_seed(seed, layer, t), outl, dev)
+    anc = torch.empty((N_PAGES, 128, 128), dtype=torch.uint8, device=dev)
+    res = torch.empty_like(anc)
+    meta = torch.empty((N_PAGES, L.META_FLOATS), dtype=torch.float32, device=dev)
+    recon = torch.empty((N_PAGES, 128, 256), dtype=torch.bfloat16, device=dev)
+
+    def table(B, layer_of):
+        t = torch.empty((B, HKV, NPPH), dtype=torch.int32)
+        base = torch.arange(NPPH, dtype=torch.int32)
+        for b in range(B):
+            lay = layer_of(b)
+            for h in range(HKV):
+                t[b, h] = 2 * lay * PER + h * NPPH + base
+        return t.to(dev)
+
+    pt1 = table(N_LAYERS, lambda b: b)
+    pt8 = table(8 * N_LAYERS, lambda b: (b // 8 + b % 8) % N_LAYERS)
+    ctx1 = torch.full((N_LAYERS,), N_TOK, dtype=torch.int32, device=dev)
+    ctx8 = torch.full((8 * N_LAYERS,), N_TOK, dtype=torch.int32, device=dev)
+    q1 = inputs.queries_torch((N_LAYERS, 1, HQ, 128), seed + 1, dev)
+    q8 = inputs.queries_torch((8 * N_LAYERS, 1, HQ, 128), seed + 2, dev)
+    qv = inputs.queries_torch((N_LAYERS, 8, HQ, 128), seed + 3, dev)
+
+    def ws(B, T):
+        n = L.lynx_decode_attn_workspace_size(B, T, HQ, HKV, 128, NPPH)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    b = dict(x=x, anc=anc, res=res, meta=meta, recon=recon, pt1=pt1, pt8=pt8, ctx1=ctx1, ctx8=ctx8,
+             q1=q1, q8=q8, qv=qv, ws1=ws(N_LAYERS, 1), ws8=ws(8 * N_LAYERS, 1), wsv=ws(N_LAYERS, 8),
+             o1=torch.empty((N_LAYERS, 1, HQ, 128), dtype=torch.float32, device=dev),
+             o8=torch.empty((8 * N_LAYERS, 1, HQ, 128), dtype=torch.float32, device=dev),
+             ov=torch.empty((N_LAYERS, 8, HQ, 128), dtype=torch.float32, device=dev))
+    b["l1"] = torch.empty((N_LAYERS, 1, HQ), dtype=torch.float32, device=dev)
+    b["l8"] = torch.empty((8 * N_LAYERS, 1, HQ), dtype=torch.float32, device=dev)
+    b["lv"] = torch.empty((N_LAYERS, 8, HQ), dtype=torch.float32, device=dev)
+    return b
+
+
+def kernel_list(torch, L, b):
+    """(name, callable, launches, headline bytes, moved bytes) of the step's kernels."""
+    anc, res, meta = b["anc"], b["res"], b["meta"]
+    # K pages of layer l are pages 2l*512 + ..., V pages follow 512 pages later
+    kA, vA = anc, anc[PER:]
+    kR, vR = res, res[PER:]
+    kM, vM = meta, meta[PER:]
+    xk, xv = b["x"], b["x"][PER:]
+    n_pool = N_PAGES - PER
+    p = L.Params()
+    dec_pages1 = N_LAYERS * HKV * NPPH
+    dec_pages8 = 8 * dec_pages1
+
+    def dec_anchor(q, pt, ctx, o, l, ws):
+        return lambda: L.lynx_decode_attn(q, kA, None, kM, vA, None, vM, pt, ctx, HKV, p, out=o, lse=l,
+                                          workspace=ws)
+    ks = [
+        ("encode", lambda: L.lynx_encode_pages(b["x"], p, anc, res, meta), 1,
+         N_PAGES * BYTES["encode"][0], N_PAGES * BYTES["encode"][1]),
+        ("reconstruct_anchor", lambda: L.lynx_reconstruct(anc, None, meta, p, out=b["recon"]), 1,
+         N_PAGES * BYTES["reconstruct_anchor"][0], N_PAGES * BYTES["reconstruct_anchor"][1]),
+        ("reconstruct_full", lambda: L.lynx_reconstruct(anc, res, meta, p, out=b["recon"]), 1,
+         N_PAGES * BYTES["reconstruct_full"][0], N_PAGES * BYTES["reconstruct_full"][1]),
+        ("decode_anchor_b1", dec_anchor(b["q1"], b["pt1"], b["ctx1"], b["o1"], b["l1"], b["ws1"]), 2,
+         2 * dec_pages1 * BYTES["decode_anchor"][0], 2 * dec_pages1 * BYTES["decode_anchor"][1]),
+        ("decode_anchor_b8", dec_anchor(b["q8"], b["pt8"], b["ctx8"], b["o8"], b["l8"], b["ws8"]), 2,
+         2 * dec_pages8 * BYTES["decode_anchor"][0], 2 * dec_pages8 * BYTES["decode_anchor"][1]),
+        ("verify_full_t8", lambda: L.lynx_decode_attn(b["qv"], kA, kR, kM, vA, vR, vM, b["pt1"], b["ctx1"], HKV, p,
+                                                       causal=True, out=b["ov"], lse=b["lv"], workspace=b["wsv"]),
+         2, 2 * dec_pages1 * BYTES["decode_full"][0], 2 * dec_pages1 * BYTES["decode_full"][1]),
+        ("decode_bf16_b1", lambda: L.lynx_decode_attn_bf16(b["q1"], xk, xv, b["pt1"], b["ctx1"], HKV, out=b["o1"],
+                                                           lse=b["l1"], workspace=b["ws1"]), 2,
+         2 * dec_pages1 * BYTES["decode_bf16"][0], 2 * dec_pages1 * BYTES["decode_bf16"][1]),
+    ]
+    del n_pool
+    return ks
+
+
+def profile_traffic(name):
+    """DRAM traffic per launch from the committed ncu summary, if the kernel's
+    source is unchanged since it was captured; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "progressive_kv_quantization_gb300", "csrc", e["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return e["bytes_per_launch"] if sha == e["source_sha"] else None
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from progressive_kv_quantization_gb300 import build as _build
+    from progressive_kv_quantization_gb300 import inputs
+    from progressive_kv_quantization_gb300 import lynx as L
+
+    _build.build()
+    L.load()
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = build_buffers(torch, L, inputs, dev, seed=rank)
+    ks = kernel_list(torch, L, b)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        for k in ks:
+            k[1]()
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+
+    ev = {k[0]: [] for k in ks}
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        for name, fn, _, _, _ in ks:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ev[name].append((e0, e1))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    L.lynx_device_status()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    gbps_peak, peak_kind = peaks()
+    kern = {}
+    for name, _, launches, head, moved in ks:
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[name])
+        kern[name] = {"ms": round(ms, 4), "GBps_headline": round(head / ms / 1e6, 1),
+                      "GBps_moved": round(moved / ms / 1e6, 1),
+                      "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3), "launches": launches,
+                      "headline_bytes": head, "moved_bytes": moved}
+    head_total = sum(k[3] for k in ks)
+    value = world * head_total / (ms_step * 1e6)
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    src = {"encode": "encode.cu", "reconstruct_anchor": "reconstruct.cu",
+           "reconstruct_full": "reconstruct.cu"}.get(dom, "decode_attn.cu")
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["GBps_moved"], "peak": gbps_peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_of_hbm"],
+            "traffic": profile_traffic(dom), "source": src}
+    e2e = run_e2e(torch, L, b, ks, args, dev) if rank == 0 else None
+    if rank != 0:
+        return None
+    launches = args.steps * sum(k[2] for k in ks)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "pages": N_PAGES, "bf16_bytes": N_PAGES * PAGE,
+                   "l2": "inputs larger than L2 (4.29e9 B cache), no flush",
+                   "alpha": 100.0, "eps": 1e-6, "parallelism": f"replicas x{world} (one cache per GPU)"},
+        "kernels": kern,
+        "encode_GBps_bf16_in": kern["encode"]["GBps_headline"],
+        "decode_anchor_GBps_packed": kern["decode_anchor_b1"]["GBps_headline"],
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess(args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_subprocess(seconds):
+    """The oracle timed in a fresh single-threaded process on the host cores."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference", "--cpu-only-seconds",
+                        str(seconds)], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "error": r.stderr[-300:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])["cpu_baseline"]
+
+
+def run_e2e(torch, L, b, ks, args, dev):
+    """The same step through host buffers: the BF16 cache and the queries are
+    copied from pinned host memory, and the step's results (encoded planes,
+    metadata, reconstructed cache, attention outputs) are read back."""
+    host_x = torch.empty(b["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+    host_x.copy_(b["x"])
+    h_q = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True).copy_(b[k]) for k in ("q1", "q8", "qv")}
+    outs = ["anc", "res", "meta", "o1", "o8", "ov", "l1", "l8", "lv"]
+    h_out = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in outs}
+    h2d = host_x.numel() * 2 + sum(v.numel() * v.element_size() for v in h_q.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    stream = torch.cuda.current_stream()
+    steps = max(1, min(args.steps, 3))
+
+    def one():
+        b["x"].copy_(host_x, non_blocking=True)
+        for k, v in h_q.items():
+            b[k].copy_(v, non_blocking=True)
+        for k in ks:
+            k[1]()
+        for k in outs:
+            h_out[k].copy_(b[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    head_total = sum(k[3] for k in ks)
+    return {"value": round(head_total / (ms * 1e6), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_sample_step():
+    """A bounded sample of the step for the CPU oracle: one layer's K and V of
+    one KV head (64 + 64 pages) through encode, both reconstructs, the draft
+    decode at B=1 and B=8, the T=8 verification and the BF16 decode.
+    Returns (headline bytes, seconds)."""
+    import numpy as np
+
+    from oracle import attention as at
+    from oracle import lynx_oracle as lo
+    from progressive_kv_quantization_gb300 import inputs
+
+    eps = np.float32(1e-6)
+    outl = inputs.outlier_pairs(1, 0, count=1)
+    kb = inputs.kv_pages_np(1, N_TOK, 1, outl)
+    vb = inputs.kv_pages_np(1, N_TOK, 2, outl)
+    G = HQ // HKV
+    q1 = inputs.queries_np((1, 1, G, 128), 3)
+    q8 = inputs.queries_np((8, 1, G, 128), 4)
+    qv = inputs.queries_np((1, 8, G, 128), 5)
+    table1 = np.arange(NPPH, dtype=np.int32)[None, None]
+    table8 = np.repeat(table1, 8, axis=0)
+    ctx1 = np.array([N_TOK])
+    ctx8 = np.full(8, N_TOK)
+    scale = 1 / math.sqrt(128)
+    t0 = time.perf_counter()
+    ka, kr, km = lo.encode_pages(kb, 100.0, eps)
+    va, vr, vm = lo.encode_pages(vb, 100.0, eps)
+    kd_a = lo.reconstruct(ka, None, km, 100.0, eps)
+    vd_a = lo.reconstruct(va, None, vm, 100.0, eps)
+    kd_f = lo.reconstruct(ka, kr, km, 100.0, eps)
+    vd_f = lo.reconstruct(va, vr, vm, 100.0, eps)
+    fa = lambda ids: (kd_a[ids], vd_a[ids])
+    ff = lambda ids: (kd_f[ids], vd_f[ids])
+    fb = lambda ids: (lo.bf16_to_f32(kb[ids]).astype(np.float64), lo.bf16_to_f32(vb[ids]).astype(np.float64))
+    qf = lambda q: lo.bf16_to_f32(q).astype(np.float64)
+    at.decode_attention(qf(q1), fa, table1, ctx1, 1, scale, False)
+    at.decode_attention(qf(q8), fa, table8, ctx8, 1, scale, False)
+    at.decode_attention(qf(qv), ff, table1, ctx1, 1, scale, True)
+    at.decode_attention(qf(q1), fb, table1, ctx1, 1, scale, False)
+    sec = time.perf_counter() - t0
+    n = 2 * NPPH
+    head = (n * BYTES["encode"][0] + n * BYTES["reconstruct_anchor"][0] + n * BYTES["reconstruct_full"][0]
+            + n * BYTES["decode_anchor"][0] * (1 + 8) + n * BYTES["decode_full"][0] + n * BYTES["decode_bf16"][0])
+    return head, sec
+
+
+def run_reference_sample(seconds=15.0, steps=None, warmup=0):
+    """Times the oracle on repeated bounded samples (the caller's process runs
+    with one BLAS / OpenMP thread)."""
+    for _ in range(warmup):
+        oracle_sample_step()
+    tot_b, tot_s, n = 0, 0.0, 0
+    while (steps is None and (tot_s < seconds or n == 0)) or (steps is not None and n < steps):
+        bb, ss = oracle_sample_step()
+        tot_b += bb
+        tot_s += ss
+        n += 1
+    v = tot_b / tot_s / 1e9
+    return {"value": v, "seconds": tot_s, "samples": n,
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": (f"{n} x (one layer's K and V of one KV head: 2 x 64 pages, 16384 tokens, "
+                                        "4 query heads) through encode, both reconstructs, B=1 and B=8 draft "
+                                        "decode, T=8 verify, BF16 decode; numpy, 1 thread"),
+                             "seconds": round(tot_s, 2)}}
+
+
+def main():
+    if "--impl" in sys.argv and "reference" in sys.argv:
+        # the oracle runs single-threaded: fix the thread count before numpy loads
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["lynx", "reference"], default="lynx")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-only-seconds", type=float, default=None)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 only; other ranks exit without work
+        if rank != 0:
+            return
+        if args.cpu_only_seconds is not None:
+            r = run_reference_sample(seconds=args.cpu_only_seconds)
+        else:
+            r = run_reference_sample(steps=args.steps, warmup=args.warmup)
+        line = {"metric": METRIC, "value": round(r["value"], 4), "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1000 * r["seconds"] / max(r["samples"], 1), 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": WORKLOAD, "sample": "one KV head of one layer per step (CPU oracle)"},
+                "cpu_baseline": r["cpu_baseline"],
+                "e2e": {"value": round(r["value"], 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = run_gpu(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
