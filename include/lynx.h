@@ -166,6 +166,32 @@ int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int
                           float sm_scale, int causal, float* out, float* lse,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* lynx_decode_attn without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: a connector or deserializer plugin that a
+ * serving engine loads with a fixed memory budget and no allocator, or a
+ * decode loop that must not call cudaMalloc / cudaFree because they
+ * synchronise the device.  The paper has no counterpart; this is an
+ * integration entry point of this library.
+ *   Arguments: as lynx_decode_attn, minus workspace and workspace_bytes.
+ *   Scratch: a static device array of 8 MiB inside the library, held by every
+ *   GPU that loads the library until the process exits.  Shapes whose
+ *   lynx_decode_attn_workspace_size() exceeds 8 MiB return
+ *   LYNX_ERR_WORKSPACE.  The first call on a device resolves the array's
+ *   device address (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.
+ *   No allocation: the call never calls cudaMalloc, cudaFree or any allocating
+ *   routine.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (the kernels overwrite all of it that they read, so it
+ *   needs no clearing); calls whose kernels overlap on the GPU (different
+ *   streams, no ordering between them) race on it and give wrong results. */
+int lynx_decode_attn_noalloc(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                             const uint8_t* k_anc, const uint8_t* k_res, const float* k_meta,
+                             const uint8_t* v_anc, const uint8_t* v_res, const float* v_meta,
+                             int64_t n_pool_pages, const int32_t* page_table, int max_pages,
+                             const int32_t* ctx_len, const lynx_params_t* params, float sm_scale,
+                             int causal, float* out, float* lse, void* stream);
+
 /* Workspace bytes needed by lynx_decode_attn / lynx_decode_attn_bf16 for the
  * given shape on the current device (0 for invalid shapes). */
 size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages);

@@ -113,6 +113,8 @@ const LutTables* lut_tables(float alpha, float eps) {
   return &lut;
 }
 
+int set_error(int status, const char* message) { return fail(status, "%s", message); }
+
 int device_sm_count() {
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return 1;

@@ -45,6 +45,7 @@ const EncodeTables* encode_tables(float alpha, float eps);
 const LutTables* lut_tables(float alpha, float eps);
 
 int device_sm_count();
+int set_error(int status, const char* message);   // records lynx_last_error(), returns status
 int* device_status_ptr();   // device address of this device's error word
 
 // Launchers (one per kernel family).  Return cudaGetLastError() of the launch.

@@ -57,6 +57,8 @@ SIGNATURES = {
                                 _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "lynx_decode_attn_bf16": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I64, _VP, _I32,
                                      _VP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "lynx_decode_attn_noalloc": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                        _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP]),
     "lynx_decode_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lynx_device_status": (_I32, []),
     "lynx_status_string": (ctypes.c_char_p, [_I32]),
@@ -186,6 +188,27 @@ def lynx_decode_attn(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page_table, 
         _ptr(v_res), _ptr(v_meta), n_pool, _ptr(page_table), max_pages, _ptr(ctx_len),
         ctypes.byref(p), scale, int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_decode_attn")
+    return out, lse
+
+
+def lynx_decode_attn_noalloc(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page_table, ctx_len,
+                             n_kv_heads, params: Params = Params(), sm_scale=None, causal=False,
+                             out=None, lse=None, stream=None):
+    """lynx_decode_attn without a workspace argument: the library's own 8 MiB
+    static scratch is used, for callers that cannot allocate device memory."""
+    _need(q, torch.bfloat16, "q")
+    B, T, Hq, D = q.shape
+    max_pages = page_table.shape[2]
+    out = out if out is not None else torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
+    lse = lse if lse is not None else torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    n_pool = k_anc.numel() // PLANE_BYTES
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
+    p = params.c()
+    _check(load().lynx_decode_attn_noalloc(
+        _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_anc), _ptr(k_res), _ptr(k_meta), _ptr(v_anc),
+        _ptr(v_res), _ptr(v_meta), n_pool, _ptr(page_table), max_pages, _ptr(ctx_len),
+        ctypes.byref(p), scale, int(bool(causal)), _ptr(out), _ptr(lse), _stream(stream)),
+        "lynx_decode_attn_noalloc")
     return out, lse
 
 
