@@ -31,7 +31,9 @@
  *                segments per byte).  16384 B per page.
  *   Residual     Same layout, 4-bit two's-complement residual.  16384 B.
  *   Metadata     Per page float32[2304] = gamma_min[128], gamma_scale[128],
- *                mu[128][8], sigma[128][8] (Algorithm 1's metadata).  9216 B.
+ *                mu[8][128], sigma[8][128] (Algorithm 1's metadata; mu and
+ *                sigma chunk-major: element [b][c] is chunk b of channel c).
+ *                9216 B.
  *
  * Code definition (per channel c of a page, per token t, chunk b = t / 32):
  *   x_n = (x - gamma_min) / (gamma_scale + eps)              (Stage 1)

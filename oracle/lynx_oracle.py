@@ -177,23 +177,26 @@ def unpack_nibbles(b: np.ndarray) -> np.ndarray:
 
 
 def meta_size(H: int, P: int, C: int) -> int:
-    """float32 scalars of metadata per page: gamma_min[H], gamma_scale[H], mu[H][P/C], sigma[H][P/C]."""
+    """float32 scalars of metadata per page: gamma_min[H], gamma_scale[H],
+    mu[P/C][H], sigma[P/C][H] (chunk-major: one chunk's H values are contiguous)."""
     return 2 * H + 2 * H * (P // C)
 
 
 def pack_meta(gmin, gscale, mu, sigma) -> np.ndarray:
+    """mu, sigma given as [N, H, P/C]; stored chunk-major."""
     N, H = gmin.shape
-    return np.concatenate([gmin, gscale, mu.reshape(N, -1), sigma.reshape(N, -1)],
-                          axis=1).astype(np.float32)
+    return np.concatenate([gmin, gscale, mu.transpose(0, 2, 1).reshape(N, -1),
+                           sigma.transpose(0, 2, 1).reshape(N, -1)], axis=1).astype(np.float32)
 
 
 def unpack_meta(meta: np.ndarray, H: int, P: int, C: int):
+    """Inverse of pack_meta; returns mu, sigma as [N, H, P/C]."""
     meta = np.asarray(meta, dtype=np.float32).reshape(-1, meta_size(H, P, C))
     nb = P // C
     gmin = meta[:, :H]
     gscale = meta[:, H:2 * H]
-    mu = meta[:, 2 * H:2 * H + H * nb].reshape(-1, H, nb)
-    sigma = meta[:, 2 * H + H * nb:].reshape(-1, H, nb)
+    mu = meta[:, 2 * H:2 * H + H * nb].reshape(-1, nb, H).transpose(0, 2, 1)
+    sigma = meta[:, 2 * H + H * nb:].reshape(-1, nb, H).transpose(0, 2, 1)
     return gmin, gscale, mu, sigma
 
 
@@ -210,7 +213,7 @@ def encode_pages(x_bits: np.ndarray, alpha, eps, C: int = 32, return_stages: boo
     """Algorithm 1 on BF16 pages [N, H, P]; returns (anchor, residual, meta).
 
     anchor, residual: uint8 [N, H, P/2] packed planes; meta: float32
-    [N, 2H + 2H*P/C] = gamma_min[H], gamma_scale[H], mu[H][P/C], sigma[H][P/C].
+    [N, 2H + 2H*P/C] = gamma_min[H], gamma_scale[H], mu[P/C][H], sigma[P/C][H].
     """
     st = run_stages(x_bits, alpha, eps, C)
     q_anc, q_res = split_stream(st.I, st.S)

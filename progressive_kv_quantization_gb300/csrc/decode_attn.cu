@@ -324,8 +324,8 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
         const int d = 4 * L + j;
         const float gmin = km[d];
         const float dg = __fadd_rn(km[kH + d], eps);
-        const float mu = km[kMetaMuOff + d * kChunks + blk];
-        const float ds = __fadd_rn(km[kMetaSigmaOff + d * kChunks + blk], eps);
+        const float mu = km[kMetaMuOff + blk * kH + d];
+        const float ds = __fadd_rn(km[kMetaSigmaOff + blk * kH + d], eps);
         const float A = __fmaf_rn(dg, mu, gmin);
         const float Bc = __fmul_rn(dg, ds);
         const float4 q = reinterpret_cast<const float4*>(s_qs)[d];
@@ -577,8 +577,8 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
           const int ch = 16 * w + c4 + 4 * k;
           const float gmin = vm[ch];
           const float dg = __fadd_rn(vm[kH + ch], eps);
-          const float mu = vm[kMetaMuOff + ch * kChunks + blk_v];
-          const float ds = __fadd_rn(vm[kMetaSigmaOff + ch * kChunks + blk_v], eps);
+          const float mu = vm[kMetaMuOff + blk_v * kH + ch];
+          const float ds = __fadd_rn(vm[kMetaSigmaOff + blk_v * kH + ch], eps);
           const float A = __fmaf_rn(dg, mu, gmin);
           const float Bc = __fmul_rn(dg, ds);
 #pragma unroll
@@ -719,11 +719,12 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s) {
-  switch (mode) {
-    case kModeAnchor: return launch_mode<kModeAnchor>(a, lut, s);
-    case kModeFull: return launch_mode<kModeFull>(a, lut, s);
-    default: return launch_mode<kModeBf16>(a, lut, s);
-  }
+  if (mode == kModeBf16) return launch_mode<kModeBf16>(a, lut, s);
+  cudaError_t e = launch_decode_quant(a, mode == kModeFull, lut, s);
+  if (e != cudaSuccess) return e;
+  dim3 g2(a.n_rg * kRows, a.Hkv, a.B);
+  decode_combine_kernel<<<g2, kH, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace lynx

@@ -7,8 +7,8 @@
 // min/max of a row is a 3-step xor shuffle over its 8 lanes; the chunk mean is
 // the lane's own left-to-right sum of its 32 values, which is the order the
 // code definition fixes.  Each lane then writes 16 bytes of the Anchor plane,
-// 16 bytes of the Residual plane and its chunk's (mu, sigma); a warp's stores
-// are contiguous 512-byte runs.  The next row group's 64 bytes are prefetched
+// 16 bytes of the Residual plane and its chunk's (mu, sigma); a warp's plane
+// stores are contiguous 512-byte runs.  The next row group's 64 bytes are prefetched
 // into registers while the current one is processed.
 //
 // Exactness.  Every Stage 1-2 step is a single correctly rounded float32
@@ -133,8 +133,8 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
       mp[ch] = mn;
       mp[kH + ch] = gscale;
     }
-    mp[kMetaMuOff + 32 * rgrp + lane] = mu;
-    mp[kMetaSigmaOff + 32 * rgrp + lane] = sigma;
+    mp[kMetaMuOff + (lane & 7) * kH + ch] = mu;
+    mp[kMetaSigmaOff + (lane & 7) * kH + ch] = sigma;
   }
 }
 

@@ -17,8 +17,8 @@ constexpr int kPageElems = kH * kP;                    // 32768
 constexpr int kPlaneBytes = kH * kP / 2;               // 16384: one 4-bit plane
 constexpr int kMetaFloats = 2 * kH + 2 * kH * kChunks; // 2304
 constexpr int kMetaBytes = kMetaFloats * 4;            // 9216
-constexpr int kMetaMuOff = 2 * kH;                     // mu[128][8] starts here
-constexpr int kMetaSigmaOff = 2 * kH + kH * kChunks;   // sigma[128][8]
+constexpr int kMetaMuOff = 2 * kH;                     // mu[8][128] (chunk-major) starts here
+constexpr int kMetaSigmaOff = 2 * kH + kH * kChunks;   // sigma[8][128]
 
 // Quantiser tables for one (alpha, eps).  thr[k] (k = 1..127) is the smallest
 // float32 f with 127 ln(1 + alpha f)/ln(1 + alpha) >= k - 1/2, so that for a
@@ -91,6 +91,8 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode);
+bool n_pool_too_large(int64_t n_pool);
+cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);
 
 }  // namespace lynx

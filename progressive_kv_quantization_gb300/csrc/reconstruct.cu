@@ -44,8 +44,8 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
     const float* mp = meta + page * kMetaFloats;
     const float gmin = __ldg(mp + ch);
     const float dg = __fadd_rn(__ldg(mp + kH + ch), eps);
-    const float mu = __ldg(mp + kMetaMuOff + ch * kChunks + blk);
-    const float ds = __fadd_rn(__ldg(mp + kMetaSigmaOff + ch * kChunks + blk), eps);
+    const float mu = __ldg(mp + kMetaMuOff + blk * kH + ch);
+    const float ds = __fadd_rn(__ldg(mp + kMetaSigmaOff + blk * kH + ch), eps);
 
     float xv[8];
 #pragma unroll

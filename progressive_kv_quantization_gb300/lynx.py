@@ -153,6 +153,21 @@ def lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages) -> int:
     return int(load().lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages))
 
 
+def _pool_pages(k_anc, k_res, k_meta, v_anc, v_res, v_meta) -> int:
+    """Pages addressable in every pool passed (page ids must stay below it)."""
+    for t, nm in ((k_anc, "k_anc"), (v_anc, "v_anc")):
+        _need(t, torch.uint8, nm)
+    for t, nm in ((k_meta, "k_meta"), (v_meta, "v_meta")):
+        _need(t, torch.float32, nm)
+    n = min(k_anc.numel(), v_anc.numel()) // PLANE_BYTES
+    n = min(n, k_meta.numel() // META_FLOATS, v_meta.numel() // META_FLOATS)
+    for t in (k_res, v_res):
+        if t is not None:
+            _need(t, torch.uint8, "residual pool")
+            n = min(n, t.numel() // PLANE_BYTES)
+    return n
+
+
 def _decode_prep(q, page_table, ctx_len, n_kv_heads, out, lse, workspace):
     _need(q, torch.bfloat16, "q")
     if q.dim() != 4:
@@ -180,7 +195,7 @@ def lynx_decode_attn(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page_table, 
     None: anchor-only draft KV).  Returns (out f32[B,T,Hq,128], lse f32[B,T,Hq])."""
     B, T, Hq, D, max_pages, out, lse, workspace = _decode_prep(q, page_table, ctx_len, n_kv_heads,
                                                                out, lse, workspace)
-    n_pool = k_anc.numel() // PLANE_BYTES
+    n_pool = _pool_pages(k_anc, k_res, k_meta, v_anc, v_res, v_meta)
     scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
     p = params.c()
     _check(load().lynx_decode_attn(
@@ -201,7 +216,7 @@ def lynx_decode_attn_noalloc(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page
     max_pages = page_table.shape[2]
     out = out if out is not None else torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
     lse = lse if lse is not None else torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
-    n_pool = k_anc.numel() // PLANE_BYTES
+    n_pool = _pool_pages(k_anc, k_res, k_meta, v_anc, v_res, v_meta)
     scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
     p = params.c()
     _check(load().lynx_decode_attn_noalloc(
@@ -219,7 +234,7 @@ def lynx_decode_attn_bf16(q, k_pages, v_pages, page_table, ctx_len, n_kv_heads, 
                                                                out, lse, workspace)
     _need(k_pages, torch.bfloat16, "k_pages")
     _need(v_pages, torch.bfloat16, "v_pages")
-    n_pool = k_pages.numel() // (H * P)
+    n_pool = min(k_pages.numel(), v_pages.numel()) // (H * P)
     scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
     _check(load().lynx_decode_attn_bf16(
         _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_pages), _ptr(v_pages), n_pool, _ptr(page_table),
