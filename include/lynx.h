@@ -113,6 +113,13 @@ enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 };
 int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
                       uint8_t* anchor, uint8_t* residual, float* meta, void* stream);
 
+/* Stage 3 of Algorithm 1 alone: codes[i] = round(127 ln(1 + alpha |a_i|) /
+ * ln(1 + alpha)) in 0..127 for float32 magnitudes |a_i| <= 1 (larger values
+ * are clamped to 1), decided exactly for the float32 input as in
+ * lynx_encode_pages.  a: n float32 (device), codes: n uint8 (device). */
+int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* params,
+                             uint8_t* codes, void* stream);
+
 /* Dequantisation (paper §4.2: Anchor phase and Residual phase).
  *   residual == NULL selects the anchor-only reconstruction (draft KV);
  *   otherwise the full code is used (verification KV).

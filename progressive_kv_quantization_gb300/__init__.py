@@ -14,6 +14,7 @@ from .lynx import (  # noqa: F401
     lynx_decode_attn_workspace_size,
     lynx_device_status,
     lynx_encode_pages,
+    lynx_quantize_magnitudes,
     lynx_reconstruct,
     load,
 )

@@ -8,40 +8,114 @@
 // the lane's own left-to-right sum of its 32 values, which is the order the
 // code definition fixes.  Each lane then writes 16 bytes of the Anchor plane,
 // 16 bytes of the Residual plane and its chunk's (mu, sigma); a warp's plane
-// stores are contiguous 512-byte runs.  The next row group's 64 bytes are prefetched
-// into registers while the current one is processed.
+// stores are contiguous 512-byte runs.  The next row group's 64 bytes are
+// prefetched into registers while the current one is processed.
 //
 // Exactness.  Every Stage 1-2 step is a single correctly rounded float32
-// operation written with explicit _rn intrinsics (no contraction).  Each
-// division x / d by a per-row or per-chunk divisor d uses r = RN(1/d), then
-// q = RN(x r) corrected by one FMA residual step, q' = RN(q + r (x - q d))
+// operation (packed two-wide where the values come in pairs; no contraction).
+// Each division x / d by a per-row or per-chunk divisor d uses r = RN(1/d),
+// then q = RN(x r) corrected by one FMA residual step, q' = RN(q + r (x - q d))
 // (Markstein's FMA division correction), which returns the correctly rounded
-// quotient.  The Stage 3 code round(127 ln(1+alpha a)/ln(1+alpha)) is first
-// estimated with the hardware log2; when the estimate lies within a safety
+// quotient.  sigma = max_t |x_n,t - mu| is taken as
+// max(RN(x_n(max x) - mu), RN(mu - x_n(min x))): every step from x to
+// x_n - mu is a monotone rounding, so the extreme deviations sit at the
+// chunk's extreme inputs and the value is the same.  The Stage 3 code
+// round(127 ln(1+alpha a)/ln(1+alpha)) is estimated with the hardware log2
+// and rounded by adding 1.5 * 2^23; when the estimate lies within a safety
 // margin of a rounding edge the code is decided exactly from the threshold
 // table (the smallest float32 of each code).
+//
+// Packing.  The lane's 32 codes sit in the low bytes of the rounded floats;
+// byte permutes gather four of them per word, and the anchor nibble
+// ((S>0 ? I : ~I) >> 4) and residual nibble ((7 - I) mod 16) are formed four
+// at a time before the nibbles of eight tokens are merged into one word.
 
 #include "lynx_internal.cuh"
+
+#include <cuda_bf16.h>
 
 namespace lynx {
 namespace {
 
-__device__ __forceinline__ float div_rn_by(float x, float d, float r) {
+constexpr float kMagic = 12582912.0f;     // 1.5 * 2^23: x + kMagic rounds x to an integer
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// correctly rounded x / d for a pair, given r = RN(1/d) and nd = -d
+__device__ __forceinline__ float2 div2(float2 x, float2 nd, float2 r) {
+  const float2 q = __fmul2_rn(x, r);
+  const float2 e = __ffma2_rn(q, nd, x);
+  return __ffma2_rn(e, r, q);
+}
+
+__device__ __forceinline__ float div1(float x, float d, float r) {
   const float q = __fmul_rn(x, r);
   const float e = __fmaf_rn(-q, d, x);
   return __fmaf_rn(e, r, q);
 }
 
-__device__ __forceinline__ int quantise_mag(float a, const float* __restrict__ s_thr, float c_lg2,
-                                            float alpha, float edge) {
-  const float y = __fmul_rn(c_lg2, __log2f(__fmaf_rn(alpha, a, 1.0f)));
-  const float r = rintf(y);
-  int I = __float2int_rn(r);
-  if (fabsf(y - r) > edge) {
-    I = min(max(I, 0), 127);
-    I += (a >= s_thr[I + 1] ? 1 : 0) - (a < s_thr[I] ? 1 : 0);
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t lt_zero_mask(float x) {   // 0xFFFFFFFF if x < 0 (-0 is not)
+  uint32_t m;
+  asm("set.lt.u32.f32 %0, %1, 0f00000000;" : "=r"(m) : "f"(x));
+  return m;
+}
+
+// bytes 0 of w0..w3 -> one word
+__device__ __forceinline__ uint32_t gather4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  return prmt(prmt(w0, w1, 0x0040u), prmt(w2, w3, 0x0040u), 0x5410u);
+}
+
+// low nibbles of the 4 bytes of lo (tokens 0-3) and hi (tokens 4-7) -> 8 nibbles, token k at bits 4k
+__device__ __forceinline__ uint32_t merge_nibbles(uint32_t lo, uint32_t hi) {
+  const uint32_t a = lo | (lo >> 4);
+  const uint32_t b = hi | (hi >> 4);
+  return prmt(a, b, 0x6420u);
+}
+
+struct QuantConsts {
+  float2 alpha2, c2;
+  float edge;
+};
+
+// Stage 3 for eight magnitudes a (pairs): the rounded code of each lands in the
+// low byte of ib[e] (the bits of code + 1.5 * 2^23).  The estimate
+// y = c * log2(1 + alpha a) is off by less than 0.5 - edge; when any of the
+// eight lies within that margin of a rounding edge, all eight are decided
+// exactly: with I0 = round(y) and j = I0 + (y > I0), the code is
+// j - 1 + (a >= thr[j]), thr[k] being the smallest float32 with code k.
+__device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8],
+                                          const float* __restrict__ s_thr, const QuantConsts& qc) {
+  const float2 one2 = f2(1.0f), mone2 = f2(-1.0f), magic2 = f2(kMagic), nmagic2 = f2(-kMagic);
+  float2 d[4];
+  float dmax = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 tt = __ffma2_rn(qc.alpha2, a[u], one2);
+    const float2 y = __fmul2_rn(qc.c2, make_float2(__log2f(tt.x), __log2f(tt.y)));
+    const float2 r = __fadd2_rn(y, magic2);                     // round to nearest (even)
+    const float2 ry = __fadd2_rn(r, nmagic2);                   // round(y), exact
+    d[u] = __ffma2_rn(ry, mone2, y);                            // y - round(y), exact
+    ib[2 * u] = __float_as_uint(r.x);
+    ib[2 * u + 1] = __float_as_uint(r.y);
+    dmax = fmaxf(dmax, fmaxf(fabsf(d[u].x), fabsf(d[u].y)));
   }
-  return min(max(I, 0), 127);
+  if (dmax > qc.edge) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float de = (e & 1) ? d[e >> 1].y : d[e >> 1].x;
+      const float ae = (e & 1) ? a[e >> 1].y : a[e >> 1].x;
+      const int I0 = min(max((int)(ib[e] - kMagicBits), 0), 127);
+      const int j = I0 + (de > 0.0f ? 1 : 0);
+      ib[e] = kMagicBits + (uint32_t)(j - 1 + (ae >= s_thr[j] ? 1 : 0));
+    }
+  }
 }
 
 __device__ __forceinline__ void load_chunk(const uint4* __restrict__ src, uint4 (&raw)[4]) {
@@ -49,7 +123,7 @@ __device__ __forceinline__ void load_chunk(const uint4* __restrict__ src, uint4 
   for (int k = 0; k < 4; ++k) raw[k] = __ldg(src + k);
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__ anchor,
               uint4* __restrict__ residual, float* __restrict__ meta, const EncodeTables tab) {
   __shared__ float s_thr[129];
@@ -60,67 +134,95 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const float eps = tab.eps;
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
 
   uint4 raw[4];
   if (g < n_groups) load_chunk(x + g * 128 + lane * 4, raw);
 
   for (; g < n_groups; g += n_warps) {
-    float v[32];
+    uint32_t w[16];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
-        v[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
+      w[4 * k] = raw[k].x;
+      w[4 * k + 1] = raw[k].y;
+      w[4 * k + 2] = raw[k].z;
+      w[4 * k + 3] = raw[k].w;
     }
     const int64_t g_next = g + n_warps;
     if (g_next < n_groups) load_chunk(x + g_next * 128 + lane * 4, raw);
 
-    // ---- Stage 1: per-channel page min / scale
-    float mn = v[0], mx = v[0];
+    // ---- chunk and row extremes on the packed BF16 pairs (exact)
+    __nv_bfloat162 bmn = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
+    __nv_bfloat162 bmx = bmn;
 #pragma unroll
-    for (int t = 1; t < 32; ++t) {
-      mn = fminf(mn, v[t]);
-      mx = fmaxf(mx, v[t]);
+    for (int t = 1; t < 16; ++t) {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[t]);
+      bmn = __hmin2(bmn, v);
+      bmx = __hmax2(bmx, v);
     }
+    const float cmn = fminf(__low2float(bmn), __high2float(bmn));   // chunk min of x
+    const float cmx = fmaxf(__low2float(bmx), __high2float(bmx));   // chunk max of x
+    float mn = cmn, mx = cmx;
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
+
+    // ---- Stage 1: x_n = (x - gamma_min) / (gamma_scale + eps)
     const float gscale = __fsub_rn(mx, mn);
     const float dg = __fadd_rn(gscale, eps);
     const float rg = __frcp_rn(dg);
+    const float2 nmn2 = f2(-mn), ndg2 = f2(-dg), rg2 = f2(rg);
+    float2 xn[16];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) v[t] = div_rn_by(__fsub_rn(v[t], mn), dg, rg);
-
-    // ---- Stage 2: chunk mean and max deviation
-    float s = v[0];
-#pragma unroll
-    for (int t = 1; t < 32; ++t) s = __fadd_rn(s, v[t]);
-    const float mu = __fmul_rn(s, 0.03125f);
-    float sigma = 0.0f;
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      v[t] = __fsub_rn(v[t], mu);
-      sigma = fmaxf(sigma, fabsf(v[t]));
+    for (int t = 0; t < 16; ++t) {
+      const float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+      xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
     }
+
+    // ---- Stage 2: mu (left-to-right sum), sigma, x_f
+    float s = xn[0].x;
+    s = __fadd_rn(s, xn[0].y);
+#pragma unroll
+    for (int t = 1; t < 16; ++t) {
+      s = __fadd_rn(s, xn[t].x);
+      s = __fadd_rn(s, xn[t].y);
+    }
+    const float mu = __fmul_rn(s, 0.03125f);
+    const float xn_max = div1(__fsub_rn(cmx, mn), dg, rg);
+    const float xn_min = div1(__fsub_rn(cmn, mn), dg, rg);
+    const float sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
     const float ds = __fadd_rn(sigma, eps);
     const float rs = __frcp_rn(ds);
+    const float2 nmu2 = f2(-mu), nds2 = f2(-ds), rs2 = f2(rs);
 
-    // ---- Stages 3-4: code, split, pack
-    uint32_t pa[4] = {0u, 0u, 0u, 0u}, pr[4] = {0u, 0u, 0u, 0u};
+    // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
+    // rounded floats, sign masks, then split and pack
+    uint32_t pa[4], pr[4];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const float xf = div_rn_by(v[t], ds, rs);
-      const int I = quantise_mag(fabsf(xf), s_thr, tab.c_lg2, tab.alpha, tab.edge);
-      const int q8 = (xf < 0.0f) ? ~I : I;                // sign-aware 8-bit code
-      const uint32_t an = (uint32_t)(q8 >> 4) & 0xFu;      // anchor nibble
-      const uint32_t rn = (uint32_t)(7 - I) & 0xFu;        // residual 16(I>>4)+7-I, mod 16
-      pa[t >> 3] |= an << (4 * (t & 7));
-      pr[t >> 3] |= rn << (4 * (t & 7));
+    for (int q = 0; q < 4; ++q) {
+      uint32_t ib[8], sm[8];
+      float2 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = 4 * q + u;
+        const float2 xc = __fadd2_rn(xn[t], nmu2);
+        sm[2 * u] = lt_zero_mask(xc.x);
+        sm[2 * u + 1] = lt_zero_mask(xc.y);
+        a[u] = div2(make_float2(fabsf(xc.x), fabsf(xc.y)), nds2, rs2);   // |x_f|
+      }
+      quantise8(a, ib, s_thr, qc);
+      uint32_t an[2], rn[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t I4 = gather4(ib[4 * hh], ib[4 * hh + 1], ib[4 * hh + 2], ib[4 * hh + 3]);
+        const uint32_t S4 = gather4(sm[4 * hh], sm[4 * hh + 1], sm[4 * hh + 2], sm[4 * hh + 3]);
+        an[hh] = ((I4 >> 4) ^ S4) & 0x0F0F0F0Fu;                        // (S>0 ? I : ~I) >> 4
+        rn[hh] = (((~I4) & 0x0F0F0F0Fu) + 0x08080808u) & 0x0F0F0F0Fu;  // (7 - I) mod 16
+      }
+      pa[q] = merge_nibbles(an[0], an[1]);
+      pr[q] = merge_nibbles(rn[0], rn[1]);
     }
     anchor[g * 32 + lane] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
     residual[g * 32 + lane] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
@@ -138,7 +240,46 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
   }
 }
 
+// Stage 3 alone on float32 magnitudes (|a|, expected in [0, 1]): one 8-value group per thread.
+__global__ void __launch_bounds__(256)
+quantize_kernel(const float* __restrict__ a, int64_t n, uint8_t* __restrict__ codes,
+                const EncodeTables tab) {
+  __shared__ float s_thr[129];
+  for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
+  __syncthreads();
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
+  const int64_t n_groups = (n + 7) / 8;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int64_t i = g * 8 + e;
+      v[e] = i < n ? fminf(fabsf(a[i]), 1.0f) : 0.0f;
+    }
+    float2 av[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) av[u] = make_float2(v[2 * u], v[2 * u + 1]);
+    uint32_t ib[8];
+    quantise8(av, ib, s_thr, qc);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int64_t i = g * 8 + e;
+      if (i < n) codes[i] = (uint8_t)(ib[e] & 0xFFu);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,
+                            cudaStream_t s) {
+  const int64_t groups = (n + 7) / 8;
+  const int64_t blocks = (groups + 255) / 256;
+  const int grid = (int)(blocks < (int64_t)device_sm_count() * 8 ? blocks : (int64_t)device_sm_count() * 8);
+  quantize_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(a, n, codes, *tab);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
                           float* meta, const EncodeTables* tab, cudaStream_t s) {

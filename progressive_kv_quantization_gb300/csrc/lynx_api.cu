@@ -78,9 +78,14 @@ const EncodeTables* encode_tables(float alpha, float eps) {
   tab.alpha = alpha;
   tab.eps = eps;
   // Margin around a rounding edge inside which the code is decided from the
-  // table: far above the error of c * log2(1 + alpha a) evaluated with the
-  // hardware log2 and float32 rounding.
-  tab.edge = (float)(0.5 - (1e-3 + c * ldexp(1.0, -16)));
+  // table.  The estimate c * log2(1 + alpha a) uses the hardware log2, whose
+  // absolute error on [1, 2^20) stays below 2^-21 * max(1, log2(t)) (measured
+  // over every float32 t in that range: at most 2^-22.5 below 4, 2^-20.9 below
+  // 256, 2^-19 below 2^20); the rounding of 1 + alpha a, of c and of the
+  // product add at most c * 1e-7 + 1.6e-5.  The margin is twice the sum.
+  const double L = log2(1.0 + a);
+  const double err = c * (ldexp(1.0, -21) * (L > 1.0 ? L : 1.0) + 1e-7) + 1.6e-5;
+  tab.edge = (float)(0.5 - 2.0 * err);
   cached_alpha = alpha;
   cached_eps = eps;
   return &tab;
@@ -178,6 +183,21 @@ int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* 
   cudaError_t e = launch_encode(x_bf16, n_pages, anchor, residual, meta, tab,
                                 static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_pages launch");
+  return LYNX_OK;
+}
+
+int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* params,
+                             uint8_t* codes, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (n < 0) return fail(LYNX_ERR_INVALID_ARG, "n=%lld < 0", (long long)n);
+  if (n == 0) return LYNX_OK;
+  if (!a || !codes) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(a) || misaligned(codes)) return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  const EncodeTables* tab = encode_tables(params->alpha, params->eps);
+  cudaError_t e = launch_quantize(a, n, codes, tab, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_quantize_magnitudes launch");
   return LYNX_OK;
 }
 

@@ -33,19 +33,37 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
   const float eps = lut.eps;
   const float* lut_lane = s_lut + lane;
 
-  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < n_rows;
-       row += n_warps) {
-    const uint32_t wa = __ldg(anchor + row * 32 + lane);
-    uint32_t wr = 0;
-    if (kFull) wr = __ldg(residual + row * 32 + lane);
+  // the next row's words and metadata are loaded before the current row is
+  // computed, so each warp keeps one row of loads in flight
+  struct RowIn {
+    uint32_t wa, wr;
+    float gmin, gs, mu, sg;
+  };
+  auto load_row = [&](int64_t row) {
+    RowIn r;
+    r.wa = __ldg(anchor + row * 32 + lane);
+    r.wr = kFull ? __ldg(residual + row * 32 + lane) : 0u;
     const int64_t page = row >> 7;
     const int ch = (int)(row & 127);
     const int blk = lane >> 2;
     const float* mp = meta + page * kMetaFloats;
-    const float gmin = __ldg(mp + ch);
-    const float dg = __fadd_rn(__ldg(mp + kH + ch), eps);
-    const float mu = __ldg(mp + kMetaMuOff + blk * kH + ch);
-    const float ds = __fadd_rn(__ldg(mp + kMetaSigmaOff + blk * kH + ch), eps);
+    r.gmin = __ldg(mp + ch);
+    r.gs = __ldg(mp + kH + ch);
+    r.mu = __ldg(mp + kMetaMuOff + blk * kH + ch);
+    r.sg = __ldg(mp + kMetaSigmaOff + blk * kH + ch);
+    return r;
+  };
+  int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  RowIn nxt{};
+  if (row < n_rows) nxt = load_row(row);
+  for (; row < n_rows; row += n_warps) {
+    const RowIn cur = nxt;
+    if (row + n_warps < n_rows) nxt = load_row(row + n_warps);
+    const uint32_t wa = cur.wa, wr = cur.wr;
+    const float gmin = cur.gmin;
+    const float dg = __fadd_rn(cur.gs, eps);
+    const float mu = cur.mu;
+    const float ds = __fadd_rn(cur.sg, eps);
 
     float xv[8];
 #pragma unroll

@@ -53,6 +53,7 @@ _PP = ctypes.POINTER(lynx_params_t)
 SIGNATURES = {
     "lynx_encode_pages": (_I32, [_VP, _I64, _PP, _VP, _VP, _VP, _VP]),
     "lynx_reconstruct": (_I32, [_VP, _VP, _VP, _I64, _PP, _VP, _I32, _VP]),
+    "lynx_quantize_magnitudes": (_I32, [_VP, _I64, _PP, _VP, _VP]),
     "lynx_decode_attn": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                 _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "lynx_decode_attn_bf16": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I64, _VP, _I32,
@@ -128,6 +129,17 @@ def lynx_encode_pages(x, params: Params = Params(), anchor=None, residual=None, 
     _check(load().lynx_encode_pages(_ptr(x), n, ctypes.byref(p), _ptr(anchor), _ptr(residual),
                                     _ptr(meta), _stream(stream)), "lynx_encode_pages")
     return anchor, residual, meta
+
+
+def lynx_quantize_magnitudes(a, params: Params = Params(), codes=None, stream=None):
+    """Stage 3 alone: 7-bit magnitude codes (uint8) of float32 magnitudes a."""
+    _need(a, torch.float32, "a")
+    codes = codes if codes is not None else torch.empty(a.shape, dtype=torch.uint8, device=a.device)
+    _need(codes, torch.uint8, "codes")
+    p = params.c()
+    _check(load().lynx_quantize_magnitudes(_ptr(a), a.numel(), ctypes.byref(p), _ptr(codes),
+                                           _stream(stream)), "lynx_quantize_magnitudes")
+    return codes
 
 
 def lynx_reconstruct(anchor, residual, meta, params: Params = Params(), out=None,
