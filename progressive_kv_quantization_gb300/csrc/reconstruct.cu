@@ -1,13 +1,17 @@
 // lynx_reconstruct kernels: the Anchor-phase and Residual-phase dequantisation
 // of the Lynx paper (§4.2; inverse compander of Eq. (4)).
 //
-// Work mapping.  One warp owns one channel row (256 tokens) of a page; lane L
-// owns tokens 8L .. 8L+7, which are one 32-bit word of each 4-bit plane
-// (coalesced 128-byte warp loads) and 16 bytes of BF16 output (coalesced
-// 512-byte warp stores).  The per-element inverse compander is a table
-// lookup in shared memory with one copy of the table per lane (entry e of
-// lane L at word e*32 + L), so a warp's lookups never share a bank.  The two
-// affine steps are fused multiply-adds:
+// Work mapping.  A CTA of 8 warps takes 8 consecutive channel rows of a page
+// (a row octet) at a time; warp w owns row w, lane L owns tokens 8L .. 8L+7,
+// which are one 32-bit word of each 4-bit plane (coalesced 128-byte warp
+// loads) and 16 bytes of BF16 output (coalesced 512-byte warp stores).  The
+// octet's chunk-major metadata (mu[8 chunks][8 rows], sigma likewise: eight
+// 32-byte runs each) is loaded once by the CTA into shared memory, double
+// buffered with one barrier per octet; the next octet's plane words and
+// metadata are loaded before the current octet is computed.  The inverse
+// compander is a shared-memory table lookup with one copy of the table per
+// lane (entry e of lane L at word e*32 + L), so lookups never share a bank.
+// The two affine steps are fused multiply-adds, two tokens at a time:
 //   x = fmaf(fmaf(S*l(I_hat), sigma+eps, mu), gamma_scale+eps, gamma_min).
 
 #include "lynx_internal.cuh"
@@ -20,89 +24,114 @@ namespace {
 template <bool kFull, bool kF32>
 __global__ void __launch_bounds__(256)
 reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restrict__ residual,
-                   const float* __restrict__ meta, int64_t n_rows, void* __restrict__ out,
+                   const float* __restrict__ meta, int64_t n_octets, void* __restrict__ out,
                    const LutTables lut) {
   constexpr int kEntries = kFull ? 256 : 16;
   __shared__ float s_lut[kEntries * 32];
+  __shared__ float s_meta[2][4][64];       // [buffer][gmin, gscale, mu, sigma][chunk * 8 + row]
   for (int i = threadIdx.x; i < kEntries * 32; i += blockDim.x)
     s_lut[i] = kFull ? lut.full[i >> 5] : lut.anc16[i >> 5];
-  __syncthreads();
 
-  const int lane = threadIdx.x & 31;
-  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int tid = threadIdx.x;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
   const float eps = lut.eps;
   const float* lut_lane = s_lut + lane;
 
-  // the next row's words and metadata are loaded before the current row is
-  // computed, so each warp keeps one row of loads in flight
-  struct RowIn {
-    uint32_t wa, wr;
-    float gmin, gs, mu, sg;
+  // metadata of octet o: thread tid < 128 loads one value (kind = tid >> 5 ... see below)
+  auto load_meta = [&](int64_t o) {
+    float v = 0.0f;
+    if (tid < 144) {
+      const float* mp = meta + (o >> 4) * kMetaFloats;
+      const int ch0 = 8 * (int)(o & 15);
+      if (tid < 64) {                      // mu[chunk][row]
+        v = __ldg(mp + kMetaMuOff + (tid >> 3) * kH + ch0 + (tid & 7));
+      } else if (tid < 128) {              // sigma[chunk][row]
+        const int i = tid - 64;
+        v = __ldg(mp + kMetaSigmaOff + (i >> 3) * kH + ch0 + (i & 7));
+      } else {                             // gamma_min[row], gamma_scale[row]
+        const int i = tid - 128;
+        v = __ldg(mp + (i >> 3) * kH + ch0 + (i & 7));
+      }
+    }
+    return v;
   };
-  auto load_row = [&](int64_t row) {
-    RowIn r;
-    r.wa = __ldg(anchor + row * 32 + lane);
-    r.wr = kFull ? __ldg(residual + row * 32 + lane) : 0u;
-    const int64_t page = row >> 7;
-    const int ch = (int)(row & 127);
-    const int blk = lane >> 2;
-    const float* mp = meta + page * kMetaFloats;
-    r.gmin = __ldg(mp + ch);
-    r.gs = __ldg(mp + kH + ch);
-    r.mu = __ldg(mp + kMetaMuOff + blk * kH + ch);
-    r.sg = __ldg(mp + kMetaSigmaOff + blk * kH + ch);
-    return r;
+  auto store_meta = [&](int buf, float v) {
+    if (tid < 64) s_meta[buf][2][tid] = v;
+    else if (tid < 128) s_meta[buf][3][tid - 64] = v;
+    else if (tid < 144) s_meta[buf][(tid - 128) >> 3][tid & 7] = v;
   };
-  int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  RowIn nxt{};
-  if (row < n_rows) nxt = load_row(row);
-  for (; row < n_rows; row += n_warps) {
-    const RowIn cur = nxt;
-    if (row + n_warps < n_rows) nxt = load_row(row + n_warps);
-    const uint32_t wa = cur.wa, wr = cur.wr;
-    const float gmin = cur.gmin;
-    const float dg = __fadd_rn(cur.gs, eps);
-    const float mu = cur.mu;
-    const float ds = __fadd_rn(cur.sg, eps);
 
-    float xv[8];
+  const int64_t stride = gridDim.x;
+  int64_t o = blockIdx.x;
+  uint32_t wa_n = 0, wr_n = 0;
+  if (o < n_octets) {
+    store_meta(0, load_meta(o));
+    const int64_t row = 8 * o + w;
+    wa_n = __ldg(anchor + row * 32 + lane);
+    if (kFull) wr_n = __ldg(residual + row * 32 + lane);
+  }
+  __syncthreads();
+  int buf = 0;
+  for (; o < n_octets; o += stride, buf ^= 1) {
+    const int64_t row = 8 * o + w;
+    const uint32_t wa = wa_n, wr = wr_n;
+    const int64_t on = o + stride;
+    float mnext = 0.0f;
+    if (on < n_octets) {
+      mnext = load_meta(on);
+      wa_n = __ldg(anchor + (8 * on + w) * 32 + lane);
+      if (kFull) wr_n = __ldg(residual + (8 * on + w) * 32 + lane);
+    }
+    const int blk = lane >> 2;
+    const float gmin = s_meta[buf][0][w];
+    const float dgv = __fadd_rn(s_meta[buf][1][w], eps);
+    const float muv = s_meta[buf][2][blk * 8 + w];
+    const float dsv = __fadd_rn(s_meta[buf][3][blk * 8 + w], eps);
+    const float2 ds2 = make_float2(dsv, dsv), mu2 = make_float2(muv, muv);
+    const float2 dg2 = make_float2(dgv, dgv), gm2 = make_float2(gmin, gmin);
+    float2 xv[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t code = (wa >> (4 * k)) & 0xFu;
-      if (kFull) code |= ((wr >> (4 * k)) & 0xFu) << 4;
-      const float l = lut_lane[code * 32];
-      xv[k] = __fmaf_rn(__fmaf_rn(l, ds, mu), dg, gmin);
+    for (int k = 0; k < 4; ++k) {
+      uint32_t c0 = (wa >> (8 * k)) & 0xFu, c1 = (wa >> (8 * k + 4)) & 0xFu;
+      if (kFull) {
+        c0 |= ((wr >> (8 * k)) & 0xFu) << 4;
+        c1 |= ((wr >> (8 * k + 4)) & 0xFu) << 4;
+      }
+      const float2 l = make_float2(lut_lane[c0 * 32], lut_lane[c1 * 32]);
+      xv[k] = __ffma2_rn(__ffma2_rn(l, ds2, mu2), dg2, gm2);
     }
     if (kF32) {
-      float4* o = reinterpret_cast<float4*>(out) + row * 64 + lane * 2;
-      o[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-      o[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+      float4* op = reinterpret_cast<float4*>(out) + row * 64 + lane * 2;
+      op[0] = make_float4(xv[0].x, xv[0].y, xv[1].x, xv[1].y);
+      op[1] = make_float4(xv[2].x, xv[2].y, xv[3].x, xv[3].y);
     } else {
       uint32_t pk[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(xv[2 * j], xv[2 * j + 1]);
-        pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(xv[k].x, xv[k].y);
+        pk[k] = *reinterpret_cast<const uint32_t*>(&h);
       }
       reinterpret_cast<uint4*>(out)[row * 32 + lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+    if (on < n_octets) store_meta(buf ^ 1, mnext);
+    __syncthreads();
   }
 }
 
 template <bool kFull, bool kF32>
 cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                    int64_t n_pages, void* out, const LutTables* lut, cudaStream_t s) {
-  const int64_t n_rows = n_pages * kH;
+  const int64_t n_octets = n_pages * (kH / 8);
   const int threads = 256;
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_kernel<kFull, kF32>, threads, 0);
   if (per_sm < 1) per_sm = 1;
   const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
-  const int64_t need = (n_rows + 7) / 8;
-  const int blocks = (int)(need < max_blocks ? need : max_blocks);
+  const int blocks = (int)(n_octets < max_blocks ? n_octets : max_blocks);
   reconstruct_kernel<kFull, kF32><<<blocks, threads, 0, s>>>(
       reinterpret_cast<const uint32_t*>(anchor), reinterpret_cast<const uint32_t*>(residual), meta,
-      n_rows, out, *lut);
+      n_octets, out, *lut);
   return cudaGetLastError();
 }
 
