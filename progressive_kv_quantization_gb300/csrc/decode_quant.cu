@@ -56,10 +56,10 @@ struct QGeo {
 static_assert(QGeo<false>::kUnit % 1024 == 0 && QGeo<true>::kUnit % 1024 == 0,
               "ring slots must keep the 1024-byte alignment of swizzled tiles");
 
-// per consumer warp: coefficients [128][8] f32, partial logits [8 groups][32] f32x4,
+// per consumer warp: coefficients [128][4 rows] f32, partial logits [8 groups][32] f32x4,
 // probabilities [16 pairs] f32x4 for rows 0-1 and 2-3
 constexpr int kWarpCoef = 0;
-constexpr int kWarpPart = kWarpCoef + kH * 8 * 4;
+constexpr int kWarpPart = kWarpCoef + kH * 4 * 4;
 constexpr int kWarpPs01 = kWarpPart + 8 * 32 * 16;
 constexpr int kWarpPs23 = kWarpPs01 + 16 * 16;
 constexpr int kWarpBytes = kWarpPs23 + 16 * 16;
@@ -342,9 +342,8 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
           const float A = __fmaf_rn(dg, mu, gmin);
           const float Bc = __fmul_rn(dg, ds);
           const float4 q = lds<float4>(smem, s_qs + 16 * d);
-          float* cf = reinterpret_cast<float*>(smem + s_coef + 32 * d);
-          reinterpret_cast<float4*>(cf)[0] = make_float4(q.x * Bc, q.x * Bc, q.y * Bc, q.y * Bc);
-          reinterpret_cast<float4*>(cf)[1] = make_float4(q.z * Bc, q.z * Bc, q.w * Bc, q.w * Bc);
+          *reinterpret_cast<float4*>(smem + s_coef + 16 * d) =
+              make_float4(q.x * Bc, q.y * Bc, q.z * Bc, q.w * Bc);
           ck[0] = __fmaf_rn(q.x, A, ck[0]);
           ck[1] = __fmaf_rn(q.y, A, ck[1]);
           ck[2] = __fmaf_rn(q.z, A, ck[2]);
@@ -363,15 +362,14 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
 #pragma unroll
           for (int k = 0; k < 4; ++k) acc[r][k] = make_float2(0.f, 0.f);
         const uint32_t pa = unitK + k_off;
-        const uint32_t cbase = s_coef + 32 * cg;
+        const uint32_t cbase = s_coef + 16 * cg;
 #pragma unroll 4
         for (int j = 0; j < 16; ++j) {
           const uint32_t wa = lds<uint32_t>(smem, pa + j * 1024);
           const uint32_t wr = FULL ? lds<uint32_t>(smem, pa + G::kResOff + j * 1024) : 0u;
-          const float4 c01 = lds<float4>(smem, cbase + j * 256);
-          const float4 c23 = lds<float4>(smem, cbase + j * 256 + 16);
-          const float2 cc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
-                                make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+          const float4 c = lds<float4>(smem, cbase + j * 128);       // channel cg + 8j, rows 0-3
+          const float2 cc[4] = {make_float2(c.x, c.x), make_float2(c.y, c.y),
+                                make_float2(c.z, c.z), make_float2(c.w, c.w)};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float2 lv = lut_pair<FULL>(lut_lane, wa, wr, k);
