@@ -46,6 +46,13 @@ N_LAYERS, HKV, HQ, N_TOK = 64, 8, 32, 16384
 NPPH = N_TOK // 256                 # pages per head
 PER = HKV * NPPH                    # pages per tensor per layer (512)
 N_PAGES = 2 * N_LAYERS * PER        # 65536
+
+
+def set_layers(n):
+    """Smaller caches (fewer layers) for profiling captures."""
+    global N_LAYERS, N_PAGES
+    N_LAYERS = n
+    N_PAGES = 2 * N_LAYERS * PER
 PLANE, META, PAGE = 16384, 9216, 65536
 
 # per-page byte counts (headline, moved) of each kernel
@@ -240,6 +247,8 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", local)
     b = build_buffers(torch, L, inputs, dev, seed=rank)
     ks = kernel_list(torch, L, b)
+    if args.only:
+        ks = [k for k in ks if k[0] in args.only.split(",")]
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -298,7 +307,7 @@ def run_gpu(args, rank, world):
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["GBps_moved"], "peak": gbps_peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_of_hbm"],
             "traffic": profile_traffic(dom), "source": src}
-    e2e = run_e2e(torch, L, b, ks, args, dev) if rank == 0 else None
+    e2e = run_e2e(torch, L, b, ks, args, dev) if rank == 0 and not args.no_e2e else None
     if rank != 0:
         return None
     launches = args.steps * sum(k[2] for k in ks)
@@ -306,12 +315,13 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "pages": N_PAGES, "bf16_bytes": N_PAGES * PAGE,
+        "config": {"workload": WORKLOAD if N_LAYERS == 64 else WORKLOAD.replace("64 layers", f"{N_LAYERS} layers"),
+                   "pages": N_PAGES, "bf16_bytes": N_PAGES * PAGE,
                    "l2": "inputs larger than L2 (4.29e9 B cache), no flush",
                    "alpha": 100.0, "eps": 1e-6, "parallelism": f"replicas x{world} (one cache per GPU)"},
         "kernels": kern,
-        "encode_GBps_bf16_in": kern["encode"]["GBps_headline"],
-        "decode_anchor_GBps_packed": kern["decode_anchor_b1"]["GBps_headline"],
+        "encode_GBps_bf16_in": kern.get("encode", {}).get("GBps_headline"),
+        "decode_anchor_GBps_packed": kern.get("decode_anchor_b1", {}).get("GBps_headline"),
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -452,7 +462,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-only-seconds", type=float, default=None)
+    ap.add_argument("--layers", type=int, default=64, help="cache layers (64 = the benchmark workload)")
+    ap.add_argument("--only", default="", help="comma-separated kernel names to run (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
+    if args.layers != 64:
+        set_layers(args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
 

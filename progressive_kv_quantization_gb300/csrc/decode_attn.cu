@@ -691,11 +691,13 @@ cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t 
 }  // namespace
 
 DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
-  (void)mode;
   DecodePlan pl{};
   const int G = Hq / Hkv;
   pl.n_rg = (T * G + kRows - 1) / kRows;
   const int64_t units = (int64_t)B * Hkv * pl.n_rg;
+  // CTAs per split: the tensor-core kernel takes four row groups per CTA
+  const bool mma = mode != kModeBf16 && use_mma_rows(T * G);
+  const int64_t cta_units = mma ? (int64_t)B * Hkv * ((pl.n_rg + 3) / 4) : units;
   const int64_t resident = device_sm_count();   // one CTA per SM (shared-memory bound)
   int best_s = 1;
   double best = 1e300;
@@ -704,7 +706,7 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
     const int pps = (max_pages + s - 1) / s;
     const int s_eff = (max_pages + pps - 1) / pps;
     if (s_eff != s) continue;
-    const int64_t ctas = units * s_eff;
+    const int64_t ctas = cta_units * s_eff;
     const int64_t waves = (ctas + resident - 1) / resident;
     const double cost = (double)waves * (pps + 2.0);
     if (cost < best - 1e-9) {

@@ -94,6 +94,7 @@ struct DecodePlan {
 
 DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode);
 bool n_pool_too_large(int64_t n_pool);
+bool use_mma_rows(int rows);
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);
 

@@ -128,6 +128,25 @@ def test_odd_group_sizes_and_tiny_contexts(cuda_device, llama_pools, mode):
         check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
 
 
+@pytest.mark.parametrize("mode", ["anchor", "full", "bf16"])
+@pytest.mark.parametrize("T", [5, 7])
+def test_sixteen_row_tiles_ragged(cuda_device, llama_pools, mode, T):
+    """G = 3, T = 5 or 7: 15 or 21 query rows per KV head, so the last 16-row
+    tile of the tensor-core path is partly empty and its last 4-row group is
+    ragged; contexts include 0 keys, fewer keys than T and a partial page."""
+    B, Hkv = 5, 2
+    Hq = 3 * Hkv
+    ctx = np.array([0, T - 2, 1000, 4099, 1])
+    table = np.stack([contiguous_table(1, Hkv, 20, 64, offset=3 * b)[0] for b in range(B)])
+    q = inputs.queries_np((B, T, Hq, 128), 300 + T)
+    for causal in (False, True):
+        o, lse = run(llama_pools, mode, q, table, ctx, Hkv, causal)
+        ro, rl = reference(llama_pools, mode, q, table, ctx, Hkv, causal)
+        empty = np.isnan(ro[..., 0])
+        assert np.all(o[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
+        check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
+
+
 def test_scale_and_shared_pages(cuda_device, llama_pools):
     """Eight sequences whose page tables point at overlapping pages (as eight
     sequences realised over a multi-layer cache), with a non-default scale."""
