@@ -1,0 +1,161 @@
+// Shared pieces of the two quantised-KV decode kernels (CUDA-core and
+// tensor-core): the page-unit geometry of the shared-memory ring, PTX helpers
+// for mbarriers, TMA and bulk copies, and the producer lane that streams a
+// split's K and V units through the ring.
+#pragma once
+
+#include "lynx_internal.cuh"
+
+#include <cuda.h>
+#include <math_constants.h>
+
+namespace lynx {
+
+// 2-D tensor map over a pool of 4-bit planes (rows of 128 bytes, one 128 x 128
+// tile per page, 128-byte swizzle); false if the driver refuses it
+bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool);
+
+namespace {
+
+constexpr int kConsumers = 8;
+constexpr int kThreadsQ = (kConsumers + 1) * 32;
+constexpr int kRows = 4;
+constexpr int kWsPerCta = kRows * kH + 2 * kRows;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+template <bool FULL>
+struct QGeo {
+  static constexpr int kStages = 3;
+  static constexpr int kUnit = FULL ? 2 * kPlaneBytes + kMetaBytes : kPlaneBytes + kMetaBytes;
+  static constexpr int kResOff = kPlaneBytes;
+  static constexpr int kMetaOff = FULL ? 2 * kPlaneBytes : kPlaneBytes;
+  // anchor: byte -> (value of low nibble, value of high nibble), 32 copies (entry stride 256 B)
+  // full:   8-bit code -> value, 32 copies (entry stride 128 B)
+  static constexpr int kLutBytes = FULL ? 256 * 32 * 4 : 256 * 32 * 8;
+};
+static_assert(QGeo<false>::kUnit % 1024 == 0 && QGeo<true>::kUnit % 1024 == 0,
+              "ring slots must keep the 1024-byte alignment of swizzled tiles");
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// gives up after kWaitNs (clock checked every 256 polls) or 2^26 polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_tile_g2s(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ T lds(const uint8_t* smem, uint32_t off) {
+  return *reinterpret_cast<const T*>(smem + off);
+}
+
+// Producer lane of a decode CTA: streams the K and V units of pages
+// [p_begin, p_begin + np) of one page-table row through the kStages-slot ring.
+// Unit u (K of page u/2 for even u, V for odd u) goes to slot u % kStages once
+// the consumers released that slot's previous unit.  An out-of-range page id
+// is reported (status 2) and page 0 read instead.  A wait that gives up sets
+// status 1 and the CTA's abort flag, then waits (bounded) for the copies
+// already in flight to land before returning.
+template <bool FULL>
+__device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np,
+                              uint32_t s_ring, uint32_t bar_full, uint32_t bar_empty,
+                              const CUtensorMap* tm_ka, const CUtensorMap* tm_va,
+                              const CUtensorMap* tm_kr, const CUtensorMap* tm_vr, int* s_flag) {
+  using G = QGeo<FULL>;
+  constexpr int kSt = G::kStages;
+  int issued = 0;
+  bool ok = true;
+  for (int u = 0; u < 2 * np; ++u) {
+    const int st = u % kSt;
+    if (u >= kSt && !mbar_wait(bar_empty + 8 * st, ((u / kSt) - 1) & 1)) {
+      ok = false;
+      break;
+    }
+    const int p = p_begin + (u >> 1);
+    const bool is_v = (u & 1) != 0;
+    int64_t id = pt_row[p];
+    if (id < 0 || id >= a.n_pool) {
+      atomicExch(a.status, 2);
+      id = 0;
+    }
+    const uint32_t dst = s_ring + st * G::kUnit;
+    const uint32_t bar = bar_full + 8 * st;
+    mbar_expect_tx(bar, G::kUnit);
+    tma_tile_g2s(dst, is_v ? tm_va : tm_ka, 0, (int)(id * kH), bar);
+    if (FULL) tma_tile_g2s(dst + G::kResOff, is_v ? tm_vr : tm_kr, 0, (int)(id * kH), bar);
+    bulk_g2s(dst + G::kMetaOff, (is_v ? a.v_meta : a.k_meta) + id * kMetaFloats, kMetaBytes, bar);
+    ++issued;
+  }
+  if (!ok) {
+    atomicExch(a.status, 1);
+    *s_flag = 1;
+    // the newest issue of every slot must land before the CTA leaves
+    for (int u = issued - 1; u >= 0 && u >= issued - kSt; --u)
+      mbar_wait(bar_full + 8 * (u % kSt), (u / kSt) & 1);
+  }
+}
+
+}  // namespace
+}  // namespace lynx

@@ -1,0 +1,533 @@
+// Tensor-core verification attention over Lynx-encoded pages: the attention
+// of the Lynx paper (§2.1) run on the KV that the Anchor phase (draft) or the
+// Anchor and Residual phases (verification) of §4.2-4.3 deliver, for 16 of
+// the query rows that share one KV head (T tokens x Hq/Hkv heads) per CTA.
+//
+// CTA skeleton as in the CUDA-core kernel: a producer lane streams the split's
+// K and V page units through a 3-slot shared-memory ring (2-D TMA tile for the
+// planes, bulk copy for the metadata); 8 consumer warps, warp w owning the
+// 32-token chunk w of every page with its own online softmax; one merge of the
+// 8 chunk states at the end.
+//
+// Each chunk's two contractions run on the tensor cores (mma.sync, float32
+// accumulation); the rows sharing one KV head make both a dense contraction.
+//
+//   K side   S[16 rows x 32 tokens] = Q K^T as TF32 m16n8k8 over 16 k-steps of
+//            8 channels.  Q (BF16) is exact in TF32.  k = A + B l~ is
+//            dequantised in float32 (A = gamma_min + (gamma_scale + eps) mu,
+//            B = (gamma_scale + eps)(sigma + eps), the chunk's affine
+//            constants) and split into its TF32 head and the float32
+//            remainder, two MMAs, so each product keeps ~21 bits.  Per 16
+//            tokens one n-tile holds the even and one the odd tokens, so one
+//            table lookup per packed byte feeds both.
+//   V side   U[128 channels x 16 rows] = l~ P^T as fp16 m16n8k16, two k-steps
+//            of 16 tokens, then folded into the output with the chunk's
+//            constants: O = O corr + A psum + B U.  l~ comes from a table of
+//            fp16 head/remainder pairs (two MMAs, ~22 bits); P is fp16, scaled
+//            by 2^10 away from fp16 subnormals (O and the row sums carry the
+//            2^10, removed once at the end).  Slot order of k-step q16: slots
+//            2t, 2t+1 hold tokens 16 q16 + 4t + {0, 1}, slots 2t+8, 2t+9 hold
+//            16 q16 + 4t + {2, 3}.  With that order the A fragments are packed
+//            bytes as stored (both tokens of a byte in one register) and the P
+//            fragments are S accumulator entries the lane holds already.
+//
+// Lane (g = L >> 2, t = L & 3) holds S of rows g and g+8 for tokens
+// 16 q16 + 4t + j (j = 0..3) of its chunk.
+//
+// Rounding: P is rounded to fp16 (relative 2^-11); everything else keeps at
+// least ~21 bits, sums are float32.
+
+#include "decode_common.cuh"
+
+#include <cuda_fp16.h>
+
+namespace lynx {
+namespace {
+
+constexpr int kTcRows = 16;
+constexpr int kTcWarpBytes = kH * 8;   // per warp: float2 (A, B) per channel of the current unit
+
+template <bool FULL>
+struct TLayout {
+  using G = QGeo<FULL>;
+  static constexpr int kRing = 0;
+  // Tables, 32 copies (one per lane) in rows of 256 B, row = byte or code.
+  //   anchor  kLutK: byte -> (l~ low nibble, l~ high nibble) float2, copy at 8L
+  //           kLutV: byte -> fp16 pairs (heads, remainders), copy at 8L
+  //   full    kLutK: code -> l~ float, copy at 4L; fp16 (head, remainder) at 128 + 4L
+  static constexpr int kLutK = kRing + G::kStages * G::kUnit;
+  static constexpr int kLutV = FULL ? kLutK : kLutK + 256 * 256;
+  static constexpr int kWarps = kLutV + 256 * 256;
+  static constexpr int kQ = kWarps + kConsumers * kTcWarpBytes;   // uint4 [16 k-steps][32 lanes]
+  static constexpr int kFlag = kQ + 16 * 32 * 16;
+  static constexpr int kBar = kFlag + 16;
+  static constexpr int kTotal = kBar + 2 * G::kStages * 8;
+  static constexpr int kAlloc = kTotal + 1024;
+  // end-of-kernel merge area (reuses the ring): m[8][16], l[8][16], o[8][16][128]
+  static constexpr int kMergeM = 0;
+  static constexpr int kMergeL = kMergeM + kConsumers * kTcRows * 4;
+  static constexpr int kMergeO = kMergeL + kConsumers * kTcRows * 4;
+  static_assert(kMergeO + kConsumers * kTcRows * kH * 4 <= G::kStages * G::kUnit, "merge area");
+};
+static_assert(TLayout<false>::kAlloc <= 232448, "shared memory (anchor, tensor core)");
+static_assert(TLayout<true>::kAlloc <= 232448, "shared memory (full, tensor core)");
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// TF32 head (low 13 mantissa bits cleared) and the exact float32 remainder
+__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+__device__ __forceinline__ uint32_t tf32_lo(float x) {
+  return __float_as_uint(x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u));
+}
+
+// fp16 pair, `lo` in the low half (the lower k index of a fragment register)
+__device__ __forceinline__ uint32_t h2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2(__half lo, __half hi) {
+  const __half2 v = __halves2half2(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// table offset for byte j of `word`: the byte in bits 8..15, the lane's copy
+// offset (< 256) in bits 0..7
+__device__ __forceinline__ uint32_t byte_sel(uint32_t j) { return 0x5504u | (j << 4); }
+__device__ __forceinline__ uint32_t lut_off(uint32_t word, uint32_t lane_off, uint32_t sel) {
+  return prmt(word, lane_off, sel);
+}
+
+// full codes (anchor nibble | residual nibble << 4) of the even and of the odd
+// tokens of the four bytes of an anchor word and its residual word
+__device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& ev, uint32_t& od) {
+  ev = (wa & 0x0F0F0F0Fu) | ((wr << 4) & 0xF0F0F0F0u);
+  od = ((wa >> 4) & 0x0F0F0F0Fu) | (wr & 0xF0F0F0F0u);
+}
+
+template <bool FULL>
+__global__ void __launch_bounds__(kThreadsQ, 1)
+decode_tc_kernel(const DecodeArgs a, const LutTables lut,
+                 const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_va,
+                 const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr) {
+  using G = QGeo<FULL>;
+  using S = TLayout<FULL>;
+  constexpr int kSt = G::kStages;
+  constexpr int R = kTcRows;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_u32);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int L = tid & 31;
+  const int g = L >> 2, t = L & 3;
+  const int split = blockIdx.x;
+  const int TG = a.T * a.G;
+  const int n_tiles = (TG + R - 1) / R;
+  const int h = blockIdx.y / n_tiles;
+  const int row0 = (blockIdx.y % n_tiles) * R;
+  const int b = blockIdx.z;
+  const int max_keys = a.max_pages * kP;
+
+  int ctx = a.ctx_len[b];
+  if (ctx < 0 || ctx > max_keys) {
+    if (tid == 0) atomicExch(a.status, 3);
+    ctx = ctx < 0 ? 0 : max_keys;
+  }
+  // keys visible to row r of this CTA (0 for padding rows)
+  auto n_visible = [&](int r) {
+    const int row = row0 + r;
+    if (row >= TG) return 0;
+    const int n = a.causal ? ctx - a.T + row / a.G + 1 : ctx;
+    return n < 0 ? 0 : n;
+  };
+  int max_vis = 0, min_vis = max_keys;
+  for (int r = 0; r < R && row0 + r < TG; ++r) {
+    max_vis = max(max_vis, n_visible(r));
+    min_vis = min(min_vis, n_visible(r));
+  }
+  const int nv_lo = n_visible(g), nv_hi = n_visible(g + 8);
+  const int n_pages = (max_vis + kP - 1) / kP;
+  const int p_begin = split * a.pages_per_split;
+  const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
+  const int32_t* pt_row = a.page_table + ((int64_t)b * a.Hkv + h) * a.max_pages;
+
+  const uint32_t s_ring = base + S::kRing;
+  const uint32_t bar_full = base + S::kBar;
+  const uint32_t bar_empty = bar_full + 8 * kSt;
+  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
+
+  // ---- prologue: value tables, Q fragments, barriers
+  for (int i = tid; i < 256 * 32; i += kThreadsQ) {
+    const int e = i >> 5, ln = i & 31;
+    if (!FULL) {
+      const float2 v = lut.anc_pair[e];
+      const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+      const __half lx = __float2half_rn(v.x - __half2float(hx));
+      const __half ly = __float2half_rn(v.y - __half2float(hy));
+      *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+      *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+    } else {
+      const float v = lut.full[e];
+      const __half hv = __float2half_rn(v);
+      const __half lv = __float2half_rn(v - __half2float(hv));
+      *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+      *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+    }
+  }
+  // entry (ks, lane, e): row g' + 8 (e & 1), channel 8 ks + t' + 4 (e >> 1); BF16 is exact in TF32
+  for (int i = tid; i < 16 * 32 * 4; i += kThreadsQ) {
+    const int e = i & 3, ln = (i >> 2) & 31, ks = i >> 7;
+    const int row = row0 + (ln >> 2) + 8 * (e & 1);
+    const int d = 8 * ks + (ln & 3) + 4 * (e >> 1);
+    uint32_t v = 0u;
+    if (row < TG)
+      v = (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + d] << 16;
+    reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
+  }
+  if (tid == 0) {
+    for (int st = 0; st < kSt; ++st) {
+      mbar_init(bar_full + 8 * st, 1);
+      mbar_init(bar_empty + 8 * st, kConsumers);
+    }
+    *s_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  float l_run[2] = {0.0f, 0.0f};
+  float2 O[8][2][2];   // O[mt][nt][c]: channel 16 mt + g + 8c, rows 8 nt + 2t and 8 nt + 2t + 1
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) O[mt][nt][0] = O[mt][nt][1] = make_float2(0.f, 0.f);
+
+  if (warp == kConsumers) {
+    if (L == 0)
+      produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
+                          &tm_vr, s_flag);
+  } else {
+    const int w = warp;
+    const uint32_t s_ab = S::kWarps + w * kTcWarpBytes;
+    const uint32_t lane8 = 8u * L, lane4 = 4u * L, lane4v = 128u + 4u * L;
+    // K side: byte 8 q16 + g of a channel row = byte g & 3 of word 2 q16 + (g >> 2)
+    const uint32_t ksel = byte_sel(g & 3);
+    const uint32_t kword = 4 * (g >> 2);
+    // V side: bytes 8 q16 + 2t (+1) of channel 16 mt + g = bytes 2 (t & 1) (+1) of word 2 q16 + (t >> 1)
+    const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * (t >> 1);
+    const uint32_t vsel0 = byte_sel(2 * (t & 1)), vsel1 = byte_sel(2 * (t & 1) + 1);
+    const float eps = a.eps;
+    const float sc = a.scale_log2;
+    bool failed = false;
+
+    auto prep_ab = [&](uint32_t unit) {
+      const uint32_t mt = unit + G::kMetaOff;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int d = L + 32 * k;
+        const float gmin = lds<float>(smem, mt + 4 * d);
+        const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
+        const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
+        const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
+        *reinterpret_cast<float2*>(smem + s_ab + 8 * d) =
+            make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+      }
+    };
+
+    for (int i = 0; i < np && !failed; ++i) {
+      const int p = p_begin + i;
+      const int uK = 2 * i, uV = 2 * i + 1;
+      const int sK = uK % kSt, sV = uV % kSt;
+      const uint32_t unitK = S::kRing + sK * G::kUnit;
+      const uint32_t unitV = S::kRing + sV * G::kUnit;
+
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1));
+      if (failed) break;
+      prep_ab(unitK);
+      __syncwarp();
+
+      // ---- S = Q K^T: n-tile A of token group q16 = even tokens, n-tile B = odd tokens
+      float sA[2][4], sB[2][4];
+#pragma unroll
+      for (int q16 = 0; q16 < 2; ++q16)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sA[q16][e] = sB[q16][e] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks) {
+        const uint4 qf = lds<uint4>(smem, S::kQ + (ks * 32 + L) * 16);
+        const int c0 = 8 * ks + t, c1 = c0 + 4;
+        const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
+        const float2 ab1 = lds<float2>(smem, s_ab + 8 * c1);
+        const uint32_t r0 = unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword;
+        const uint32_t r1 = unitK + c1 * 128 + ((w ^ (c1 & 7)) << 4) + kword;
+#pragma unroll
+        for (int q16 = 0; q16 < 2; ++q16) {
+          const uint32_t wa0 = lds<uint32_t>(smem, r0 + 8 * q16);
+          const uint32_t wa1 = lds<uint32_t>(smem, r1 + 8 * q16);
+          float2 l0, l1;
+          if (!FULL) {
+            l0 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel));
+            l1 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel));
+          } else {
+            uint32_t e0, o0, e1, o1;
+            full_codes(wa0, lds<uint32_t>(smem, r0 + 8 * q16 + G::kResOff), e0, o0);
+            full_codes(wa1, lds<uint32_t>(smem, r1 + 8 * q16 + G::kResOff), e1, o1);
+            l0 = make_float2(lds<float>(smem, S::kLutK + lut_off(e0, lane4, ksel)),
+                             lds<float>(smem, S::kLutK + lut_off(o0, lane4, ksel)));
+            l1 = make_float2(lds<float>(smem, S::kLutK + lut_off(e1, lane4, ksel)),
+                             lds<float>(smem, S::kLutK + lut_off(o1, lane4, ksel)));
+          }
+          const float2 k0 = __ffma2_rn(l0, make_float2(ab0.y, ab0.y), make_float2(ab0.x, ab0.x));
+          const float2 k1 = __ffma2_rn(l1, make_float2(ab1.y, ab1.y), make_float2(ab1.x, ab1.x));
+          mma_tf32(sA[q16], qf.x, qf.y, qf.z, qf.w, tf32_hi(k0.x), tf32_hi(k1.x));
+          mma_tf32(sA[q16], qf.x, qf.y, qf.z, qf.w, tf32_lo(k0.x), tf32_lo(k1.x));
+          mma_tf32(sB[q16], qf.x, qf.y, qf.z, qf.w, tf32_hi(k0.y), tf32_hi(k1.y));
+          mma_tf32(sB[q16], qf.x, qf.y, qf.z, qf.w, tf32_lo(k0.y), tf32_lo(k1.y));
+        }
+      }
+      __syncwarp();
+      if (L == 0) mbar_arrive(bar_empty + 8 * sK);
+
+      // ---- online softmax: row g (rh 0, S entries 0-1) and g + 8 (rh 1, entries 2-3);
+      // token 16 q16 + 4t + j is sA[q16][2rh] (j 0), sB (j 1), sA[q16][2rh+1] (j 2), sB (j 3)
+      const int pos0 = p * kP + 32 * w + 4 * t;
+      const bool all_visible = (p + 1) * kP <= min_vis;
+      float pr[2][2][4];   // [q16][rh][j], probabilities x 2^10
+      float corr[2], psum[2];
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const int nv = rh ? nv_hi : nv_lo;
+        float mloc = -CUDART_INF_F;
+#pragma unroll
+        for (int q16 = 0; q16 < 2; ++q16) {
+          const float v4[4] = {sA[q16][2 * rh], sB[q16][2 * rh], sA[q16][2 * rh + 1], sB[q16][2 * rh + 1]};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float sv = v4[j] * sc;
+            if (!all_visible && pos0 + 16 * q16 + j >= nv) sv = -CUDART_INF_F;
+            pr[q16][rh][j] = sv;
+            mloc = fmaxf(mloc, sv);
+          }
+        }
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+        const float mnew = fmaxf(m_run[rh], mloc);
+        corr[rh] = (mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[rh] - mnew);
+        float ps = 0.0f;
+#pragma unroll
+        for (int q16 = 0; q16 < 2; ++q16)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float sv = pr[q16][rh][j];
+            const float pv = (sv == -CUDART_INF_F) ? 0.0f : exp2f(sv - mnew) * 1024.0f;
+            pr[q16][rh][j] = pv;
+            ps += pv;
+          }
+        l_run[rh] = l_run[rh] * corr[rh] + ps;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        psum[rh] = ps;
+        m_run[rh] = mnew;
+      }
+      // P^T fragments of k-step q16, n-tile nt (rows 8 nt + g): tokens 16 q16 + 4t + {0,1} and + {2,3}
+      uint32_t pb[2][2][2];
+#pragma unroll
+      for (int q16 = 0; q16 < 2; ++q16)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          pb[q16][nt][0] = h2(pr[q16][nt][0], pr[q16][nt][1]);
+          pb[q16][nt][1] = h2(pr[q16][nt][2], pr[q16][nt][3]);
+        }
+      // statistics of U's columns: rows 8 nt + 2t + e live in lane 8t + 4e
+      float2 cr[2], pss[2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        cr[nt] = make_float2(__shfl_sync(0xffffffffu, corr[nt], 8 * t),
+                             __shfl_sync(0xffffffffu, corr[nt], 8 * t + 4));
+        pss[nt] = make_float2(__shfl_sync(0xffffffffu, psum[nt], 8 * t),
+                              __shfl_sync(0xffffffffu, psum[nt], 8 * t + 4));
+      }
+      const bool rescale = __any_sync(0xffffffffu, corr[0] != 1.0f || corr[1] != 1.0f);
+
+      // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1));
+      if (failed) break;
+      prep_ab(unitV);
+      __syncwarp();
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int c0 = 16 * mt + g;
+        const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
+        const float2 ab1 = lds<float2>(smem, s_ab + 8 * (c0 + 8));
+        const uint32_t off = unitV + mt * 2048 + vofs;
+        float u[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) u[nt][e] = 0.0f;
+#pragma unroll
+        for (int q16 = 0; q16 < 2; ++q16) {
+          const uint32_t wa0 = lds<uint32_t>(smem, off + 8 * q16);
+          const uint32_t wa1 = lds<uint32_t>(smem, off + 1024 + 8 * q16);
+          // (head pair, remainder pair) of bytes j0 = 2 (t & 1) and j1 = j0 + 1 of rows c0, c0 + 8
+          uint2 x00, x10, x01, x11;
+          if (!FULL) {
+            x00 = lds<uint2>(smem, S::kLutV + lut_off(wa0, lane8, vsel0));
+            x10 = lds<uint2>(smem, S::kLutV + lut_off(wa1, lane8, vsel0));
+            x01 = lds<uint2>(smem, S::kLutV + lut_off(wa0, lane8, vsel1));
+            x11 = lds<uint2>(smem, S::kLutV + lut_off(wa1, lane8, vsel1));
+          } else {
+            uint32_t e0, o0, e1, o1;
+            full_codes(wa0, lds<uint32_t>(smem, off + 8 * q16 + G::kResOff), e0, o0);
+            full_codes(wa1, lds<uint32_t>(smem, off + 1024 + 8 * q16 + G::kResOff), e1, o1);
+            auto pair = [&](uint32_t ev, uint32_t od, uint32_t sel) {
+              const uint32_t he = lds<uint32_t>(smem, S::kLutV + lut_off(ev, lane4v, sel));
+              const uint32_t ho = lds<uint32_t>(smem, S::kLutV + lut_off(od, lane4v, sel));
+              return make_uint2(prmt(he, ho, 0x5410u), prmt(he, ho, 0x7632u));
+            };
+            x00 = pair(e0, o0, vsel0);
+            x10 = pair(e1, o1, vsel0);
+            x01 = pair(e0, o0, vsel1);
+            x11 = pair(e1, o1, vsel1);
+          }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            mma_f16(u[nt], x00.x, x10.x, x01.x, x11.x, pb[q16][nt][0], pb[q16][nt][1]);
+            mma_f16(u[nt], x00.y, x10.y, x01.y, x11.y, pb[q16][nt][0], pb[q16][nt][1]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float2 o0 = O[mt][nt][0], o1 = O[mt][nt][1];
+          if (rescale) {
+            o0 = __fmul2_rn(o0, cr[nt]);
+            o1 = __fmul2_rn(o1, cr[nt]);
+          }
+          o0 = __ffma2_rn(make_float2(ab0.x, ab0.x), pss[nt], o0);
+          o1 = __ffma2_rn(make_float2(ab1.x, ab1.x), pss[nt], o1);
+          O[mt][nt][0] = __ffma2_rn(make_float2(ab0.y, ab0.y), make_float2(u[nt][0], u[nt][1]), o0);
+          O[mt][nt][1] = __ffma2_rn(make_float2(ab1.y, ab1.y), make_float2(u[nt][2], u[nt][3]), o1);
+        }
+      }
+      __syncwarp();
+      if (L == 0) mbar_arrive(bar_empty + 8 * sV);
+    }
+    if (failed && L == 0) {
+      atomicExch(a.status, 1);
+      *s_flag = 1;
+    }
+  }
+
+  // ================= merge the 8 chunk states (the ring is idle now)
+  __syncthreads();
+  if (*reinterpret_cast<volatile int*>(s_flag) != 0) return;
+  float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
+  float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
+  float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
+  if (warp < kConsumers) {
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
+      float lw = l_run[rh];
+      lw += __shfl_xor_sync(0xffffffffu, lw, 1);
+      lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+      if (t == 0) {
+        mm[warp * R + g + 8 * rh] = m_run[rh];
+        ml[warp * R + g + 8 * rh] = lw;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int r = warp * R + 8 * nt + 2 * t;
+        const int c0 = 16 * mt + g;
+        mo[r * kH + c0] = O[mt][nt][0].x;
+        mo[(r + 1) * kH + c0] = O[mt][nt][0].y;
+        mo[r * kH + c0 + 8] = O[mt][nt][1].x;
+        mo[(r + 1) * kH + c0 + 8] = O[mt][nt][1].y;
+      }
+  }
+  __syncthreads();
+  for (int i = tid; i < R * kH; i += kThreadsQ) {
+    const int r = i >> 7, d = i & 127;
+    const int row = row0 + r;
+    const int rg4 = row >> 2;
+    if (rg4 >= a.n_rg) continue;
+    float mstar = -CUDART_INF_F;
+#pragma unroll
+    for (int ww = 0; ww < kConsumers; ++ww) mstar = fmaxf(mstar, mm[ww * R + r]);
+    float o = 0.0f, l = 0.0f;
+    if (mstar != -CUDART_INF_F) {
+#pragma unroll
+      for (int ww = 0; ww < kConsumers; ++ww) {
+        const float mw = mm[ww * R + r];
+        if (mw == -CUDART_INF_F) continue;
+        const float f = exp2f(mw - mstar);
+        o += mo[(ww * R + r) * kH + d] * f;
+        l += ml[ww * R + r] * f;
+      }
+    }
+    // the 2^10 scale of the probabilities cancels in o / l; remove it from both
+    const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
+    float* ws = a.ws + cta * kWsPerCta;
+    ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
+    if (d == 0) {
+      ws[kRows * kH + (row & 3)] = mstar;
+      ws[kRows * kH + kRows + (row & 3)] = l * (1.0f / 1024.0f);
+    }
+  }
+}
+
+template <bool FULL>
+cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
+  constexpr int kSmem = TLayout<FULL>::kAlloc;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FULL>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  CUtensorMap tka, tva, tkr, tvr;
+  if (n_pool_too_large(a.n_pool)) return cudaErrorInvalidValue;
+  if (!plane_map(&tka, a.k_anc, a.n_pool) || !plane_map(&tva, a.v_anc, a.n_pool))
+    return cudaErrorInvalidValue;
+  if (FULL) {
+    if (!plane_map(&tkr, a.k_res, a.n_pool) || !plane_map(&tvr, a.v_res, a.n_pool))
+      return cudaErrorInvalidValue;
+  } else {
+    tkr = tka;
+    tvr = tva;
+  }
+  dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + kTcRows - 1) / kTcRows), a.B);
+  decode_tc_kernel<FULL><<<grid, kThreadsQ, kSmem, s>>>(a, *lut, tka, tva, tkr, tvr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool use_tc_rows(int rows) { return rows >= 12; }
+int tc_rows_per_cta(int) { return kTcRows; }
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
+  return full ? launch_tc<true>(a, lut, s) : launch_tc<false>(a, lut, s);
+}
+
+}  // namespace lynx
