@@ -226,11 +226,31 @@ def profile_traffic(name):
     e = d.get(name)
     if not e:
         return None
-    src = os.path.join(ROOT, "progressive_kv_quantization_gb300", "csrc", e["source"])
-    if not os.path.exists(src):
-        return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return e["bytes_per_launch"] if sha == e["source_sha"] else None
+    return e["bytes_per_launch"] if e.get("source_sha") == source_sha(e.get("sources", [])) else None
+
+
+# the CUDA sources each timed call runs (kernel file first, then shared headers)
+KERNEL_SOURCES = {
+    "encode": ["encode.cu", "lynx_internal.cuh"],
+    "reconstruct_anchor": ["reconstruct.cu", "lynx_internal.cuh"],
+    "reconstruct_full": ["reconstruct.cu", "lynx_internal.cuh"],
+    "decode_anchor_b1": ["decode_quant.cu", "decode_common.cuh", "lynx_internal.cuh"],
+    "decode_anchor_b8": ["decode_quant.cu", "decode_common.cuh", "lynx_internal.cuh"],
+    "verify_full_t8": ["decode_tc.cu", "decode_common.cuh", "lynx_internal.cuh"],
+    "decode_bf16_b1": ["decode_attn.cu", "lynx_internal.cuh"],
+}
+
+
+def source_sha(names):
+    """sha256 (first 16 hex digits) over the named csrc files, in order; None if one is missing."""
+    h = hashlib.sha256()
+    for n in names:
+        path = os.path.join(ROOT, "progressive_kv_quantization_gb300", "csrc", n)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16] if names else None
 
 
 def run_gpu(args, rank, world):
@@ -302,8 +322,7 @@ def run_gpu(args, rank, world):
     head_total = sum(k[3] for k in ks)
     value = world * head_total / (ms_step * 1e6)
     dom = max(kern, key=lambda n: kern[n]["ms"])
-    src = {"encode": "encode.cu", "reconstruct_anchor": "reconstruct.cu",
-           "reconstruct_full": "reconstruct.cu"}.get(dom, "decode_attn.cu")
+    src = KERNEL_SOURCES[dom][0]
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["GBps_moved"], "peak": gbps_peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_of_hbm"],
             "traffic": profile_traffic(dom), "source": src}

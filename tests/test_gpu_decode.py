@@ -26,9 +26,10 @@ class Pools:
     """K and V page pools encoded by the oracle, plus their dequantised float64
     copies (anchor-only and full) and the BF16 originals."""
 
-    def __init__(self, n_heads, n_tokens, seed, alpha=100.0):
+    def __init__(self, n_heads, n_tokens, seed, alpha=100.0, lazy=False):
         out = inputs.outlier_pairs(n_heads, seed)
         self.alpha = alpha
+        self.lazy = lazy
         self.kb = inputs.kv_pages_np(n_heads, n_tokens, seed * 10 + 1, out)
         self.vb = inputs.kv_pages_np(n_heads, n_tokens, seed * 10 + 2, out)
         self.n = self.kb.shape[0]
@@ -37,6 +38,8 @@ class Pools:
         for name, bits in (("k", self.kb), ("v", self.vb)):
             a, r, m = lo.encode_pages(bits, alpha, EPS)
             self.enc[name] = (a, r, m)
+            if lazy:
+                continue
             self.deq[(name, "anchor")] = lo.reconstruct(a, None, m, alpha, EPS)
             self.deq[(name, "full")] = lo.reconstruct(a, r, m, alpha, EPS)
             self.deq[(name, "bf16")] = lo.bf16_to_f32(bits).astype(np.float64)
@@ -44,8 +47,16 @@ class Pools:
         self.dev_bf16 = {name: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
                          for name, b in (("k", self.kb), ("v", self.vb))}
 
+    def pages(self, name, mode, ids):
+        if not self.lazy:
+            return self.deq[(name, mode)][ids]
+        if mode == "bf16":
+            return lo.bf16_to_f32((self.kb if name == "k" else self.vb)[ids]).astype(np.float64)
+        a, r, m = self.enc[name]
+        return lo.reconstruct(a[ids], r[ids] if mode == "full" else None, m[ids], self.alpha, EPS)
+
     def fetch(self, mode):
-        return lambda ids: (self.deq[("k", mode)][ids], self.deq[("v", mode)][ids])
+        return lambda ids: (self.pages("k", mode, ids), self.pages("v", mode, ids))
 
 
 def run(pools, mode, q_bits, table, ctx, Hkv, causal, scale=None):
@@ -247,3 +258,27 @@ def test_qwen235b_layers_full_context_sampled(cuda_device):
                         mask=sel)
         del k, v, ka, kr, km, va, vr, vm
         torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_decode_sweep_full_context_sampled(cuda_device):
+    """Decode-attention sweep shape: 8 KV heads x 128, 32 query heads, a batch of
+    16 sequences whose contexts run from 4,096 to 131,072 tokens (ragged), over
+    one pool of oracle-encoded pages; anchor-only at T = 1 and 4, full codes at
+    T = 8 and 32 (causal verification), and the BF16 baseline at T = 8.
+    Sequences 0, 7 and 15 and query heads 0, 13 and 31 are checked against the
+    oracle over the whole context."""
+    Hkv, Hq, npph, B = 8, 32, 512, 16
+    pools = Pools(Hkv, npph * 256, 7, lazy=True)
+    ctx = np.array([4096 + b * 8192 + (37 * b) % 256 for b in range(B)])
+    ctx[-1] = npph * 256
+    table = np.stack([contiguous_table(1, Hkv, npph, npph, offset=37 * b)[0] for b in range(B)])
+    batches, heads = [0, 7, 15], [0, 13, 31]
+    for mode, T, causal in (("anchor", 1, False), ("anchor", 4, True), ("full", 8, True),
+                            ("full", 32, True), ("bf16", 8, True)):
+        q = inputs.queries_np((B, T, Hq, 128), 900 + T)
+        o, lse = run(pools, mode, q, table, ctx, Hkv, causal)
+        ro, rl = reference(pools, mode, q, table, ctx, Hkv, causal, batches=batches, q_heads=heads)
+        sel = np.zeros(o.shape[:3], dtype=bool)
+        sel[np.ix_(batches, range(T), heads)] = True
+        check_attention(o, lse, np.nan_to_num(ro), np.nan_to_num(rl, nan=0.0), mask=sel)
