@@ -26,7 +26,8 @@
 // channels cg + 8j (j = 0..15).  With the swizzle (16-byte unit u of row r at
 // u ^ (r & 7)) the lane's plane words sit at one per-lane offset plus j * 1024,
 // and the 32 lanes hit 32 different banks.  The 8 channel groups' partial
-// logits are summed through shared memory.  V phase, lane L: channels
+// logits are summed by a shuffle reduce-scatter (xor 16, 8, 4) that leaves
+// lane (tg, cg) with token 8tg + cg.  V phase, lane L: channels
 // L + 32k (k = 0..3), all 32 tokens of the chunk (one 16-byte unit per row).
 
 #include "decode_common.cuh"
@@ -34,11 +35,10 @@
 namespace lynx {
 namespace {
 
-// per consumer warp: coefficients [128][4 rows] f32, partial logits [8 groups][32] f32x4,
-// probabilities [16 pairs] f32x4 for rows 0-1 and 2-3
+// per consumer warp: coefficients [128][4 rows] f32, probabilities [16 pairs] f32x4
+// for rows 0-1 and 2-3
 constexpr int kWarpCoef = 0;
-constexpr int kWarpPart = kWarpCoef + kH * 4 * 4;
-constexpr int kWarpPs01 = kWarpPart + 8 * 32 * 16;
+constexpr int kWarpPs01 = kWarpCoef + kH * 4 * 4;
 constexpr int kWarpPs23 = kWarpPs01 + 16 * 16;
 constexpr int kWarpBytes = kWarpPs23 + 16 * 16;
 
@@ -180,7 +180,6 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
     // offsets from smem
     const uint32_t s_w = S::kWarps + w * kWarpBytes;
     const uint32_t s_coef = s_w + kWarpCoef;
-    const uint32_t s_part = s_w + kWarpPart;
     const uint32_t s_ps01 = s_w + kWarpPs01;
     const uint32_t s_ps23 = s_w + kWarpPs23;
     const uint32_t s_qs = S::kQs;
@@ -189,6 +188,9 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
     const uint32_t k_off = cg * 128 + ((w ^ cg) << 4) + 4 * tg;
     const uint8_t* lut_lane = smem + S::kLut + (FULL ? 4 * L : 8 * L);
     const float eps = a.eps;
+    float4 qd[4];   // scaled queries of channels L + 32k, rows 0-3
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qd[k] = lds<float4>(smem, s_qs + 16 * (L + 32 * k));
     bool failed = false;
 
     for (int i = 0; i < np && !failed; ++i) {
@@ -214,7 +216,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
           const float ds = __fadd_rn(lds<float>(smem, km + 4 * (kMetaSigmaOff + w * kH + d)), eps);
           const float A = __fmaf_rn(dg, mu, gmin);
           const float Bc = __fmul_rn(dg, ds);
-          const float4 q = lds<float4>(smem, s_qs + 16 * d);
+          const float4 q = qd[k];
           *reinterpret_cast<float4*>(smem + s_coef + 16 * d) =
               make_float4(q.x * Bc, q.y * Bc, q.z * Bc, q.w * Bc);
           ck[0] = __fmaf_rn(q.x, A, ck[0]);
@@ -228,6 +230,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
       __syncwarp();
 
       // ---- K phase: 16 channels x 8 tokens x 4 rows per lane
+      float s4[kRows];   // logits of token 8tg + cg of this chunk
       {
         float2 acc[kRows][4];
 #pragma unroll
@@ -250,43 +253,40 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
             for (int r = 0; r < kRows; ++r) acc[r][k] = __ffma2_rn(cc[r], lv, acc[r][k]);
           }
         }
-        // partial logits -> part[cg][32 tokens] (float4 over rows), xor-swizzled slots
-        const int f = (tg + 4 * (cg & 1)) & 7;
+        // Reduce the partial logits (row r, token 8tg + e8; e8 = 2k (+1 for .y)) over
+        // the 8 lanes of equal tg (lane bits 2..4) while scattering them: each xor
+        // exchange halves the token range a lane keeps, so that lane (tg, cg) ends
+        // with the four rows of token 8tg + cg.
+        const bool b2 = (cg & 4) != 0, b1 = (cg & 2) != 0, b0 = (cg & 1) != 0;
+        float w4[kRows][4];
 #pragma unroll
-        for (int e8 = 0; e8 < 8; ++e8) {
-          const int k = e8 >> 1;
-          const float4 v = (e8 & 1) ? make_float4(acc[0][k].y, acc[1][k].y, acc[2][k].y, acc[3][k].y)
-                                    : make_float4(acc[0][k].x, acc[1][k].x, acc[2][k].x, acc[3][k].x);
-          const int slot = cg * 32 + 8 * tg + (e8 ^ f);
-          *reinterpret_cast<float4*>(smem + s_part + 16 * slot) = v;
-        }
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = (e & 1) ? acc[r][e >> 1].y : acc[r][e >> 1].x;          // token e
+            const float hi = (e & 1) ? acc[r][2 + (e >> 1)].y : acc[r][2 + (e >> 1)].x;   // token 4 + e
+            w4[r][e] = (b2 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b2 ? lo : hi, 16);
+          }
+        float w2[kRows][2];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            w2[r][e] = (b1 ? w4[r][2 + e] : w4[r][e]) +
+                       __shfl_xor_sync(0xffffffffu, b1 ? w4[r][e] : w4[r][2 + e], 8);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+          s4[r] = (b0 ? w2[r][1] : w2[r][0]) + __shfl_xor_sync(0xffffffffu, b0 ? w2[r][0] : w2[r][1], 4) +
+                  ck[r];
       }
       __syncwarp();
       // every read of the K unit is done: hand the slot back
       if (L == 0) mbar_arrive(bar_empty + 8 * sK);
 
-      // ---- logits of token L (of this chunk) for the 4 rows
-      float s4[kRows];
-      {
-        const int tgo = L >> 3, e8 = L & 7;
-        float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int f = (tgo + 4 * (c & 1)) & 7;
-          const float4 v = lds<float4>(smem, s_part + 16 * (c * 32 + 8 * tgo + (e8 ^ f)));
-          acc4.x += v.x;
-          acc4.y += v.y;
-          acc4.z += v.z;
-          acc4.w += v.w;
-        }
-        s4[0] = acc4.x + ck[0];
-        s4[1] = acc4.y + ck[1];
-        s4[2] = acc4.z + ck[2];
-        s4[3] = acc4.w + ck[3];
-      }
       // ---- online softmax over this chunk's 32 tokens
       float corr[kRows], pb[kRows], pv[kRows];
-      const int pos = p * kP + 32 * w + L;
+      const int tok = 8 * tg + cg;
+      const int pos = p * kP + 32 * w + tok;
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
         const float sr = (pos < nvis[r]) ? s4[r] : -CUDART_INF_F;
@@ -300,7 +300,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
       {
         float* p01 = reinterpret_cast<float*>(smem + s_ps01);
         float* p23 = reinterpret_cast<float*>(smem + s_ps23);
-        const int m = L >> 1, e = L & 1;
+        const int m = tok >> 1, e = tok & 1;
         p01[4 * m + e] = pv[0];
         p01[4 * m + 2 + e] = pv[1];
         p23[4 * m + e] = pv[2];
