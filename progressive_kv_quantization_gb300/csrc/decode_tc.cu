@@ -17,22 +17,25 @@
 //            dequantised in float32 (A = gamma_min + (gamma_scale + eps) mu,
 //            B = (gamma_scale + eps)(sigma + eps), the chunk's affine
 //            constants) and split into its TF32 head and the float32
-//            remainder, two MMAs, so each product keeps ~21 bits.  Per 16
-//            tokens one n-tile holds the even and one the odd tokens, so one
-//            table lookup per packed byte feeds both.
+//            remainder, two MMAs, so each product keeps ~21 bits.  Four
+//            n-tiles per chunk: column n of n-tile k holds token 4n + k, so
+//            lane (g, t) needs bytes 2g and 2g+1 of a channel row, both in one
+//            32-bit plane word, and one table lookup per byte feeds two tiles.
 //   V side   U[128 channels x 16 rows] = l~ P^T as fp16 m16n8k16, two k-steps
 //            of 16 tokens, then folded into the output with the chunk's
 //            constants: O = O corr + A psum + B U.  l~ comes from a table of
 //            fp16 head/remainder pairs (two MMAs, ~22 bits); P is fp16, scaled
 //            by 2^10 away from fp16 subnormals (O and the row sums carry the
-//            2^10, removed once at the end).  Slot order of k-step q16: slots
-//            2t, 2t+1 hold tokens 16 q16 + 4t + {0, 1}, slots 2t+8, 2t+9 hold
-//            16 q16 + 4t + {2, 3}.  With that order the A fragments are packed
-//            bytes as stored (both tokens of a byte in one register) and the P
-//            fragments are S accumulator entries the lane holds already.
+//            2^10, removed once at the end).  Slot order of k-step kv: slots
+//            2t, 2t+1 hold tokens 8t + 4kv + {0, 1}, slots 2t+8, 2t+9 hold
+//            8t + 4kv + {2, 3}.  With that order the A fragments are packed
+//            bytes as stored (both tokens of a byte in one register; bytes
+//            4t..4t+3 of a channel row, one plane word, serve both k-steps)
+//            and the P fragments are S accumulator entries the lane holds
+//            already.
 //
-// Lane (g = L >> 2, t = L & 3) holds S of rows g and g+8 for tokens
-// 16 q16 + 4t + j (j = 0..3) of its chunk.
+// Lane (g = L >> 2, t = L & 3) holds S of rows g and g+8 for tokens 8t + j
+// (j = 4hh + k: entry hh of n-tile k) of its chunk.
 //
 // Rounding: P is rounded to fp16 (relative 2^-11); everything else keeps at
 // least ~21 bits, sums are float32.
@@ -225,12 +228,12 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     const int w = warp;
     const uint32_t s_ab = S::kWarps + w * kTcWarpBytes;
     const uint32_t lane8 = 8u * L, lane4 = 4u * L, lane4v = 128u + 4u * L;
-    // K side: byte 8 q16 + g of a channel row = byte g & 3 of word 2 q16 + (g >> 2)
-    const uint32_t ksel = byte_sel(g & 3);
-    const uint32_t kword = 4 * (g >> 2);
-    // V side: bytes 8 q16 + 2t (+1) of channel 16 mt + g = bytes 2 (t & 1) (+1) of word 2 q16 + (t >> 1)
-    const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * (t >> 1);
-    const uint32_t vsel0 = byte_sel(2 * (t & 1)), vsel1 = byte_sel(2 * (t & 1) + 1);
+    // K side: bytes 2g (n-tiles 0, 1) and 2g+1 (n-tiles 2, 3) of a channel row,
+    // bytes 2 (g & 1) and 2 (g & 1) + 1 of its word g >> 1
+    const uint32_t ksel0 = byte_sel(2 * (g & 1)), ksel1 = byte_sel(2 * (g & 1) + 1);
+    const uint32_t kword = 4 * (g >> 1);
+    // V side: bytes 4t..4t+3 of channel 16 mt + g, word t of its chunk unit
+    const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * t;
     const float eps = a.eps;
     const float sc = a.scale_log2;
     bool failed = false;
@@ -261,12 +264,12 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       prep_ab(unitK);
       __syncwarp();
 
-      // ---- S = Q K^T: n-tile A of token group q16 = even tokens, n-tile B = odd tokens
-      float sA[2][4], sB[2][4];
+      // ---- S = Q K^T over 16 k-steps of channels (t, t + 4) + 8 ks; n-tile k, column n: token 4n + k
+      float sacc[4][4];
 #pragma unroll
-      for (int q16 = 0; q16 < 2; ++q16)
+      for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sA[q16][e] = sB[q16][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) sacc[n][e] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
         const uint4 qf = lds<uint4>(smem, S::kQ + (ks * 32 + L) * 16);
@@ -275,54 +278,58 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         const float2 ab1 = lds<float2>(smem, s_ab + 8 * c1);
         const uint32_t r0 = unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword;
         const uint32_t r1 = unitK + c1 * 128 + ((w ^ (c1 & 7)) << 4) + kword;
+        const uint32_t wa0 = lds<uint32_t>(smem, r0), wa1 = lds<uint32_t>(smem, r1);
+        // l~ pairs (even, odd token) of bytes 2g (jb 0) and 2g+1 (jb 1) of channels c0, c1
+        float2 l00, l01, l10, l11;
+        if (!FULL) {
+          l00 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel0));
+          l01 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel1));
+          l10 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel0));
+          l11 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel1));
+        } else {
+          uint32_t e0, o0, e1, o1;
+          full_codes(wa0, lds<uint32_t>(smem, r0 + G::kResOff), e0, o0);
+          full_codes(wa1, lds<uint32_t>(smem, r1 + G::kResOff), e1, o1);
+          auto val = [&](uint32_t codes, uint32_t sel) {
+            return lds<float>(smem, S::kLutK + lut_off(codes, lane4, sel));
+          };
+          l00 = make_float2(val(e0, ksel0), val(o0, ksel0));
+          l01 = make_float2(val(e0, ksel1), val(o0, ksel1));
+          l10 = make_float2(val(e1, ksel0), val(o1, ksel0));
+          l11 = make_float2(val(e1, ksel1), val(o1, ksel1));
+        }
+        const float2 A0 = make_float2(ab0.x, ab0.x), B0 = make_float2(ab0.y, ab0.y);
+        const float2 A1 = make_float2(ab1.x, ab1.x), B1 = make_float2(ab1.y, ab1.y);
+        const float2 k00 = __ffma2_rn(l00, B0, A0), k01 = __ffma2_rn(l01, B0, A0);
+        const float2 k10 = __ffma2_rn(l10, B1, A1), k11 = __ffma2_rn(l11, B1, A1);
+        // n-tile k = 2 jb + eo: b0 = channel c0, b1 = channel c1
+        const float x0[4] = {k00.x, k00.y, k01.x, k01.y};
+        const float x1[4] = {k10.x, k10.y, k11.x, k11.y};
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16) {
-          const uint32_t wa0 = lds<uint32_t>(smem, r0 + 8 * q16);
-          const uint32_t wa1 = lds<uint32_t>(smem, r1 + 8 * q16);
-          float2 l0, l1;
-          if (!FULL) {
-            l0 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel));
-            l1 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel));
-          } else {
-            uint32_t e0, o0, e1, o1;
-            full_codes(wa0, lds<uint32_t>(smem, r0 + 8 * q16 + G::kResOff), e0, o0);
-            full_codes(wa1, lds<uint32_t>(smem, r1 + 8 * q16 + G::kResOff), e1, o1);
-            l0 = make_float2(lds<float>(smem, S::kLutK + lut_off(e0, lane4, ksel)),
-                             lds<float>(smem, S::kLutK + lut_off(o0, lane4, ksel)));
-            l1 = make_float2(lds<float>(smem, S::kLutK + lut_off(e1, lane4, ksel)),
-                             lds<float>(smem, S::kLutK + lut_off(o1, lane4, ksel)));
-          }
-          const float2 k0 = __ffma2_rn(l0, make_float2(ab0.y, ab0.y), make_float2(ab0.x, ab0.x));
-          const float2 k1 = __ffma2_rn(l1, make_float2(ab1.y, ab1.y), make_float2(ab1.x, ab1.x));
-          mma_tf32(sA[q16], qf.x, qf.y, qf.z, qf.w, tf32_hi(k0.x), tf32_hi(k1.x));
-          mma_tf32(sA[q16], qf.x, qf.y, qf.z, qf.w, tf32_lo(k0.x), tf32_lo(k1.x));
-          mma_tf32(sB[q16], qf.x, qf.y, qf.z, qf.w, tf32_hi(k0.y), tf32_hi(k1.y));
-          mma_tf32(sB[q16], qf.x, qf.y, qf.z, qf.w, tf32_lo(k0.y), tf32_lo(k1.y));
+        for (int n = 0; n < 4; ++n) {
+          mma_tf32(sacc[n], qf.x, qf.y, qf.z, qf.w, tf32_hi(x0[n]), tf32_hi(x1[n]));
+          mma_tf32(sacc[n], qf.x, qf.y, qf.z, qf.w, tf32_lo(x0[n]), tf32_lo(x1[n]));
         }
       }
       __syncwarp();
       if (L == 0) mbar_arrive(bar_empty + 8 * sK);
 
       // ---- online softmax: row g (rh 0, S entries 0-1) and g + 8 (rh 1, entries 2-3);
-      // token 16 q16 + 4t + j is sA[q16][2rh] (j 0), sB (j 1), sA[q16][2rh+1] (j 2), sB (j 3)
-      const int pos0 = p * kP + 32 * w + 4 * t;
+      // token 8t + j, j = 4 hh + k, is entry 2 rh + hh of n-tile k
+      const int pos0 = p * kP + 32 * w + 8 * t;
       const bool all_visible = (p + 1) * kP <= min_vis;
-      float pr[2][2][4];   // [q16][rh][j], probabilities x 2^10
+      float pr[2][8];   // [rh][j], probabilities x 2^10
       float corr[2], psum[2];
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
         const int nv = rh ? nv_hi : nv_lo;
         float mloc = -CUDART_INF_F;
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16) {
-          const float v4[4] = {sA[q16][2 * rh], sB[q16][2 * rh], sA[q16][2 * rh + 1], sB[q16][2 * rh + 1]};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float sv = v4[j] * sc;
-            if (!all_visible && pos0 + 16 * q16 + j >= nv) sv = -CUDART_INF_F;
-            pr[q16][rh][j] = sv;
-            mloc = fmaxf(mloc, sv);
-          }
+        for (int j = 0; j < 8; ++j) {
+          float sv = sacc[j & 3][2 * rh + (j >> 2)] * sc;
+          if (!all_visible && pos0 + j >= nv) sv = -CUDART_INF_F;
+          pr[rh][j] = sv;
+          mloc = fmaxf(mloc, sv);
         }
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
@@ -330,28 +337,26 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         corr[rh] = (mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[rh] - mnew);
         float ps = 0.0f;
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float sv = pr[q16][rh][j];
-            const float pv = (sv == -CUDART_INF_F) ? 0.0f : exp2f(sv - mnew) * 1024.0f;
-            pr[q16][rh][j] = pv;
-            ps += pv;
-          }
+        for (int j = 0; j < 8; ++j) {
+          const float sv = pr[rh][j];
+          const float pv = (sv == -CUDART_INF_F) ? 0.0f : exp2f(sv - mnew) * 1024.0f;
+          pr[rh][j] = pv;
+          ps += pv;
+        }
         l_run[rh] = l_run[rh] * corr[rh] + ps;
         ps += __shfl_xor_sync(0xffffffffu, ps, 1);
         ps += __shfl_xor_sync(0xffffffffu, ps, 2);
         psum[rh] = ps;
         m_run[rh] = mnew;
       }
-      // P^T fragments of k-step q16, n-tile nt (rows 8 nt + g): tokens 16 q16 + 4t + {0,1} and + {2,3}
+      // P^T fragments of k-step kv, n-tile nt (rows 8 nt + g): tokens 8t + 4kv + {0,1} and + {2,3}
       uint32_t pb[2][2][2];
 #pragma unroll
-      for (int q16 = 0; q16 < 2; ++q16)
+      for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          pb[q16][nt][0] = h2(pr[q16][nt][0], pr[q16][nt][1]);
-          pb[q16][nt][1] = h2(pr[q16][nt][2], pr[q16][nt][3]);
+          pb[kv][nt][0] = h2(pr[nt][4 * kv], pr[nt][4 * kv + 1]);
+          pb[kv][nt][1] = h2(pr[nt][4 * kv + 2], pr[nt][4 * kv + 3]);
         }
       // statistics of U's columns: rows 8 nt + 2t + e live in lane 8t + 4e
       float2 cr[2], pss[2];
@@ -375,40 +380,34 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
         const float2 ab1 = lds<float2>(smem, s_ab + 8 * (c0 + 8));
         const uint32_t off = unitV + mt * 2048 + vofs;
+        const uint32_t wa0 = lds<uint32_t>(smem, off);
+        const uint32_t wa1 = lds<uint32_t>(smem, off + 1024);
+        uint32_t e0 = 0, o0 = 0, e1 = 0, o1 = 0;
+        if (FULL) {
+          full_codes(wa0, lds<uint32_t>(smem, off + G::kResOff), e0, o0);
+          full_codes(wa1, lds<uint32_t>(smem, off + 1024 + G::kResOff), e1, o1);
+        }
+        // (head pair, remainder pair) of byte j of row c0 (c = 0) or c0 + 8 (c = 1)
+        auto vpair = [&](int c, uint32_t j) -> uint2 {
+          const uint32_t sel = byte_sel(j);
+          if (!FULL) return lds<uint2>(smem, S::kLutV + lut_off(c ? wa1 : wa0, lane8, sel));
+          const uint32_t he = lds<uint32_t>(smem, S::kLutV + lut_off(c ? e1 : e0, lane4v, sel));
+          const uint32_t ho = lds<uint32_t>(smem, S::kLutV + lut_off(c ? o1 : o0, lane4v, sel));
+          return make_uint2(prmt(he, ho, 0x5410u), prmt(he, ho, 0x7632u));
+        };
         float u[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[nt][e] = 0.0f;
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16) {
-          const uint32_t wa0 = lds<uint32_t>(smem, off + 8 * q16);
-          const uint32_t wa1 = lds<uint32_t>(smem, off + 1024 + 8 * q16);
-          // (head pair, remainder pair) of bytes j0 = 2 (t & 1) and j1 = j0 + 1 of rows c0, c0 + 8
-          uint2 x00, x10, x01, x11;
-          if (!FULL) {
-            x00 = lds<uint2>(smem, S::kLutV + lut_off(wa0, lane8, vsel0));
-            x10 = lds<uint2>(smem, S::kLutV + lut_off(wa1, lane8, vsel0));
-            x01 = lds<uint2>(smem, S::kLutV + lut_off(wa0, lane8, vsel1));
-            x11 = lds<uint2>(smem, S::kLutV + lut_off(wa1, lane8, vsel1));
-          } else {
-            uint32_t e0, o0, e1, o1;
-            full_codes(wa0, lds<uint32_t>(smem, off + 8 * q16 + G::kResOff), e0, o0);
-            full_codes(wa1, lds<uint32_t>(smem, off + 1024 + 8 * q16 + G::kResOff), e1, o1);
-            auto pair = [&](uint32_t ev, uint32_t od, uint32_t sel) {
-              const uint32_t he = lds<uint32_t>(smem, S::kLutV + lut_off(ev, lane4v, sel));
-              const uint32_t ho = lds<uint32_t>(smem, S::kLutV + lut_off(od, lane4v, sel));
-              return make_uint2(prmt(he, ho, 0x5410u), prmt(he, ho, 0x7632u));
-            };
-            x00 = pair(e0, o0, vsel0);
-            x10 = pair(e1, o1, vsel0);
-            x01 = pair(e0, o0, vsel1);
-            x11 = pair(e1, o1, vsel1);
-          }
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint2 x00 = vpair(0, 2 * kv), x10 = vpair(1, 2 * kv);
+          const uint2 x01 = vpair(0, 2 * kv + 1), x11 = vpair(1, 2 * kv + 1);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            mma_f16(u[nt], x00.x, x10.x, x01.x, x11.x, pb[q16][nt][0], pb[q16][nt][1]);
-            mma_f16(u[nt], x00.y, x10.y, x01.y, x11.y, pb[q16][nt][0], pb[q16][nt][1]);
+            mma_f16(u[nt], x00.x, x10.x, x01.x, x11.x, pb[kv][nt][0], pb[kv][nt][1]);
+            mma_f16(u[nt], x00.y, x10.y, x01.y, x11.y, pb[kv][nt][0], pb[kv][nt][1]);
           }
         }
 #pragma unroll
