@@ -26,9 +26,11 @@
 // table (the smallest float32 of each code).
 //
 // Packing.  The lane's 32 codes sit in the low bytes of the rounded floats;
-// byte permutes gather four of them per word, and the anchor nibble
-// ((S>0 ? I : ~I) >> 4) and residual nibble ((7 - I) mod 16) are formed four
-// at a time before the nibbles of eight tokens are merged into one word.
+// byte permutes gather the even and the odd tokens of each group of eight into
+// two words (and the sign bytes likewise, straight from the float sign bits),
+// and two masked logic steps form the anchor nibbles ((S>0 ? I : ~I) >> 4) and
+// the residual nibbles ((7 - I) mod 16 = (I ^ 7) & 15) of all eight tokens,
+// even tokens in the low and odd tokens in the high nibbles.
 
 #include "lynx_internal.cuh"
 
@@ -61,22 +63,18 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t lt_zero_mask(float x) {   // 0xFFFFFFFF if x < 0 (-0 is not)
-  uint32_t m;
-  asm("set.lt.u32.f32 %0, %1, 0f00000000;" : "=r"(m) : "f"(x));
-  return m;
-}
-
 // bytes 0 of w0..w3 -> one word
 __device__ __forceinline__ uint32_t gather4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
   return prmt(prmt(w0, w1, 0x0040u), prmt(w2, w3, 0x0040u), 0x5410u);
 }
 
-// low nibbles of the 4 bytes of lo (tokens 0-3) and hi (tokens 4-7) -> 8 nibbles, token k at bits 4k
-__device__ __forceinline__ uint32_t merge_nibbles(uint32_t lo, uint32_t hi) {
-  const uint32_t a = lo | (lo >> 4);
-  const uint32_t b = hi | (hi >> 4);
-  return prmt(a, b, 0x6420u);
+// sign bytes (0xFF where the float is negative, else 0) of x0..x3 -> one word.
+// The selector nibbles 0xB / 0xF replicate the sign bit of byte 3 of each
+// operand.  A centred value x_n - mu is never -0 (round-to-nearest gives +0
+// for equal operands), so the sign bit is the test x < 0.
+__device__ __forceinline__ uint32_t signs4(float x0, float x1, float x2, float x3) {
+  return prmt(prmt(__float_as_uint(x0), __float_as_uint(x1), 0x00FBu),
+              prmt(__float_as_uint(x2), __float_as_uint(x3), 0x00FBu), 0x5410u);
 }
 
 struct QuantConsts {
@@ -85,23 +83,24 @@ struct QuantConsts {
 };
 
 // Stage 3 for eight magnitudes a (pairs): the rounded code of each lands in the
-// low byte of ib[e] (the bits of code + 1.5 * 2^23).  The estimate
-// y = c * log2(1 + alpha a) is off by less than 0.5 - edge; when any of the
+// low byte of ib[e] (the bits of code + 1.5 * 2^23, the fused c lg + 1.5 * 2^23
+// rounding c lg to an integer).  The estimate y = c * log2(1 + alpha a) is off
+// by less than 0.5 - edge; when any of the
 // eight lies within that margin of a rounding edge, all eight are decided
 // exactly: with I0 = round(y) and j = I0 + (y > I0), the code is
 // j - 1 + (a >= thr[j]), thr[k] being the smallest float32 with code k.
 __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8],
                                           const float* __restrict__ s_thr, const QuantConsts& qc) {
-  const float2 one2 = f2(1.0f), mone2 = f2(-1.0f), magic2 = f2(kMagic), nmagic2 = f2(-kMagic);
+  const float2 one2 = f2(1.0f), mone2 = f2(-1.0f), magic2 = f2(kMagic);
   float2 d[4];
   float dmax = 0.0f;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const float2 tt = __ffma2_rn(qc.alpha2, a[u], one2);
-    const float2 y = __fmul2_rn(qc.c2, make_float2(__log2f(tt.x), __log2f(tt.y)));
-    const float2 r = __fadd2_rn(y, magic2);                     // round to nearest (even)
-    const float2 ry = __fadd2_rn(r, nmagic2);                   // round(y), exact
-    d[u] = __ffma2_rn(ry, mone2, y);                            // y - round(y), exact
+    const float2 lg = make_float2(__log2f(tt.x), __log2f(tt.y));
+    const float2 r = __ffma2_rn(qc.c2, lg, magic2);             // c lg rounded to an integer, + 1.5 2^23
+    const float2 nry = __ffma2_rn(r, mone2, magic2);             // -round(c lg), exact
+    d[u] = __ffma2_rn(qc.c2, lg, nry);                           // c lg - round(c lg)
     ib[2 * u] = __float_as_uint(r.x);
     ib[2 * u + 1] = __float_as_uint(r.y);
     dmax = fmaxf(dmax, fmaxf(fabsf(d[u].x), fabsf(d[u].y)));
@@ -202,27 +201,25 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     uint32_t pa[4], pr[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint32_t ib[8], sm[8];
+      uint32_t ib[8];
+      float xs[8];   // centred values (for their signs)
       float2 a[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = 4 * q + u;
         const float2 xc = __fadd2_rn(xn[t], nmu2);
-        sm[2 * u] = lt_zero_mask(xc.x);
-        sm[2 * u + 1] = lt_zero_mask(xc.y);
+        xs[2 * u] = xc.x;
+        xs[2 * u + 1] = xc.y;
         a[u] = div2(make_float2(fabsf(xc.x), fabsf(xc.y)), nds2, rs2);   // |x_f|
       }
       quantise8(a, ib, s_thr, qc);
-      uint32_t an[2], rn[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t I4 = gather4(ib[4 * hh], ib[4 * hh + 1], ib[4 * hh + 2], ib[4 * hh + 3]);
-        const uint32_t S4 = gather4(sm[4 * hh], sm[4 * hh + 1], sm[4 * hh + 2], sm[4 * hh + 3]);
-        an[hh] = ((I4 >> 4) ^ S4) & 0x0F0F0F0Fu;                        // (S>0 ? I : ~I) >> 4
-        rn[hh] = (((~I4) & 0x0F0F0F0Fu) + 0x08080808u) & 0x0F0F0F0Fu;  // (7 - I) mod 16
-      }
-      pa[q] = merge_nibbles(an[0], an[1]);
-      pr[q] = merge_nibbles(rn[0], rn[1]);
+      // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
+      const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
+      const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
+      // byte m of a packed word: token 2m in the low nibble, token 2m + 1 in the high nibble.
+      // anchor nibble (S>0 ? I : ~I) >> 4 = ((I >> 4) ^ S) & 15; residual (7 - I) mod 16 = (I ^ 7) & 15
+      pa[q] = (((Ie >> 4) ^ Se) & 0x0F0F0F0Fu) | ((Io ^ So) & 0xF0F0F0F0u);
+      pr[q] = ((Ie ^ 0x07070707u) & 0x0F0F0F0Fu) | (((Io << 4) ^ 0x70707070u) & 0xF0F0F0F0u);
     }
     anchor[g * 32 + lane] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
     residual[g * 32 + lane] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
