@@ -122,7 +122,7 @@ __device__ __forceinline__ void load_chunk(const uint4* __restrict__ src, uint4 
   for (int k = 0; k < 4; ++k) raw[k] = __ldg(src + k);
 }
 
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, 2)
 encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__ anchor,
               uint4* __restrict__ residual, float* __restrict__ meta, const EncodeTables tab) {
   __shared__ float s_thr[129];
