@@ -16,7 +16,9 @@
 // Each division x / d by a per-row or per-chunk divisor d uses r = RN(1/d),
 // then q = RN(x r) corrected by one FMA residual step, q' = RN(q + r (x - q d))
 // (Markstein's FMA division correction), which returns the correctly rounded
-// quotient.  sigma = max_t |x_n,t - mu| is taken as
+// quotient.  The Stage 2 quotient |x_c| / (sigma + eps) feeds only the code
+// decision: its estimate uses q = RN(x r) (within 1.5 ulp), and the corrected
+// quotient is formed where the code is decided from the threshold table.  sigma = max_t |x_n,t - mu| is taken as
 // max(RN(x_n(max x) - mu), RN(mu - x_n(min x))): every step from x to
 // x_n - mu is a monotone rounding, so the extreme deviations sit at the
 // chunk's extreme inputs and the value is the same.  The Stage 3 code
@@ -89,8 +91,13 @@ struct QuantConsts {
 // eight lies within that margin of a rounding edge, all eight are decided
 // exactly: with I0 = round(y) and j = I0 + (y > I0), the code is
 // j - 1 + (a >= thr[j]), thr[k] being the smallest float32 with code k.
+// exact_a(e) returns the correctly rounded magnitude of element e; the rule
+// compares it with the thresholds, while the estimate may start from a value
+// within a relative 2^-22 of it (the margin covers that).
+template <typename ExactA>
 __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8],
-                                          const float* __restrict__ s_thr, const QuantConsts& qc) {
+                                          const float* __restrict__ s_thr, const QuantConsts& qc,
+                                          ExactA exact_a) {
   const float2 one2 = f2(1.0f), mone2 = f2(-1.0f), magic2 = f2(kMagic);
   float2 d[4];
   float dmax = 0.0f;
@@ -109,7 +116,7 @@ __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float de = (e & 1) ? d[e >> 1].y : d[e >> 1].x;
-      const float ae = (e & 1) ? a[e >> 1].y : a[e >> 1].x;
+      const float ae = exact_a(e);
       const int I0 = min(max((int)(ib[e] - kMagicBits), 0), 127);
       const int j = I0 + (de > 0.0f ? 1 : 0);
       ib[e] = kMagicBits + (uint32_t)(j - 1 + (ae >= s_thr[j] ? 1 : 0));
@@ -194,7 +201,7 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     const float sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
     const float ds = __fadd_rn(sigma, eps);
     const float rs = __frcp_rn(ds);
-    const float2 nmu2 = f2(-mu), nds2 = f2(-ds), rs2 = f2(rs);
+    const float2 nmu2 = f2(-mu), rs2 = f2(rs);
 
     // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
     // rounded floats, sign masks, then split and pack
@@ -210,9 +217,10 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
         const float2 xc = __fadd2_rn(xn[t], nmu2);
         xs[2 * u] = xc.x;
         xs[2 * u + 1] = xc.y;
-        a[u] = div2(make_float2(fabsf(xc.x), fabsf(xc.y)), nds2, rs2);   // |x_f|
+        a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
       }
-      quantise8(a, ib, s_thr, qc);
+      // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
+      quantise8(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
       // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
       const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
       const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
@@ -258,7 +266,7 @@ quantize_kernel(const float* __restrict__ a, int64_t n, uint8_t* __restrict__ co
 #pragma unroll
     for (int u = 0; u < 4; ++u) av[u] = make_float2(v[2 * u], v[2 * u + 1]);
     uint32_t ib[8];
-    quantise8(av, ib, s_thr, qc);
+    quantise8(av, ib, s_thr, qc, [&](int e) { return v[e]; });
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int64_t i = g * 8 + e;

@@ -82,9 +82,12 @@ const EncodeTables* encode_tables(float alpha, float eps) {
   // absolute error on [1, 2^20) stays below 2^-21 * max(1, log2(t)) (measured
   // over every float32 t in that range: at most 2^-22.5 below 4, 2^-20.9 below
   // 256, 2^-19 below 2^20); the rounding of 1 + alpha a, of c and of the
-  // product add at most c * 1e-7 + 1.6e-5.  The margin is twice the sum.
+  // product add at most c * 1e-7 + 1.6e-5; a magnitude estimate within a
+  // relative 2^-22 of the exact one (the encoder's a = RN(x RN(1/d))) moves
+  // the estimate by at most c 2^-22 / ln 2 < c * 3.5e-7.  The margin is twice
+  // the sum.
   const double L = log2(1.0 + a);
-  const double err = c * (ldexp(1.0, -21) * (L > 1.0 ? L : 1.0) + 1e-7) + 1.6e-5;
+  const double err = c * (ldexp(1.0, -21) * (L > 1.0 ? L : 1.0) + 1e-7 + 3.5e-7) + 1.6e-5;
   tab.edge = (float)(0.5 - 2.0 * err);
   cached_alpha = alpha;
   cached_eps = eps;
