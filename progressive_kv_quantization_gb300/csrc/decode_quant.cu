@@ -64,19 +64,20 @@ static_assert(QLayout<true>::kAlloc <= 232448, "shared memory (full)");
 
 // value pair (l~ of token 2m, l~ of token 2m+1) for one anchor byte, or for
 // one anchor byte and the matching residual byte
+// lut points at the table; lane_off is the lane's copy offset (8L anchor, 4L full)
 template <bool FULL>
-__device__ __forceinline__ float2 lut_pair(const uint8_t* lut_lane, uint32_t a_word, uint32_t r_word,
-                                           int k) {
+__device__ __forceinline__ float2 lut_pair(const uint8_t* lut, uint32_t lane_off, uint32_t a_word,
+                                           uint32_t r_word, int k) {
   if (!FULL) {
-    // entry stride 256 B: offset = byte k of a_word placed in bits 8..15
-    const uint32_t off = prmt(a_word, 0u, 0x4404u | ((uint32_t)k << 4));
-    return lds<float2>(lut_lane, off);
+    // entry stride 256 B: byte k of a_word in bits 8..15, the lane's offset (< 256) in bits 0..7
+    const uint32_t off = prmt(a_word, lane_off, 0x5504u | ((uint32_t)k << 4));
+    return lds<float2>(lut, off);
   } else {
     const uint32_t ab = (a_word >> (8 * k)) & 0xFFu;
     const uint32_t rb = (r_word >> (8 * k)) & 0xFFu;
     const uint32_t c0 = (ab & 0xFu) | ((rb & 0xFu) << 4);
     const uint32_t c1 = (ab >> 4) | (rb & 0xF0u);
-    return make_float2(lds<float>(lut_lane, c0 << 7), lds<float>(lut_lane, c1 << 7));
+    return make_float2(lds<float>(lut, lane_off + (c0 << 7)), lds<float>(lut, lane_off + (c1 << 7)));
   }
 }
 
@@ -186,7 +187,8 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
     const int tg = L & 3, cg = L >> 2;
     // K phase: plane word of (row cg + 8j, unit w ^ cg, word tg) = k_off + j * 1024
     const uint32_t k_off = cg * 128 + ((w ^ cg) << 4) + 4 * tg;
-    const uint8_t* lut_lane = smem + S::kLut + (FULL ? 4 * L : 8 * L);
+    const uint8_t* lut = smem + S::kLut;
+    const uint32_t lane_off = FULL ? 4u * L : 8u * L;
     const float eps = a.eps;
     float4 qd[4];   // scaled queries of channels L + 32k, rows 0-3
 #pragma unroll
@@ -248,7 +250,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
                                 make_float2(c.z, c.z), make_float2(c.w, c.w)};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 lv = lut_pair<FULL>(lut_lane, wa, wr, k);
+            const float2 lv = lut_pair<FULL>(lut, lane_off, wa, wr, k);
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[r][k] = __ffma2_rn(cc[r], lv, acc[r][k]);
           }
@@ -346,7 +348,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
           for (int k = 0; k < 4; ++k) {
             const uint32_t wa = (m < 4) ? va[k].x : (m < 8) ? va[k].y : (m < 12) ? va[k].z : va[k].w;
             const uint32_t wr = (m < 4) ? vr[k].x : (m < 8) ? vr[k].y : (m < 12) ? vr[k].z : vr[k].w;
-            const float2 lv = lut_pair<FULL>(lut_lane, wa, wr, m & 3);
+            const float2 lv = lut_pair<FULL>(lut, lane_off, wa, wr, m & 3);
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[k][r] = __ffma2_rn(pp[r], lv, acc[k][r]);
           }
