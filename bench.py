@@ -216,6 +216,22 @@ def kernel_list(torch, L, b):
     return ks
 
 
+def reduce_max(value, world, dist, device=None):
+    """Largest value over the ranks (a job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(head_bytes_per_rank, world, ms_step):
+    """Whole-job GB/s: the bytes all ranks processed in one step over the
+    (slowest rank's) step time; every rank runs the same workload (weak scaling)."""
+    return world * head_bytes_per_rank / (ms_step * 1e6)
+
+
 def profile_traffic(name):
     """DRAM traffic per launch from the committed ncu summary, if the kernel's
     source is unchanged since it was captured; else None."""
@@ -306,11 +322,7 @@ def run_gpu(args, rank, world):
     barrier()
     clk = clocks.stop()
     L.lynx_device_status()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = reduce_max(t0.elapsed_time(t1), world, dist if world > 1 else None, dev)
     ms_step = ms_total / args.steps
     gbps_peak, peak_kind = peaks()
     kern = {}
@@ -321,7 +333,7 @@ def run_gpu(args, rank, world):
                       "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3), "launches": launches,
                       "headline_bytes": head, "moved_bytes": moved}
     head_total = sum(k[3] for k in ks)
-    value = world * head_total / (ms_step * 1e6)
+    value = job_value(head_total, world, ms_step)
     dom = max(kern, key=lambda n: kern[n]["ms"])
     src = KERNEL_SOURCES[dom][0]
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["GBps_moved"], "peak": gbps_peak,
