@@ -19,6 +19,9 @@
  *                         verification pass of §4.3).
  *   lynx_decode_attn_bf16 the same attention over plain BF16 pages (the
  *                         uncompressed baseline the paper compares against).
+ *   lynx_attn_merge       combines attention over two disjoint key sets by
+ *                         their log-sum-exps (the drafts' own uncompressed KV
+ *                         joined to the verification over the packed cache).
  *
  * ---------------------------------------------------------------------------
  * Data layout (all sizes for H = 128 channels, P = 256 tokens, C = 32):
@@ -200,6 +203,24 @@ int lynx_decode_attn_noalloc(const void* q_bf16, int B, int T, int Hq, int Hkv, 
                              int64_t n_pool_pages, const int32_t* page_table, int max_pages,
                              const int32_t* ctx_len, const lynx_params_t* params, float sm_scale,
                              int causal, float* out, float* lse, void* stream);
+
+/* Merge of two attention results over disjoint key sets.  The verification
+ * pass (paper §4.3) also attends to the draft tokens' own K and V, which the
+ * caller holds uncompressed (e.g. as a BF16 page read by
+ * lynx_decode_attn_bf16); attention over a union of key sets is the
+ * log-sum-exp weighted combination of the attention over its parts:
+ *   m   = max(lse_a, lse_b),  w_a = e^(lse_a - m),  w_b = e^(lse_b - m)
+ *   o   = (w_a o_a + w_b o_b) / (w_a + w_b),   lse = m + ln(w_a + w_b)
+ * per row, with natural-log LSEs as lynx_decode_attn returns them.  A row whose
+ * lse is -inf in one input takes the other input's row; -inf in both gives
+ * o = 0, lse = -inf.
+ *   o_a, o_b, o    [rows][head_dim] float32;  lse_a, lse_b, lse  [rows] float32.
+ *   o may be o_a or o_b and lse may be lse_a or lse_b (in place); other
+ *   overlaps are not allowed.
+ * rows == 0 is a no-op.  Errors: INVALID_ARG (null pointer, rows < 0),
+ * UNSUPPORTED (head_dim != 128), ALIGNMENT, CUDA. */
+int lynx_attn_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                    int64_t rows, int head_dim, float* o, float* lse, void* stream);
 
 /* Workspace bytes needed by lynx_decode_attn / lynx_decode_attn_bf16 for the
  * given shape on the current device (0 for invalid shapes). */

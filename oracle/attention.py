@@ -93,3 +93,14 @@ def decode_attention(q: np.ndarray, kv_pages, page_table: np.ndarray, ctx_len: n
             o[b][:, heads, :] = oo.reshape(T, len(heads), D)
             lse[b][:, heads] = ll.reshape(T, len(heads))
     return o, lse
+
+
+def vnmse(o: np.ndarray, o_ref: np.ndarray) -> float:
+    """Compression error of attention outputs as the Lynx paper measures it
+    (§6.3 "Compression error", the vNMSE it reports in Table 3): the mean over
+    output rows (every query token and head) of ||o - o_ref||^2 / ||o_ref||^2,
+    with o the output over compressed KV and o_ref the output over the
+    uncompressed KV.  Rows are the last axis; float64."""
+    o = np.asarray(o, dtype=np.float64).reshape(-1, np.shape(o)[-1])
+    r = np.asarray(o_ref, dtype=np.float64).reshape(-1, np.shape(o_ref)[-1])
+    return float(np.mean(np.sum((o - r) ** 2, axis=1) / np.sum(r ** 2, axis=1)))

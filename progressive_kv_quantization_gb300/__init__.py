@@ -9,6 +9,7 @@ library; the first call does, and raises ``LynxError`` if it is missing.
 from .lynx import (  # noqa: F401
     LynxError,
     Params,
+    lynx_attn_merge,
     lynx_decode_attn,
     lynx_decode_attn_bf16,
     lynx_decode_attn_workspace_size,

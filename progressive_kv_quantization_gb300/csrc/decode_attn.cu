@@ -667,6 +667,35 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   if (d == 0 && a.lse) a.lse[o_idx] = (mstar + log2f(l)) * 0.6931471805599453f;
 }
 
+// Log-sum-exp merge of two attention results over disjoint key sets: one warp
+// per row, lane L holds channels 4L..4L+3.
+__global__ void __launch_bounds__(256)
+attn_merge_kernel(const float* __restrict__ oa, const float* __restrict__ la,
+                  const float* __restrict__ ob, const float* __restrict__ lb, int64_t rows,
+                  float* o, float* lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += n_warps) {
+    const float a = la[r], b = lb[r];
+    const float m = fmaxf(a, b);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = -CUDART_INF_F;
+    if (m != -CUDART_INF_F) {
+      const float wa = (a == -CUDART_INF_F) ? 0.0f : expf(a - m);
+      const float wb = (b == -CUDART_INF_F) ? 0.0f : expf(b - m);
+      const float s = wa + wb;
+      const float4 x = reinterpret_cast<const float4*>(oa + r * kH)[lane];
+      const float4 y = reinterpret_cast<const float4*>(ob + r * kH)[lane];
+      v = make_float4((wa * x.x + wb * y.x) / s, (wa * x.y + wb * y.y) / s, (wa * x.z + wb * y.z) / s,
+                      (wa * x.w + wb * y.w) / s);
+      l = m + logf(s);
+    }
+    __syncwarp();   // every lane has read row r before it is overwritten in place
+    reinterpret_cast<float4*>(o + r * kH)[lane] = v;
+    if (lane == 0) lse[r] = l;
+  }
+}
+
 template <int MODE>
 cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
   constexpr int kSmem = Layout<MODE>::kTotal;
@@ -719,6 +748,14 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
   pl.pages_per_split = (max_pages + best_s - 1) / best_s;
   pl.ws_bytes = (size_t)units * pl.n_splits * kWsPerCta * sizeof(float);
   return pl;
+}
+
+cudaError_t launch_attn_merge(const float* oa, const float* la, const float* ob, const float* lb,
+                              int64_t rows, float* o, float* lse, cudaStream_t s) {
+  const int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  attn_merge_kernel<<<(int)(blocks < cap ? blocks : cap), 256, 0, s>>>(oa, la, ob, lb, rows, o, lse);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s) {

@@ -328,6 +328,22 @@ int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head
                        params->alpha, params->eps, stream);
 }
 
+int lynx_attn_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                    int64_t rows, int head_dim, float* o, float* lse, void* stream) {
+  g_last_error[0] = '\0';
+  if (rows < 0) return fail(LYNX_ERR_INVALID_ARG, "rows=%lld < 0", (long long)rows);
+  if (head_dim != kH) return fail(LYNX_ERR_UNSUPPORTED, "head_dim=%d (need 128)", head_dim);
+  if (rows == 0) return LYNX_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse)
+    return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(o_a) || misaligned(o_b) || misaligned(o) || misaligned(lse_a) || misaligned(lse_b) ||
+      misaligned(lse))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  cudaError_t e = launch_attn_merge(o_a, lse_a, o_b, lse_b, rows, o, lse, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_attn_merge launch");
+  return LYNX_OK;
+}
+
 int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
                           const void* k_pages, const void* v_pages, int64_t n_pool_pages,
                           const int32_t* page_table, int max_pages, const int32_t* ctx_len,

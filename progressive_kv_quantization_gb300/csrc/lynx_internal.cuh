@@ -101,5 +101,7 @@ int tc_rows_per_cta(int rows);
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);
+cudaError_t launch_attn_merge(const float* oa, const float* la, const float* ob, const float* lb,
+                              int64_t rows, float* o, float* lse, cudaStream_t s);
 
 }  // namespace lynx

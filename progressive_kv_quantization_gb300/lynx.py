@@ -60,6 +60,7 @@ SIGNATURES = {
                                      _VP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "lynx_decode_attn_noalloc": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                         _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP]),
+    "lynx_attn_merge": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]),
     "lynx_decode_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lynx_device_status": (_I32, []),
     "lynx_status_string": (ctypes.c_char_p, [_I32]),
@@ -252,6 +253,22 @@ def lynx_decode_attn_bf16(q, k_pages, v_pages, page_table, ctx_len, n_kv_heads, 
         _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_pages), _ptr(v_pages), n_pool, _ptr(page_table),
         max_pages, _ptr(ctx_len), scale, int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_decode_attn_bf16")
+    return out, lse
+
+
+def lynx_attn_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """Log-sum-exp merge of two attention results over disjoint key sets:
+    o_a, o_b [..., 128] float32 and lse_a, lse_b [...] float32 (natural log)."""
+    for t, nm in ((o_a, "o_a"), (o_b, "o_b")):
+        _need(t, torch.float32, nm)
+    for t, nm in ((lse_a, "lse_a"), (lse_b, "lse_b")):
+        _need(t, torch.float32, nm)
+    if o_a.shape != o_b.shape or lse_a.shape != lse_b.shape or tuple(o_a.shape[:-1]) != tuple(lse_a.shape):
+        raise LynxError("o_a/o_b [..., D] and lse_a/lse_b [...] shapes disagree")
+    out = out if out is not None else torch.empty_like(o_a)
+    lse = lse if lse is not None else torch.empty_like(lse_a)
+    _check(load().lynx_attn_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), lse_a.numel(),
+                                  o_a.shape[-1], _ptr(out), _ptr(lse), _stream(stream)), "lynx_attn_merge")
     return out, lse
 
 

@@ -103,3 +103,20 @@ def test_rows_without_visible_keys():
     assert np.max(np.abs(o[1] - o2[0])) < 1e-12 and abs(lse[1] - l2[0]) < 1e-12
     oe, le = at.attention_rows(q, k[:0], v[:0], 0.1)
     assert np.all(np.isnan(oe)) and np.all(np.isneginf(le))
+
+
+def test_vnmse_closed_forms():
+    """vNMSE is zero for identical outputs, 1 for o = 2 o_ref and 0.25 for
+    o = o_ref / 2 (per-row ||.||^2 ratios), averages rows with equal weight,
+    and does not change when every row of both outputs is scaled alike."""
+    rng = np.random.default_rng(5)
+    r = rng.standard_normal((6, 128))
+    assert at.vnmse(r, r) == 0.0
+    assert at.vnmse(2 * r, r) == pytest.approx(1.0)
+    assert at.vnmse(0.5 * r, r) == pytest.approx(0.25)
+    o = r.copy()
+    o[0] *= 3.0                                  # one row off by ||2r||^2/||r||^2 = 4
+    assert at.vnmse(o, r) == pytest.approx(4.0 / 6)
+    s = rng.uniform(0.1, 10.0, (6, 1))
+    assert at.vnmse(o * s, r * s) == pytest.approx(at.vnmse(o, r))
+    assert at.vnmse(o.reshape(2, 3, 128), r.reshape(2, 3, 128)) == pytest.approx(at.vnmse(o, r))
