@@ -89,7 +89,7 @@ class Stages:
     S: np.ndarray         # [N, H, P]    int32 +-1 (Stage 3)
 
 
-def normalise(x: np.ndarray, C: int, eps) -> tuple:
+def normalise(x: np.ndarray, C: int, eps, valid=None) -> tuple:
     """Stages 1 and 2 of Algorithm 1 on float32 pages x[N, H, P].
 
     Stage 1: per channel (row) of a page, gamma_min = min over the
@@ -97,20 +97,52 @@ def normalise(x: np.ndarray, C: int, eps) -> tuple:
     Stage 2: view each row as P/C chunks of C tokens; mu = mean of a
     chunk, X_cent = X - mu, sigma = max |X_cent| over the chunk,
     X_final = X_cent / (sigma + eps).
+
+    valid[N] (optional; a partial last page of a sequence): only tokens
+    t < valid[n] of page n enter the statistics.  gamma_min / gamma_scale are
+    taken over them (0 and 0 for an empty page); a chunk's mu is the
+    left-to-right float32 sum of its valid x_n divided by their count, sigma
+    the largest |x_n - mu| among them (mu = sigma = 0 for a chunk without
+    valid tokens); tokens past valid[n] get X_cent = X_final = 0 (code 0,
+    positive sign).  With every valid[n] = P this is the full-page rule.
     """
     x = np.asarray(x, dtype=np.float32)
     N, H, P = x.shape
     assert P % C == 0
     e = np.float32(eps)
-    gmin = x.min(axis=2)
-    gscale = x.max(axis=2) - gmin
-    xn = (x - gmin[:, :, None]) / (gscale + e)[:, :, None]
+    if valid is None:
+        gmin = x.min(axis=2)
+        gscale = x.max(axis=2) - gmin
+        xn = (x - gmin[:, :, None]) / (gscale + e)[:, :, None]
+        xv = xn.reshape(N, H, P // C, C)
+        s = xv[..., 0].copy()
+        for j in range(1, C):                 # left-to-right float32 sum
+            s = s + xv[..., j]
+        mu = s / np.float32(C)
+        xcent = xv - mu[..., None]
+        sigma = np.abs(xcent).max(axis=3)
+        xfinal = xcent / (sigma + e)[..., None]
+        return gmin, gscale, xn, mu, xcent, sigma, xfinal
+    v = np.asarray(valid, dtype=np.int64).reshape(N, 1, 1)
+    assert np.all((v >= 0) & (v <= P))
+    m = np.arange(P)[None, None, :] < v                      # [N, 1, P]
+    gmin = np.where(m, x, np.float32(np.inf)).min(axis=2)
+    gmax = np.where(m, x, np.float32(-np.inf)).max(axis=2)
+    empty = v[:, 0, 0] == 0
+    gmin[empty] = 0.0
+    gmax[empty] = 0.0
+    gscale = gmax - gmin
+    xs = np.where(m, x, gmin[:, :, None])                    # padding never enters an operation
+    xn = (xs - gmin[:, :, None]) / (gscale + e)[:, :, None]
     xv = xn.reshape(N, H, P // C, C)
-    s = xv[..., 0].copy()
-    for j in range(1, C):                 # left-to-right float32 sum
-        s = s + xv[..., j]
-    mu = s / np.float32(C)
-    xcent = xv - mu[..., None]
+    mv = np.broadcast_to(m.reshape(N, 1, P // C, C), xv.shape)
+    nc = mv.sum(axis=3)
+    s = np.zeros(xv.shape[:3], dtype=np.float32)
+    for j in range(C):                                        # left-to-right over the valid tokens
+        s = np.where(mv[..., j], s + xv[..., j], s)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        mu = np.where(nc > 0, s / np.maximum(nc, 1).astype(np.float32), np.float32(0)).astype(np.float32)
+    xcent = np.where(mv, xv - mu[..., None], np.float32(0)).astype(np.float32)
     sigma = np.abs(xcent).max(axis=3)
     xfinal = xcent / (sigma + e)[..., None]
     return gmin, gscale, xn, mu, xcent, sigma, xfinal
@@ -200,22 +232,24 @@ def unpack_meta(meta: np.ndarray, H: int, P: int, C: int):
     return gmin, gscale, mu, sigma
 
 
-def run_stages(x_bits: np.ndarray, alpha, eps, C: int = 32) -> Stages:
-    """All intermediates of Algorithm 1 for BF16 pages x_bits[N, H, P]."""
+def run_stages(x_bits: np.ndarray, alpha, eps, C: int = 32, valid=None) -> Stages:
+    """All intermediates of Algorithm 1 for BF16 pages x_bits[N, H, P]
+    (valid: optional per-page count of valid tokens, see ``normalise``)."""
     x = bf16_to_f32(x_bits)
     N, H, P = x.shape
-    gmin, gscale, xn, mu, xcent, sigma, xfinal = normalise(x, C, eps)
+    gmin, gscale, xn, mu, xcent, sigma, xfinal = normalise(x, C, eps, valid)
     Y, I, S = quantise(xfinal.reshape(N, H, P), alpha)
     return Stages(gmin, gscale, xn, mu, xcent, sigma, xfinal, Y, I, S)
 
 
-def encode_pages(x_bits: np.ndarray, alpha, eps, C: int = 32, return_stages: bool = False):
+def encode_pages(x_bits: np.ndarray, alpha, eps, C: int = 32, return_stages: bool = False, valid=None):
     """Algorithm 1 on BF16 pages [N, H, P]; returns (anchor, residual, meta).
 
     anchor, residual: uint8 [N, H, P/2] packed planes; meta: float32
     [N, 2H + 2H*P/C] = gamma_min[H], gamma_scale[H], mu[P/C][H], sigma[P/C][H].
+    valid[N] (optional): per-page count of valid tokens (partial last pages).
     """
-    st = run_stages(x_bits, alpha, eps, C)
+    st = run_stages(x_bits, alpha, eps, C, valid)
     q_anc, q_res = split_stream(st.I, st.S)
     anchor = pack_nibbles(q_anc)
     residual = pack_nibbles(q_res)

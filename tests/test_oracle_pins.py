@@ -293,3 +293,89 @@ def test_metadata_size_printed():
     assert n == g["scalars"]
     assert round(n * 4 / 1024) == g["printed_KB_fp32"]
     assert round(n * 4 / (g["H"] * g["P"] * 2), 2) == g["printed_overhead_fraction"]
+
+
+# ---------------------------------------------------------------- partial pages
+def _pages(n, seed):
+    out = inputs.outlier_pairs(1, seed)
+    return inputs.kv_pages_np(1, 256 * n, seed, out)
+
+
+def test_partial_rule_with_full_pages_is_the_full_page_rule():
+    x = _pages(3, 31)
+    full = lo.encode_pages(x, 100.0, 1e-6)
+    part = lo.encode_pages(x, 100.0, 1e-6, valid=np.full(3, 256))
+    for a, b in zip(full, part):
+        assert np.array_equal(a, b)
+
+
+def test_partial_page_ignores_its_padding():
+    """Whatever the padding holds (other values, huge values, NaN or Inf bits),
+    the valid tokens' codes and every metadata value stay the same, and padding
+    tokens get code 0 with a positive sign (anchor 0, residual 7)."""
+    rng = np.random.default_rng(7)
+    x = _pages(4, 32)
+    valid = np.array([1, 77, 200, 255])
+    ref = lo.encode_pages(x, 100.0, 1e-6, valid=valid)
+    for fill in ("random", "huge", "nonfinite"):
+        y = x.copy()
+        for n, v in enumerate(valid):
+            if fill == "random":
+                y[n, :, v:] = rng.integers(0, 1 << 16, y[n, :, v:].shape, dtype=np.uint16) & 0x7F7F
+            elif fill == "huge":
+                y[n, :, v:] = 0x7F00                      # 2^127
+            else:
+                y[n, :, v:] = np.where(rng.random(y[n, :, v:].shape) < 0.5, 0x7FC0, 0xFF80)
+        got = lo.encode_pages(y, 100.0, 1e-6, valid=valid)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b)
+    qa = lo.unpack_nibbles(ref[0])
+    qr = lo.unpack_nibbles(ref[1])
+    for n, v in enumerate(valid):
+        assert np.all(qa[n, :, v:] == 0) and np.all(qr[n, :, v:] == 7)
+
+
+def test_partial_page_whole_chunks_match_a_full_page_with_neutral_padding():
+    """If the invalid tokens form whole chunks and are filled with the row's valid
+    minimum (so that min and max do not change), the valid chunks' codes and
+    statistics equal those of the full-page encoding of the filled page."""
+    x = _pages(1, 33)
+    v = 160                                           # chunks 0-4 valid, 5-7 invalid
+    xf = lo.bf16_to_f32(x)
+    y = x.copy()
+    rowmin = np.argmin(xf[0, :, :v], axis=1)
+    for c in range(128):
+        y[0, c, v:] = x[0, c, rowmin[c]]
+    a_p, r_p, m_p = lo.encode_pages(x, 100.0, 1e-6, valid=[v])
+    a_f, r_f, m_f = lo.encode_pages(y, 100.0, 1e-6)
+    assert np.array_equal(a_p[0, :, :v // 2], a_f[0, :, :v // 2])
+    assert np.array_equal(r_p[0, :, :v // 2], r_f[0, :, :v // 2])
+    gp, sp, mup, sgp = lo.unpack_meta(m_p, 128, 256, 32)
+    gf, sf, muf, sgf = lo.unpack_meta(m_f, 128, 256, 32)
+    assert np.array_equal(gp, gf) and np.array_equal(sp, sf)
+    assert np.array_equal(mup[..., :5], muf[..., :5]) and np.array_equal(sgp[..., :5], sgf[..., :5])
+    assert np.all(mup[..., 5:] == 0) and np.all(sgp[..., 5:] == 0)
+
+
+def test_partial_page_statistics_brute_force():
+    """gamma_min / gamma_scale are the min and the float32 range of the valid
+    tokens; a partly valid chunk's mu is within float32 summation error of the
+    float64 mean of its valid x_n and its sigma is the largest deviation among
+    them; a page with no valid token has all-zero metadata."""
+    x = _pages(2, 34)
+    valid = np.array([77, 0])
+    st = lo.run_stages(x, 100.0, 1e-6, valid=valid)
+    xf = lo.bf16_to_f32(x).astype(np.float64)
+    v = 77
+    assert np.array_equal(st.gmin[0], xf[0, :, :v].min(axis=1).astype(np.float32))
+    assert np.array_equal(st.gscale[0], (xf[0, :, :v].max(axis=1) - xf[0, :, :v].min(axis=1)).astype(np.float32))
+    xn = st.xn[0].astype(np.float64)                  # [128, 256]
+    for c in range(3):                                # chunk 2 holds 13 valid tokens
+        lo_t, hi_t = 32 * c, min(32 * c + 32, v)
+        ref_mu = xn[:, lo_t:hi_t].mean(axis=1)
+        assert np.all(np.abs(st.mu[0, :, c] - ref_mu) <= 32 * 2.0 ** -24 * np.maximum(1.0, np.abs(ref_mu)))
+        dev = np.abs(xn[:, lo_t:hi_t] - st.mu[0, :, c:c + 1].astype(np.float64))
+        assert np.all(np.abs(st.sigma[0, :, c] - dev.max(axis=1)) <= 2.0 ** -23)
+    assert np.all(st.mu[0, :, 3:] == 0) and np.all(st.sigma[0, :, 3:] == 0)
+    assert np.all(st.gmin[1] == 0) and np.all(st.gscale[1] == 0)
+    assert np.all(st.mu[1] == 0) and np.all(st.sigma[1] == 0) and np.all(st.I[1] == 0)
