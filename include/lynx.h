@@ -116,6 +116,23 @@ enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 };
 int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
                       uint8_t* anchor, uint8_t* residual, float* meta, void* stream);
 
+/* Algorithm 1 on pages of which only a prefix of tokens is valid (the last,
+ * partial page of a sequence; the paper encodes whole pages only).
+ *   valid_tokens  [n_pages] int32 (device): page n's tokens 0 .. valid_tokens[n]-1
+ *                 are valid; values are clamped to 0..256.
+ * The statistics cover the valid tokens only: gamma_min / gamma_scale over
+ * them (0 and 0 for an empty page); a chunk's mu is the left-to-right sum of
+ * its valid x_n divided by their count (a correctly rounded float32
+ * division), sigma the largest |x_n - mu| among them, and mu = sigma = 0 for
+ * a chunk without valid tokens.  Padding tokens take no part in any
+ * operation (their contents may be anything) and get code 0 with a positive
+ * sign (anchor nibble 0, residual nibble 7).  A page with 256 valid tokens is
+ * encoded exactly as lynx_encode_pages encodes it.  Other arguments and
+ * errors as lynx_encode_pages; INVALID_ARG for a NULL valid_tokens. */
+int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t* valid_tokens,
+                              const lynx_params_t* params, uint8_t* anchor, uint8_t* residual,
+                              float* meta, void* stream);
+
 /* Stage 3 of Algorithm 1 alone: codes[i] = round(127 ln(1 + alpha |a_i|) /
  * ln(1 + alpha)) in 0..127 for float32 magnitudes |a_i| <= 1 (larger values
  * are clamped to 1), decided exactly for the float32 input as in

@@ -129,9 +129,15 @@ __device__ __forceinline__ void load_chunk(const uint4* __restrict__ src, uint4 
   for (int k = 0; k < 4; ++k) raw[k] = __ldg(src + k);
 }
 
+// PARTIAL: valid[page] (clamped to 0..256) tokens of each page are valid; the
+// statistics cover them only, padding tokens get code 0 with a positive sign,
+// and a chunk without valid tokens gets mu = sigma = 0 (a partial last page of
+// a sequence).  With 256 valid tokens the result is the full-page one.
+template <bool PARTIAL>
 __global__ void __launch_bounds__(256, 2)
 encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__ anchor,
-              uint4* __restrict__ residual, float* __restrict__ meta, const EncodeTables tab) {
+              uint4* __restrict__ residual, float* __restrict__ meta, const EncodeTables tab,
+              const int32_t* __restrict__ valid) {
   __shared__ float s_thr[129];
   for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
   __syncthreads();
@@ -157,14 +163,27 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     const int64_t g_next = g + n_warps;
     if (g_next < n_groups) load_chunk(x + g_next * 128 + lane * 4, raw);
 
+    // valid tokens of the page and of this lane's chunk
+    int v_page = 256, nc = 32;
+    uint32_t wmin[16], wmax[16];   // the pairs with padding replaced by +inf / -inf (PARTIAL)
+    if (PARTIAL) {
+      v_page = min(max(__ldg(valid + (g >> 5)), 0), 256);
+      nc = min(max(v_page - 32 * (lane & 7), 0), 32);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const bool lo = 2 * t < nc, hi = 2 * t + 1 < nc;
+        wmin[t] = (lo ? (w[t] & 0xFFFFu) : 0x7F80u) | (hi ? (w[t] & 0xFFFF0000u) : 0x7F800000u);
+        wmax[t] = (lo ? (w[t] & 0xFFFFu) : 0xFF80u) | (hi ? (w[t] & 0xFFFF0000u) : 0xFF800000u);
+      }
+    }
+
     // ---- chunk and row extremes on the packed BF16 pairs (exact)
-    __nv_bfloat162 bmn = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
-    __nv_bfloat162 bmx = bmn;
+    __nv_bfloat162 bmn = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[0] : &w[0]);
+    __nv_bfloat162 bmx = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[0] : &w[0]);
 #pragma unroll
     for (int t = 1; t < 16; ++t) {
-      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[t]);
-      bmn = __hmin2(bmn, v);
-      bmx = __hmax2(bmx, v);
+      bmn = __hmin2(bmn, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[t] : &w[t]));
+      bmx = __hmax2(bmx, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[t] : &w[t]));
     }
     const float cmn = fminf(__low2float(bmn), __high2float(bmn));   // chunk min of x
     const float cmx = fmaxf(__low2float(bmx), __high2float(bmx));   // chunk max of x
@@ -173,6 +192,10 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     for (int o = 1; o < 8; o <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (PARTIAL && v_page == 0) {   // an empty page: gamma_min = gamma_scale = 0
+      mn = 0.0f;
+      mx = 0.0f;
     }
 
     // ---- Stage 1: x_n = (x - gamma_min) / (gamma_scale + eps)
@@ -183,7 +206,11 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     float2 xn[16];
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
-      const float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+      float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+      if (PARTIAL) {   // padding enters no operation: it becomes gamma_min, so x_n = 0 exactly
+        v.x = 2 * t < nc ? v.x : mn;
+        v.y = 2 * t + 1 < nc ? v.y : mn;
+      }
       xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
     }
 
@@ -195,10 +222,14 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
       s = __fadd_rn(s, xn[t].x);
       s = __fadd_rn(s, xn[t].y);
     }
-    const float mu = __fmul_rn(s, 0.03125f);
+    // (PARTIAL: padding adds exact zeros, so s is the left-to-right sum of the valid x_n)
+    float mu = __fmul_rn(s, 0.03125f);
+    if (PARTIAL && nc < 32)
+      mu = nc == 0 ? 0.0f : div1(s, (float)nc, __frcp_rn((float)nc));
     const float xn_max = div1(__fsub_rn(cmx, mn), dg, rg);
     const float xn_min = div1(__fsub_rn(cmn, mn), dg, rg);
-    const float sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
+    float sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
+    if (PARTIAL && nc == 0) sigma = 0.0f;
     const float ds = __fadd_rn(sigma, eps);
     const float rs = __frcp_rn(ds);
     const float2 nmu2 = f2(-mu), rs2 = f2(rs);
@@ -214,7 +245,11 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = 4 * q + u;
-        const float2 xc = __fadd2_rn(xn[t], nmu2);
+        float2 xc = __fadd2_rn(xn[t], nmu2);
+        if (PARTIAL) {   // padding: x_c = +0, hence code 0 with a positive sign
+          xc.x = 2 * t < nc ? xc.x : 0.0f;
+          xc.y = 2 * t + 1 < nc ? xc.y : 0.0f;
+        }
         xs[2 * u] = xc.x;
         xs[2 * u + 1] = xc.y;
         a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
@@ -277,6 +312,29 @@ quantize_kernel(const float* __restrict__ a, int64_t n, uint8_t* __restrict__ co
 
 }  // namespace
 
+template <bool PARTIAL>
+cudaError_t launch_encode_t(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
+                            float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s) {
+  const int64_t n_groups = n_pages * 32;
+  const int threads = 256;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<PARTIAL>, threads, 0);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
+  const int64_t need = (n_groups + 7) / 8;
+  const int blocks = (int)(need < max_blocks ? need : max_blocks);
+  encode_kernel<PARTIAL><<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), n_groups,
+                                                   reinterpret_cast<uint4*>(anchor),
+                                                   reinterpret_cast<uint4*>(residual), meta, *tab, valid);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
+                          float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s) {
+  return valid ? launch_encode_t<true>(x, n_pages, anchor, residual, meta, tab, valid, s)
+               : launch_encode_t<false>(x, n_pages, anchor, residual, meta, tab, nullptr, s);
+}
+
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,
                             cudaStream_t s) {
   const int64_t groups = (n + 7) / 8;
@@ -286,20 +344,6 @@ cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const Enc
   return cudaGetLastError();
 }
 
-cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
-                          float* meta, const EncodeTables* tab, cudaStream_t s) {
-  const int64_t n_groups = n_pages * 32;
-  const int threads = 256;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, threads, 0);
-  if (per_sm < 1) per_sm = 1;
-  const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
-  const int64_t need = (n_groups + 7) / 8;
-  const int blocks = (int)(need < max_blocks ? need : max_blocks);
-  encode_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), n_groups,
-                                          reinterpret_cast<uint4*>(anchor),
-                                          reinterpret_cast<uint4*>(residual), meta, *tab);
-  return cudaGetLastError();
-}
+
 
 }  // namespace lynx

@@ -170,8 +170,10 @@ const char* lynx_status_string(int status) {
   }
 }
 
-int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
-                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream) {
+namespace {
+
+int encode_common(const void* x_bf16, int64_t n_pages, const int32_t* valid, const lynx_params_t* params,
+                  uint8_t* anchor, uint8_t* residual, float* meta, void* stream, const char* name) {
   g_last_error[0] = '\0';
   int st = check_params(params);
   if (st != LYNX_OK) return st;
@@ -179,14 +181,34 @@ int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* 
   if (n_pages == 0) return LYNX_OK;
   if (!x_bf16 || !anchor || !residual || !meta)
     return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
-  if (misaligned(x_bf16) || misaligned(anchor) || misaligned(residual) || misaligned(meta))
+  if (misaligned(x_bf16) || misaligned(anchor) || misaligned(residual) || misaligned(meta) ||
+      (valid && misaligned(valid)))
     return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
   if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
   const EncodeTables* tab = encode_tables(params->alpha, params->eps);
-  cudaError_t e = launch_encode(x_bf16, n_pages, anchor, residual, meta, tab,
+  cudaError_t e = launch_encode(x_bf16, n_pages, anchor, residual, meta, tab, valid,
                                 static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_pages launch");
+  if (e != cudaSuccess) return cuda_fail(e, name);
   return LYNX_OK;
+}
+
+}  // namespace
+
+int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* params,
+                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream) {
+  return encode_common(x_bf16, n_pages, nullptr, params, anchor, residual, meta, stream,
+                       "lynx_encode_pages launch");
+}
+
+int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t* valid_tokens,
+                              const lynx_params_t* params, uint8_t* anchor, uint8_t* residual,
+                              float* meta, void* stream) {
+  if (!valid_tokens && n_pages > 0) {
+    g_last_error[0] = '\0';
+    return fail(LYNX_ERR_INVALID_ARG, "NULL valid_tokens");
+  }
+  return encode_common(x_bf16, n_pages, valid_tokens, params, anchor, residual, meta, stream,
+                       "lynx_encode_pages_partial launch");
 }
 
 int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* params,

@@ -52,6 +52,7 @@ _VP, _I64, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctyp
 _PP = ctypes.POINTER(lynx_params_t)
 SIGNATURES = {
     "lynx_encode_pages": (_I32, [_VP, _I64, _PP, _VP, _VP, _VP, _VP]),
+    "lynx_encode_pages_partial": (_I32, [_VP, _I64, _VP, _PP, _VP, _VP, _VP, _VP]),
     "lynx_reconstruct": (_I32, [_VP, _VP, _VP, _I64, _PP, _VP, _I32, _VP]),
     "lynx_quantize_magnitudes": (_I32, [_VP, _I64, _PP, _VP, _VP]),
     "lynx_decode_attn": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -110,9 +111,11 @@ def _need(t, dtype, name, device=None):
 
 
 def lynx_encode_pages(x, params: Params = Params(), anchor=None, residual=None, meta=None,
-                      stream=None):
+                      stream=None, valid_tokens=None):
     """Algorithm 1 on BF16 pages x[N, 128, 256] -> (anchor u8[N,128,128],
-    residual u8[N,128,128], meta f32[N, 2304])."""
+    residual u8[N,128,128], meta f32[N, 2304]).  valid_tokens (int32 [N] on the
+    device, optional) selects lynx_encode_pages_partial: only the first
+    valid_tokens[n] tokens of page n are valid."""
     _need(x, torch.bfloat16, "x")
     n = x.numel() // (H * P)
     if x.numel() != n * H * P:
@@ -127,6 +130,14 @@ def lynx_encode_pages(x, params: Params = Params(), anchor=None, residual=None, 
     if anchor.numel() < n * PLANE_BYTES or residual.numel() < n * PLANE_BYTES or meta.numel() < n * META_FLOATS:
         raise LynxError("output buffers too small")
     p = params.c()
+    if valid_tokens is not None:
+        _need(valid_tokens, torch.int32, "valid_tokens")
+        if valid_tokens.numel() != n:
+            raise LynxError("valid_tokens needs one count per page")
+        _check(load().lynx_encode_pages_partial(_ptr(x), n, _ptr(valid_tokens), ctypes.byref(p), _ptr(anchor),
+                                                _ptr(residual), _ptr(meta), _stream(stream)),
+               "lynx_encode_pages_partial")
+        return anchor, residual, meta
     _check(load().lynx_encode_pages(_ptr(x), n, ctypes.byref(p), _ptr(anchor), _ptr(residual),
                                     _ptr(meta), _stream(stream)), "lynx_encode_pages")
     return anchor, residual, meta

@@ -296,13 +296,13 @@ def test_metadata_size_printed():
 
 
 # ---------------------------------------------------------------- partial pages
-def _pages(n, seed):
+def _partial_pages(n, seed):
     out = inputs.outlier_pairs(1, seed)
     return inputs.kv_pages_np(1, 256 * n, seed, out)
 
 
 def test_partial_rule_with_full_pages_is_the_full_page_rule():
-    x = _pages(3, 31)
+    x = _partial_pages(3, 31)
     full = lo.encode_pages(x, 100.0, 1e-6)
     part = lo.encode_pages(x, 100.0, 1e-6, valid=np.full(3, 256))
     for a, b in zip(full, part):
@@ -314,7 +314,7 @@ def test_partial_page_ignores_its_padding():
     the valid tokens' codes and every metadata value stay the same, and padding
     tokens get code 0 with a positive sign (anchor 0, residual 7)."""
     rng = np.random.default_rng(7)
-    x = _pages(4, 32)
+    x = _partial_pages(4, 32)
     valid = np.array([1, 77, 200, 255])
     ref = lo.encode_pages(x, 100.0, 1e-6, valid=valid)
     for fill in ("random", "huge", "nonfinite"):
@@ -339,7 +339,7 @@ def test_partial_page_whole_chunks_match_a_full_page_with_neutral_padding():
     """If the invalid tokens form whole chunks and are filled with the row's valid
     minimum (so that min and max do not change), the valid chunks' codes and
     statistics equal those of the full-page encoding of the filled page."""
-    x = _pages(1, 33)
+    x = _partial_pages(1, 33)
     v = 160                                           # chunks 0-4 valid, 5-7 invalid
     xf = lo.bf16_to_f32(x)
     y = x.copy()
@@ -362,7 +362,7 @@ def test_partial_page_statistics_brute_force():
     tokens; a partly valid chunk's mu is within float32 summation error of the
     float64 mean of its valid x_n and its sigma is the largest deviation among
     them; a page with no valid token has all-zero metadata."""
-    x = _pages(2, 34)
+    x = _partial_pages(2, 34)
     valid = np.array([77, 0])
     st = lo.run_stages(x, 100.0, 1e-6, valid=valid)
     xf = lo.bf16_to_f32(x).astype(np.float64)
