@@ -157,3 +157,68 @@ def test_encode_then_reconstruct_round_trip(cuda_device):
         # a code that differs by one at a rounding edge moves that element by one code step
         err = np.abs(out.cpu().numpy() - ref) <= recon_bound(om)
         assert err.mean() > 1 - 1e-4
+
+
+# ---------------------------------------------------------------- partial pages
+def test_partial_pages_parity_and_padding_independence(cuda_device):
+    """lynx_encode_pages_partial against the oracle's partial-page rule for valid
+    counts at and around every chunk edge (0, 1, 31, 32, 33, 77, 128, 255, 256),
+    over random padding; pages with 256 valid tokens are byte-identical to
+    lynx_encode_pages, and changing the padding changes nothing."""
+    counts = np.array([0, 1, 31, 32, 33, 77, 128, 255, 256, 256, 160, 2])
+    n = len(counts)
+    bits = inputs.kv_pages_np(2, 256 * n // 2, 81, inputs.outlier_pairs(2, 81))
+    rng = np.random.default_rng(82)
+    for p, v in enumerate(counts):
+        bits[p, :, v:] = rng.integers(0, 1 << 16, bits[p, :, v:].shape, dtype=np.uint16) & 0x7F7F
+    valid = torch.from_numpy(counts.astype(np.int32)).cuda()
+    a, r, m = L.lynx_encode_pages(to_dev(bits), valid_tokens=valid)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    oa, orr, om, st = lo.encode_pages(bits, 100.0, EPS, return_stages=True, valid=counts)
+    check_codes(a.cpu().numpy(), r.cpu().numpy(), oa, orr, st.Y)
+    check_meta(m.cpu().numpy(), om)
+    # full pages: the partial kernel reproduces the full-page kernel byte for byte
+    fa, fr, fm = L.lynx_encode_pages(to_dev(bits))
+    full = np.nonzero(counts == 256)[0]
+    assert np.array_equal(a.cpu().numpy()[full], fa.cpu().numpy()[full])
+    assert np.array_equal(r.cpu().numpy()[full], fr.cpu().numpy()[full])
+    assert np.array_equal(m.cpu().numpy()[full], fm.cpu().numpy()[full])
+    # other padding (huge values and non-finite bits): same output
+    b2 = bits.copy()
+    for p, v in enumerate(counts):
+        b2[p, :, v:] = np.where(rng.random(b2[p, :, v:].shape) < 0.5, 0x7F00, 0xFF80)
+    a2, r2, m2 = L.lynx_encode_pages(to_dev(b2), valid_tokens=valid)
+    assert np.array_equal(a2.cpu().numpy(), a.cpu().numpy())
+    assert np.array_equal(r2.cpu().numpy(), r.cpu().numpy())
+    assert np.array_equal(m2.cpu().numpy(), m.cpu().numpy())
+
+
+def test_partial_last_page_then_decode(cuda_device):
+    """A 1,000-token sequence (last page 232 tokens) encoded on the GPU with its
+    valid counts, then decoded over its anchor and full codes: against the oracle
+    over the oracle's encoding of the same pages."""
+    from oracle import attention as at
+    import math
+    Hkv, Hq, ctx = 2, 8, 1000
+    out = inputs.outlier_pairs(Hkv, 83)
+    kb = inputs.kv_pages_np(Hkv, 1024, 84, out)
+    vb = inputs.kv_pages_np(Hkv, 1024, 85, out)
+    counts = np.tile(np.array([256, 256, 256, ctx - 768], dtype=np.int32), Hkv)
+    valid = torch.from_numpy(counts).cuda()
+    ka, kr, km = L.lynx_encode_pages(to_dev(kb), valid_tokens=valid)
+    va, vr, vm = L.lynx_encode_pages(to_dev(vb), valid_tokens=valid)
+    oka, okr, okm = lo.encode_pages(kb, 100.0, EPS, valid=counts)
+    ova, ovr, ovm = lo.encode_pages(vb, 100.0, EPS, valid=counts)
+    table = torch.from_numpy(np.array([[[4 * h + p for p in range(4)] for h in range(Hkv)]], dtype=np.int32)).cuda()
+    q = inputs.queries_np((1, 1, Hq, 128), 86)
+    qd = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
+    cl = torch.from_numpy(np.array([ctx], dtype=np.int32)).cuda()
+    for full in (False, True):
+        o, lse = L.lynx_decode_attn(qd, ka, kr if full else None, km, va, vr if full else None, vm, table, cl, Hkv)
+        kd = lo.reconstruct(oka, okr if full else None, okm, 100.0, EPS)
+        vd = lo.reconstruct(ova, ovr if full else None, ovm, 100.0, EPS)
+        ro, rl = at.decode_attention(lo.bf16_to_f32(q).astype(np.float64), lambda ids: (kd[ids], vd[ids]),
+                                     table.cpu().numpy(), np.array([ctx]), Hkv, 1 / math.sqrt(128), False)
+        from lynx_testutil import check_attention
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
