@@ -23,9 +23,9 @@ constexpr int kRows = 4;
 constexpr int kWsPerCta = kRows * kH + 2 * kRows;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
-template <bool FULL>
+template <bool FULL, int STAGES = 3>
 struct QGeo {
-  static constexpr int kStages = 3;
+  static constexpr int kStages = STAGES;
   static constexpr int kUnit = FULL ? 2 * kPlaneBytes + kMetaBytes : kPlaneBytes + kMetaBytes;
   static constexpr int kResOff = kPlaneBytes;
   static constexpr int kMetaOff = FULL ? 2 * kPlaneBytes : kPlaneBytes;
@@ -118,12 +118,12 @@ __device__ __forceinline__ T lds(const uint8_t* smem, uint32_t off) {
 // is reported (status 2) and page 0 read instead.  A wait that gives up sets
 // status 1 and the CTA's abort flag, then waits (bounded) for the copies
 // already in flight to land before returning.
-template <bool FULL>
+template <bool FULL, int STAGES = 3>
 __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np,
                               uint32_t s_ring, uint32_t bar_full, uint32_t bar_empty,
                               const CUtensorMap* tm_ka, const CUtensorMap* tm_va,
                               const CUtensorMap* tm_kr, const CUtensorMap* tm_vr, int* s_flag) {
-  using G = QGeo<FULL>;
+  using G = QGeo<FULL, STAGES>;
   constexpr int kSt = G::kStages;
   int issued = 0;
   bool ok = true;

@@ -42,9 +42,14 @@ constexpr int kWarpPs01 = kWarpCoef + kH * 4 * 4;
 constexpr int kWarpPs23 = kWarpPs01 + 16 * 16;
 constexpr int kWarpBytes = kWarpPs23 + 16 * 16;
 
+// ring slots of the CUDA-core kernel: 4 for the anchor planes (more bytes in
+// flight; shared memory allows it), 3 for the full codes
+template <bool FULL>
+constexpr int kStagesQ = FULL ? 3 : 4;
+
 template <bool FULL>
 struct QLayout {
-  using G = QGeo<FULL>;
+  using G = QGeo<FULL, kStagesQ<FULL>>;
   static constexpr int kRing = 0;
   static constexpr int kLut = kRing + G::kStages * G::kUnit;
   static constexpr int kWarps = kLut + G::kLutBytes;
@@ -86,7 +91,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 decode_quant_kernel(const DecodeArgs a, const LutTables lut,
                     const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_va,
                     const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr) {
-  using G = QGeo<FULL>;
+  using G = QGeo<FULL, kStagesQ<FULL>>;
   using S = QLayout<FULL>;
   constexpr int kSt = G::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -173,7 +178,7 @@ decode_quant_kernel(const DecodeArgs a, const LutTables lut,
   if (warp == kConsumers) {
     // ================= producer
     if (L == 0)
-      produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
+      produce_units<FULL, kStagesQ<FULL>>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
     // ================= consumers: warp `warp` owns chunk `warp` of every page
