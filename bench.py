@@ -376,78 +376,118 @@ def cpu_baseline_subprocess(seconds):
 
 
 def run_e2e(torch, L, b, ks, args, dev):
-    """The same step through host buffers: the BF16 cache and the queries are
-    copied in from pinned host memory, and the step's results (encoded planes,
-    metadata, attention outputs) are read back, every step.
+    """The same step's work through host buffers: the BF16 cache and the queries
+    are copied in from pinned host memory, and the step's results (encoded
+    planes, metadata, attention outputs) are read back, every step.
 
-    The cache moves in E2E_CHUNKS page chunks: chunk i is copied in on an
-    upload stream and encoded on the compute stream as soon as it has landed,
-    and its planes and metadata go back on a readback stream while later
-    chunks and the rest of the step run.  The next step's uploads wait for the
-    previous step's last use of the BF16 cache (the BF16 decode), and every step
-    ends when its readbacks have finished."""
+    The step runs per chunk of E2E_CHUNKS: chunk c is 64 / E2E_CHUNKS layers
+    (their K and V pages are contiguous).  Its BF16 pages are copied in on an
+    upload stream; once they have landed, the compute stream encodes them and
+    runs every call of the step on those layers (both reconstructions, the
+    decodes of the sequences that read them, the verification and the BF16
+    decode), and a readback stream returns its planes, metadata and outputs.
+    Later chunks' uploads overlap earlier chunks' compute.  The readbacks start
+    once every upload of the step has finished: on this host link, transfers in
+    both directions at once were measured to drop at times from 342 GB/s to
+    ~130 GB/s, which made the step time vary 3x.  The next step's uploads wait
+    until the previous step no longer reads the BF16 cache; a step ends when all
+    its readbacks have finished."""
+    n_chunks = E2E_CHUNKS
+    lpc = N_LAYERS // n_chunks                # layers per chunk
+    ppc = N_PAGES // n_chunks                 # pages per chunk (K and V of lpc layers)
+    anc, res, meta = b["anc"], b["res"], b["meta"]
+    kA, vA, kR, vR, kM, vM = anc, anc[PER:], res, res[PER:], meta, meta[PER:]
+    xk, xv = b["x"], b["x"][PER:]
+    p = L.Params()
     host_x = torch.empty(b["x"].shape, dtype=torch.bfloat16, pin_memory=True)
     host_x.copy_(b["x"])
-    h_q = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True).copy_(b[k]) for k in ("q1", "q8", "qv")}
-    planes = ["anc", "res", "meta"]
-    small = ["o1", "o8", "ov", "l1", "l8", "lv"]
-    h_out = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in planes + small}
-    h2d = host_x.numel() * 2 + sum(v.numel() * v.element_size() for v in h_q.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    p = L.Params()
-    n_chunks = E2E_CHUNKS
-    step = N_PAGES // n_chunks
-    rng = [(c * step, (c + 1) * step) for c in range(n_chunks)]
-    ev_in = [torch.cuda.Event() for _ in rng]
-    ev_enc = [torch.cuda.Event() for _ in rng]
-    ev_q, ev_free, ev_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    # the B = 8 sequences grouped by the layer their pages belong to
+    layer8 = [(s // 8 + s % 8) % N_LAYERS for s in range(8 * N_LAYERS)]
+    idx8 = [torch.tensor([s for s in range(8 * N_LAYERS) if layer8[s] // lpc == c], device=dev)
+            for c in range(n_chunks)]
+    c8 = [{k: b[k].index_select(0, idx8[c]).contiguous() for k in ("q8", "pt8", "ctx8")} for c in range(n_chunks)]
+    h_q = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True).copy_(b[k]) for k in ("q1", "qv")}
+    h_q8 = [torch.empty(c["q8"].shape, dtype=c["q8"].dtype, pin_memory=True).copy_(c["q8"]) for c in c8]
+    o8 = [{"o": torch.empty((len(idx8[c]), 1, HQ, 128), dtype=torch.float32, device=dev),
+           "l": torch.empty((len(idx8[c]), 1, HQ), dtype=torch.float32, device=dev)} for c in range(n_chunks)]
+    h_out = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in ("anc", "res", "meta", "o1", "ov", "l1", "lv")}
+    h_o8 = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in o8[c].items()} for c in range(n_chunks)]
+
+    def ws(B, T):
+        n = L.lynx_decode_attn_workspace_size(B, T, HQ, HKV, 128, NPPH)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    ws1, ws8, wsv = ws(lpc, 1), ws(8 * lpc, 1), ws(lpc, 8)
+    h2d = host_x.numel() * 2 + sum(v.numel() * v.element_size() for v in h_q.values()) + \
+        sum(v.numel() * v.element_size() for v in h_q8)
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + \
+        sum(v.numel() * v.element_size() for d in h_o8 for v in d.values())
+    # compute, uploads and readbacks each on a stream of their own (none of them the
+    # legacy default stream, which would order itself against the others)
+    comp, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_cmp = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_free = torch.cuda.Event()
     ev_free.record(comp)
-    steps = max(1, min(args.steps, 3))
+    steps = max(3, min(args.steps, 5))
 
     def one():
         with torch.cuda.stream(s_in):
             s_in.wait_event(ev_free)           # the previous step no longer reads the cache
-            for (lo, hi), ev in zip(rng, ev_in):
+            for c in range(n_chunks):
+                lo, hi = c * ppc, (c + 1) * ppc
+                sl = slice(c * lpc, (c + 1) * lpc)
                 b["x"][lo:hi].copy_(host_x[lo:hi], non_blocking=True)
-                ev.record(s_in)
-            for k, v in h_q.items():
-                b[k].copy_(v, non_blocking=True)
-            ev_q.record(s_in)
-        for (lo, hi), ei, ee in zip(rng, ev_in, ev_enc):
-            comp.wait_event(ei)
-            L.lynx_encode_pages(b["x"][lo:hi], p, b["anc"][lo:hi], b["res"][lo:hi], b["meta"][lo:hi])
-            ee.record(comp)
+                b["q1"][sl].copy_(h_q["q1"][sl], non_blocking=True)
+                b["qv"][sl].copy_(h_q["qv"][sl], non_blocking=True)
+                c8[c]["q8"].copy_(h_q8[c], non_blocking=True)
+                ev_in[c].record(s_in)
+        for c in range(n_chunks):
+            lo, hi = c * ppc, (c + 1) * ppc
+            sl = slice(c * lpc, (c + 1) * lpc)
+            comp.wait_event(ev_in[c])
+            cs = torch.cuda.stream(comp)
+            cs.__enter__()
+            L.lynx_encode_pages(b["x"][lo:hi], p, anc[lo:hi], res[lo:hi], meta[lo:hi])
+            L.lynx_reconstruct(anc[lo:hi], None, meta[lo:hi], p, out=b["recon"][lo:hi])
+            L.lynx_reconstruct(anc[lo:hi], res[lo:hi], meta[lo:hi], p, out=b["recon"][lo:hi])
+            L.lynx_decode_attn(b["q1"][sl], kA, None, kM, vA, None, vM, b["pt1"][sl], b["ctx1"][sl], HKV, p,
+                               out=b["o1"][sl], lse=b["l1"][sl], workspace=ws1)
+            L.lynx_decode_attn(c8[c]["q8"], kA, None, kM, vA, None, vM, c8[c]["pt8"], c8[c]["ctx8"], HKV, p,
+                               out=o8[c]["o"], lse=o8[c]["l"], workspace=ws8)
+            L.lynx_decode_attn(b["qv"][sl], kA, kR, kM, vA, vR, vM, b["pt1"][sl], b["ctx1"][sl], HKV, p,
+                               causal=True, out=b["ov"][sl], lse=b["lv"][sl], workspace=wsv)
+            L.lynx_decode_attn_bf16(b["q1"][sl], xk, xv, b["pt1"][sl], b["ctx1"][sl], HKV, out=b["o1"][sl],
+                                    lse=b["l1"][sl], workspace=ws1)
+            cs.__exit__(None, None, None)
+            ev_cmp[c].record(comp)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ee)
-                for k in planes:
+                s_out.wait_event(ev_in[n_chunks - 1])   # after the step's last upload
+                s_out.wait_event(ev_cmp[c])
+                for k in ("anc", "res", "meta"):
                     h_out[k][lo:hi].copy_(b[k][lo:hi], non_blocking=True)
-        comp.wait_event(ev_q)
-        for k in ks[1:]:
-            k[1]()
+                for k in ("o1", "ov", "l1", "lv"):
+                    h_out[k][sl].copy_(b[k][sl], non_blocking=True)
+                for k in ("o", "l"):
+                    h_o8[c][k].copy_(o8[c][k], non_blocking=True)
         ev_free.record(comp)
-        ev_done.record(comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done)
-            for k in small:
-                h_out[k].copy_(b[k], non_blocking=True)
         comp.wait_stream(s_out)                # results are on the host when the step ends
 
     one()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(comp)
-    for _ in range(steps):
+    # each step timed on its own; the host link is shared, so the median step is reported
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    marks[0].record(comp)
+    s_in.wait_event(marks[0])
+    for k in range(steps):
         one()
-    t1.record(comp)
+        marks[k + 1].record(comp)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
+    per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(steps))
+    ms = per_step[len(per_step) // 2]
     head_total = sum(k[3] for k in ks)
     return {"value": round(head_total / (ms * 1e6), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "chunks": n_chunks}
+            "statistic": "median step", "step_ms": [round(x, 3) for x in per_step], "chunks": n_chunks}
 
 
 # ------------------------------------------------------------------ oracle arm
