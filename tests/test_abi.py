@@ -84,3 +84,24 @@ def test_status_strings(lynx_lib):
     for code, name in ((0, b"LYNX_OK"), (-3, b"LYNX_ERR_ALIGNMENT"), (-6, b"LYNX_ERR_DEVICE")):
         assert lynx_lib.lynx_status_string(code) == name
     assert lynx_lib.lynx_version() >= 100
+
+
+def test_row_limit_merge_and_partial_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 4)
+    ok = ctypes.byref(_p())
+    # more than 256 query rows per KV head (T * Hq / Hkv = 32 * 9)
+    assert lib.lynx_decode_attn(a, 1, 32, 72, 8, 128, a, None, a, a, None, a, 4, a, 4, a, ok, 0.088, 0,
+                                a, a, a, 0, None) == -2
+    # merge: negative rows, head_dim, alignment, empty
+    assert lib.lynx_attn_merge(a, a, a, a, -1, 128, a, a, None) == -1
+    assert lib.lynx_attn_merge(a, a, a, a, 4, 64, a, a, None) == -2
+    assert lib.lynx_attn_merge(a, a, odd, a, 4, 128, a, a, None) == -3
+    assert lib.lynx_attn_merge(a, a, a, a, 0, 128, a, a, None) == 0
+    assert lib.lynx_attn_merge(None, a, a, a, 4, 128, a, a, None) == -1
+    # partial encode: the valid counts are required, and must be aligned
+    assert lib.lynx_encode_pages_partial(a, 1, None, ok, a, a, a, None) == -1
+    assert lib.lynx_encode_pages_partial(a, 1, odd, ok, a, a, a, None) == -3
+    assert lib.lynx_encode_pages_partial(a, 0, None, ok, a, a, a, None) == 0

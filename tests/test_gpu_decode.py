@@ -303,3 +303,20 @@ def test_vnmse_of_anchor_and_full_codes(cuda_device, llama_pools):
         assert va_g == pytest.approx(va_r, rel=0.05)
         assert vf_g == pytest.approx(vf_r, rel=0.3)
         assert vf_r * 100 < va_r and vf_g * 100 < va_g
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full"])
+def test_extreme_row_counts_and_alpha(cuda_device, mode):
+    """The largest supported row count per KV head (T = 32, G = 8: 256 rows in 16
+    tensor-core tiles), plain multi-head attention (G = 1) at T = 1 (CUDA-core
+    kernel) and at T = 12 (the smallest row count the tensor-core kernel takes),
+    over pools encoded at alpha = 1e4."""
+    pools = Pools(2, 2048, 9, alpha=1e4)
+    for B, T, Hq, Hkv, causal, ctx in ((1, 32, 16, 2, True, [2048]), (2, 1, 2, 2, False, [1500, 2048]),
+                                       (2, 12, 2, 2, True, [700, 2048])):
+        table = np.stack([contiguous_table(1, Hkv, 8, 8, offset=b)[0] for b in range(B)])
+        ctx = np.array(ctx)
+        q = inputs.queries_np((B, T, Hq, 128), 700 + T)
+        o, lse = run(pools, mode, q, table, ctx, Hkv, causal)
+        ro, rl = reference(pools, mode, q, table, ctx, Hkv, causal)
+        check_attention(o, lse, ro, rl)
