@@ -340,6 +340,7 @@ def run_gpu(args, rank, world):
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dom]["frac_of_hbm"],
             "traffic": profile_traffic(dom), "source": src}
     e2e = run_e2e(torch, L, b, ks, args, dev) if rank == 0 and not args.no_e2e else None
+    prog = run_progressive(torch, L, b, dev) if rank == 0 and not args.no_e2e else None
     if rank != 0:
         return None
     launches = args.steps * sum(k[2] for k in ks)
@@ -356,6 +357,7 @@ def run_gpu(args, rank, world):
         "decode_anchor_GBps_packed": kern.get("decode_anchor_b1", {}).get("GBps_headline"),
         "roofline": roof,
         "e2e": e2e,
+        "progressive": prog,
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -488,6 +490,52 @@ def run_e2e(torch, L, b, ks, args, dev):
     return {"value": round(head_total / (ms * 1e6), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "statistic": "median step", "step_ms": [round(x, 3) for x in per_step], "chunks": n_chunks}
+
+
+def run_progressive(torch, L, b, dev, reps=3):
+    """The paper's split-stream transfer on one box (paper §4.2): the encoded
+    64-layer cache goes device -> pinned host -> device layer by layer, every
+    layer's Anchor plane and metadata first, the Residual planes after them
+    (progressive.ProgressiveTransfer).  Reported: the time until every Anchor
+    (draft decoding can run) and until every Residual (verification can run)
+    has landed, against the same round trip of the BF16 cache; medians of
+    ``reps`` runs (the host link is shared)."""
+    from progressive_kv_quantization_gb300.progressive import ProgressiveTransfer
+    layers = [(2 * l * PER, 2 * (l + 1) * PER) for l in range(N_LAYERS)]
+    src = (b["anc"], b["res"], b["meta"])
+    dst = tuple(torch.empty_like(t) for t in src)
+    tr = ProgressiveTransfer(layers, dev)
+    h_x = torch.empty(b["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+    d_x = torch.empty_like(b["x"])
+    s_o, s_i = torch.cuda.Stream(), torch.cuda.Stream()
+    staged = [torch.cuda.Event() for _ in layers]
+    anchor, full, bf16 = [], [], []
+    for _ in range(reps + 1):
+        torch.cuda.synchronize()
+        tr.send(src, dst)
+        a, f = tr.times_ms()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s_o):                     # the BF16 cache along the same two-stream path
+            e0.record(s_o)
+            for (lo, hi), ev in zip(layers, staged):
+                h_x[lo:hi].copy_(b["x"][lo:hi], non_blocking=True)
+                ev.record(s_o)
+        with torch.cuda.stream(s_i):
+            s_i.wait_event(e0)
+            for (lo, hi), ev in zip(layers, staged):
+                s_i.wait_event(ev)
+                d_x[lo:hi].copy_(h_x[lo:hi], non_blocking=True)
+            e1.record(s_i)
+        e1.synchronize()
+        anchor.append(a)
+        full.append(f)
+        bf16.append(e0.elapsed_time(e1))
+    med = lambda v: round(statistics.median(v[1:]), 3)    # the first run warms the path
+    exact = all(bool(torch.equal(x, y)) for x, y in zip(src, dst)) and bool(torch.equal(d_x, b["x"]))
+    return {"anchor_ready_ms": med(anchor), "full_ready_ms": med(full), "bf16_ms": med(bf16),
+            "anchor_bytes": int(src[0].numel() + src[2].numel() * 4), "residual_bytes": int(src[1].numel()),
+            "bf16_bytes": int(b["x"].numel() * 2), "path": "device -> pinned host -> device, per layer",
+            "bytes_unchanged": exact, "statistic": f"median of {reps}"}
 
 
 # ------------------------------------------------------------------ oracle arm
