@@ -1,7 +1,8 @@
 // Tensor-core verification attention over Lynx-encoded pages: the attention
 // of the Lynx paper (§2.1) run on the KV that the Anchor phase (draft) or the
-// Anchor and Residual phases (verification) of §4.2-4.3 deliver, for 16 of
-// the query rows that share one KV head (T tokens x Hq/Hkv heads) per CTA.
+// Anchor and Residual phases (verification) of §4.2-4.3 deliver, for R = 16
+// or (full codes) R = 32 of the query rows that share one KV head (T tokens x
+// Hq/Hkv heads) per CTA.  A 32-row CTA dequantises each key once for 32 rows.
 //
 // CTA skeleton as in the CUDA-core kernel: a producer lane streams the split's
 // K and V page units through a 3-slot shared-memory ring (2-D TMA tile for the
@@ -12,7 +13,7 @@
 // Each chunk's two contractions run on the tensor cores (mma.sync, float32
 // accumulation); the rows sharing one KV head make both a dense contraction.
 //
-//   K side   S[16 rows x 32 tokens] = Q K^T as TF32 m16n8k8 over 16 k-steps of
+//   K side   S[R rows x 32 tokens] = Q K^T as TF32 m16n8k8 over 16 k-steps of
 //            8 channels.  Q (BF16) is exact in TF32.  k = A + B l~ is
 //            dequantised in float32 (A = gamma_min + (gamma_scale + eps) mu,
 //            B = (gamma_scale + eps)(sigma + eps), the chunk's affine
@@ -21,7 +22,7 @@
 //            n-tiles per chunk: column n of n-tile k holds token 4n + k, so
 //            lane (g, t) needs bytes 2g and 2g+1 of a channel row, both in one
 //            32-bit plane word, and one table lookup per byte feeds two tiles.
-//   V side   U[128 channels x 16 rows] = l~ P^T as fp16 m16n8k16, two k-steps
+//   V side   U[128 channels x R rows] = l~ P^T as fp16 m16n8k16, two k-steps
 //            of 16 tokens, then folded into the output with the chunk's
 //            constants: O = O corr + A psum + B U.  l~ comes from a table of
 //            fp16 head/remainder pairs (two MMAs, ~22 bits); P is fp16, scaled
@@ -34,8 +35,17 @@
 //            and the P fragments are S accumulator entries the lane holds
 //            already.
 //
-// Lane (g = L >> 2, t = L & 3) holds S of rows g and g+8 for tokens 8t + j
-// (j = 4hh + k: entry hh of n-tile k) of its chunk.
+// Lane (g = L >> 2, t = L & 3) holds S of rows 8 rh + g (rh = 0 .. R/8 - 1; K
+// m-tile rh >> 1, accumulator half rh & 1) for tokens 8t + j (j = 4hh + k:
+// entry hh of n-tile k) of its chunk.
+//
+// Output accumulators.  With R = 16 each consumer warp keeps its chunk's
+// O[16 rows x 128 channels] in registers.  With R = 32 they live in tensor
+// memory (TMEM): warp w owns 128 columns of the 32 TMEM lanes of quadrant
+// w mod 4 (columns 128 (w / 4) ..), lane L one row of them; the 16 values of
+// channel tile mt are read (tcgen05.ld), updated and written back
+// (tcgen05.st) per page.  Warp 0 allocates the 256 columns and frees them on
+// every exit path.
 //
 // Rounding: P is rounded to fp16 (relative 2^-11); everything else keeps at
 // least ~21 bits, sums are float32.
@@ -47,10 +57,10 @@
 namespace lynx {
 namespace {
 
-constexpr int kTcRows = 16;
 constexpr int kTcWarpBytes = kH * 8;   // per warp: float2 (A, B) per channel of the current unit
+constexpr int kTmemCols = 256;         // R = 32: 8 warps x 128 columns, 2 warps per lane quadrant
 
-template <bool FULL>
+template <bool FULL, int R>
 struct TLayout {
   using G = QGeo<FULL>;
   static constexpr int kRing = 0;
@@ -61,19 +71,70 @@ struct TLayout {
   static constexpr int kLutK = kRing + G::kStages * G::kUnit;
   static constexpr int kLutV = FULL ? kLutK : kLutK + 256 * 256;
   static constexpr int kWarps = kLutV + 256 * 256;
-  static constexpr int kQ = kWarps + kConsumers * kTcWarpBytes;   // uint4 [16 k-steps][32 lanes]
-  static constexpr int kFlag = kQ + 16 * 32 * 16;
+  static constexpr int kQ = kWarps + kConsumers * kTcWarpBytes;   // uint4 [R/16][16 k-steps][32 lanes]
+  static constexpr int kTmemSlot = kQ + (R / 16) * 16 * 32 * 16;   // u32: TMEM base (R = 32)
+  static constexpr int kFlag = kTmemSlot + 16;
   static constexpr int kBar = kFlag + 16;
   static constexpr int kTotal = kBar + 2 * G::kStages * 8;
   static constexpr int kAlloc = kTotal + 1024;
-  // end-of-kernel merge area (reuses the ring): m[8][16], l[8][16], o[8][16][128]
+  // end-of-kernel merge area (reuses the ring): m[8][R], l[8][R], o[8][16][128]
+  // (the output rows are merged 16 at a time)
   static constexpr int kMergeM = 0;
-  static constexpr int kMergeL = kMergeM + kConsumers * kTcRows * 4;
-  static constexpr int kMergeO = kMergeL + kConsumers * kTcRows * 4;
-  static_assert(kMergeO + kConsumers * kTcRows * kH * 4 <= G::kStages * G::kUnit, "merge area");
+  static constexpr int kMergeL = kMergeM + kConsumers * R * 4;
+  static constexpr int kMergeO = kMergeL + kConsumers * R * 4;
+  static_assert(kMergeO + kConsumers * 16 * kH * 4 <= G::kStages * G::kUnit, "merge area");
 };
-static_assert(TLayout<false>::kAlloc <= 232448, "shared memory (anchor, tensor core)");
-static_assert(TLayout<true>::kAlloc <= 232448, "shared memory (full, tensor core)");
+static_assert(TLayout<false, 16>::kAlloc <= 232448, "shared memory (anchor, tensor core)");
+static_assert(TLayout<true, 16>::kAlloc <= 232448, "shared memory (full, tensor core)");
+static_assert(TLayout<true, 32>::kAlloc <= 232448, "shared memory (full, tensor core, 32 rows)");
+
+// ---- tensor memory (cta_group::1).  Column allocation by one whole warp; the
+// allocated base address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 consecutive 32-bit columns of the lane's TMEM row (shape 32x32b: lane i of
+// the warp reads TMEM lane base + i)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+// the loaded registers are valid only after the wait: they are passed through
+// it so that no use of them is scheduled before it
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -120,15 +181,18 @@ __device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& e
   od = ((wa >> 4) & 0x0F0F0F0Fu) | (wr & 0xF0F0F0F0u);
 }
 
-template <bool FULL>
+template <bool FULL, int R>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 decode_tc_kernel(const DecodeArgs a, const LutTables lut,
                  const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_va,
                  const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr) {
+  static_assert(R == 16 || R == 32, "16 or 32 query rows per CTA");
+  constexpr bool kTmem = (R == 32);
+  constexpr int MT = R / 16;   // K side m-tiles (16 rows each)
+  constexpr int NR = R / 8;    // row octets: V side n-tiles, S accumulator halves
   using G = QGeo<FULL>;
-  using S = TLayout<FULL>;
+  using S = TLayout<FULL, R>;
   constexpr int kSt = G::kStages;
-  constexpr int R = kTcRows;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -163,7 +227,9 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     max_vis = max(max_vis, n_visible(r));
     min_vis = min(min_vis, n_visible(r));
   }
-  const int nv_lo = n_visible(g), nv_hi = n_visible(g + 8);
+  int nv[NR];   // visible keys of the lane's rows 8 rh + g
+#pragma unroll
+  for (int rh = 0; rh < NR; ++rh) nv[rh] = n_visible(8 * rh + g);
   const int n_pages = (max_vis + kP - 1) / kP;
   const int p_begin = split * a.pages_per_split;
   const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
@@ -174,7 +240,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   const uint32_t bar_empty = bar_full + 8 * kSt;
   int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
 
-  // ---- prologue: value tables, Q fragments, barriers
+  // ---- prologue: value tables, Q fragments, barriers, TMEM
   for (int i = tid; i < 256 * 32; i += kThreadsQ) {
     const int e = i >> 5, ln = i & 31;
     if (!FULL) {
@@ -192,10 +258,10 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
     }
   }
-  // entry (ks, lane, e): row g' + 8 (e & 1), channel 8 ks + t' + 4 (e >> 1); BF16 is exact in TF32
-  for (int i = tid; i < 16 * 32 * 4; i += kThreadsQ) {
-    const int e = i & 3, ln = (i >> 2) & 31, ks = i >> 7;
-    const int row = row0 + (ln >> 2) + 8 * (e & 1);
+  // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channel 8 ks + t' + 4 (e >> 1); BF16 is exact in TF32
+  for (int i = tid; i < MT * 16 * 32 * 4; i += kThreadsQ) {
+    const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 15, mi = i >> 11;
+    const int row = row0 + 16 * mi + (ln >> 2) + 8 * (e & 1);
     const int d = 8 * ks + (ln & 3) + 4 * (e >> 1);
     uint32_t v = 0u;
     if (row < TG)
@@ -210,13 +276,28 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     *s_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (kTmem && warp == 0) {
+    tmem_alloc(base + S::kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (kTmem) tmem_fence_before_sync();
   __syncthreads();
+  if (kTmem) tmem_fence_after_sync();
+  uint32_t tmem = 0u;
+  if (kTmem) tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kTmemSlot);
+  // this warp's 128 columns of its lane quadrant
+  const uint32_t t_warp = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128u * (uint32_t)(warp >> 2);
 
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-  float l_run[2] = {0.0f, 0.0f};
-  float2 O[8][2][2];   // O[mt][nt][c]: channel 16 mt + g + 8c, rows 8 nt + 2t and 8 nt + 2t + 1
+  float m_run[NR], l_run[NR];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+  for (int rh = 0; rh < NR; ++rh) {
+    m_run[rh] = -CUDART_INF_F;
+    l_run[rh] = 0.0f;
+  }
+  // R = 16: O[mt][nt][c] = channel 16 mt + g + 8c, rows 8 nt + 2t and 8 nt + 2t + 1
+  float2 O[kTmem ? 1 : 8][2][2];
+#pragma unroll
+  for (int mt = 0; mt < (kTmem ? 1 : 8); ++mt)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) O[mt][nt][0] = O[mt][nt][1] = make_float2(0.f, 0.f);
 
@@ -237,6 +318,14 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     const float eps = a.eps;
     const float sc = a.scale_log2;
     bool failed = false;
+
+    if (kTmem) {   // O = 0 (TMEM contents are undefined after allocation)
+      uint32_t z[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) z[k] = 0u;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) tmem_st16(t_warp + 16u * mt, z);
+    }
 
     auto prep_ab = [&](uint32_t unit) {
       const uint32_t mt = unit + G::kMetaOff;
@@ -265,14 +354,18 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       __syncwarp();
 
       // ---- S = Q K^T over 16 k-steps of channels (t, t + 4) + 8 ks; n-tile k, column n: token 4n + k
-      float sacc[4][4];
+      float sacc[MT][4][4];
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
+      for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[n][e] = 0.0f;
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mi][n][e] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
-        const uint4 qf = lds<uint4>(smem, S::kQ + (ks * 32 + L) * 16);
+        uint4 qf[MT];
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) qf[mi] = lds<uint4>(smem, S::kQ + ((mi * 16 + ks) * 32 + L) * 16);
         const int c0 = 8 * ks + t, c1 = c0 + 4;
         const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
         const float2 ab1 = lds<float2>(smem, s_ab + 8 * c1);
@@ -307,27 +400,31 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         const float x1[4] = {k10.x, k10.y, k11.x, k11.y};
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          mma_tf32(sacc[n], qf.x, qf.y, qf.z, qf.w, tf32_hi(x0[n]), tf32_hi(x1[n]));
-          mma_tf32(sacc[n], qf.x, qf.y, qf.z, qf.w, tf32_lo(x0[n]), tf32_lo(x1[n]));
+          const uint32_t h0 = tf32_hi(x0[n]), h1 = tf32_hi(x1[n]);
+          const uint32_t lo0 = tf32_lo(x0[n]), lo1 = tf32_lo(x1[n]);
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi) {
+            mma_tf32(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, h0, h1);
+            mma_tf32(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, lo0, lo1);
+          }
         }
       }
       __syncwarp();
       if (L == 0) mbar_arrive(bar_empty + 8 * sK);
 
-      // ---- online softmax: row g (rh 0, S entries 0-1) and g + 8 (rh 1, entries 2-3);
-      // token 8t + j, j = 4 hh + k, is entry 2 rh + hh of n-tile k
+      // ---- online softmax: row 8 rh + g is accumulator half rh & 1 (S entries
+      // 2 (rh & 1) + hh) of m-tile rh >> 1; token 8t + j, j = 4 hh + k, sits in n-tile k
       const int pos0 = p * kP + 32 * w + 8 * t;
       const bool all_visible = (p + 1) * kP <= min_vis;
-      float pr[2][8];   // [rh][j], probabilities x 2^10
-      float corr[2], psum[2];
+      float pr[NR][8];   // [rh][j], probabilities x 2^10
+      float corr[NR], psum[NR];
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        const int nv = rh ? nv_hi : nv_lo;
+      for (int rh = 0; rh < NR; ++rh) {
         float mloc = -CUDART_INF_F;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float sv = sacc[j & 3][2 * rh + (j >> 2)] * sc;
-          if (!all_visible && pos0 + j >= nv) sv = -CUDART_INF_F;
+          float sv = sacc[rh >> 1][j & 3][2 * (rh & 1) + (j >> 2)] * sc;
+          if (!all_visible && pos0 + j >= nv[rh]) sv = -CUDART_INF_F;
           pr[rh][j] = sv;
           mloc = fmaxf(mloc, sv);
         }
@@ -350,32 +447,38 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         m_run[rh] = mnew;
       }
       // P^T fragments of k-step kv, n-tile nt (rows 8 nt + g): tokens 8t + 4kv + {0,1} and + {2,3}
-      uint32_t pb[2][2][2];
+      uint32_t pb[2][NR][2];
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NR; ++nt) {
           pb[kv][nt][0] = h2(pr[nt][4 * kv], pr[nt][4 * kv + 1]);
           pb[kv][nt][1] = h2(pr[nt][4 * kv + 2], pr[nt][4 * kv + 3]);
         }
       // statistics of U's columns: rows 8 nt + 2t + e live in lane 8t + 4e
-      float2 cr[2], pss[2];
+      float2 cr[NR], pss[NR];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NR; ++nt) {
         cr[nt] = make_float2(__shfl_sync(0xffffffffu, corr[nt], 8 * t),
                              __shfl_sync(0xffffffffu, corr[nt], 8 * t + 4));
         pss[nt] = make_float2(__shfl_sync(0xffffffffu, psum[nt], 8 * t),
                               __shfl_sync(0xffffffffu, psum[nt], 8 * t + 4));
       }
-      const bool rescale = __any_sync(0xffffffffu, corr[0] != 1.0f || corr[1] != 1.0f);
+      bool any_corr = false;
+#pragma unroll
+      for (int rh = 0; rh < NR; ++rh) any_corr |= corr[rh] != 1.0f;
+      const bool rescale = __any_sync(0xffffffffu, any_corr);
 
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1));
       if (failed) break;
       prep_ab(unitV);
       __syncwarp();
+      if (kTmem) tmem_wait_st();   // the previous page's O stores have landed
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
+        uint32_t ov[16];   // R = 32: O of channel tile mt, [nt][c][row parity]
+        if (kTmem) tmem_ld16(t_warp + 16u * mt, ov);
         const int c0 = 16 * mt + g;
         const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
         const float2 ab1 = lds<float2>(smem, s_ab + 8 * (c0 + 8));
@@ -395,9 +498,9 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
           const uint32_t ho = lds<uint32_t>(smem, S::kLutV + lut_off(c ? o1 : o0, lane4v, sel));
           return make_uint2(prmt(he, ho, 0x5410u), prmt(he, ho, 0x7632u));
         };
-        float u[2][4];
+        float u[NR][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[nt][e] = 0.0f;
 #pragma unroll
@@ -405,101 +508,164 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
           const uint2 x00 = vpair(0, 2 * kv), x10 = vpair(1, 2 * kv);
           const uint2 x01 = vpair(0, 2 * kv + 1), x11 = vpair(1, 2 * kv + 1);
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < NR; ++nt) {
             mma_f16(u[nt], x00.x, x10.x, x01.x, x11.x, pb[kv][nt][0], pb[kv][nt][1]);
             mma_f16(u[nt], x00.y, x10.y, x01.y, x11.y, pb[kv][nt][0], pb[kv][nt][1]);
           }
         }
+        if (kTmem) tmem_wait_ld(ov);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float2 o0 = O[mt][nt][0], o1 = O[mt][nt][1];
-          if (rescale) {
-            o0 = __fmul2_rn(o0, cr[nt]);
-            o1 = __fmul2_rn(o1, cr[nt]);
+        for (int nt = 0; nt < NR; ++nt) {
+          float2 p0, p1;
+          if (kTmem) {
+            p0 = make_float2(__uint_as_float(ov[4 * nt]), __uint_as_float(ov[4 * nt + 1]));
+            p1 = make_float2(__uint_as_float(ov[4 * nt + 2]), __uint_as_float(ov[4 * nt + 3]));
+          } else {
+            p0 = O[kTmem ? 0 : mt][nt & 1][0];
+            p1 = O[kTmem ? 0 : mt][nt & 1][1];
           }
-          o0 = __ffma2_rn(make_float2(ab0.x, ab0.x), pss[nt], o0);
-          o1 = __ffma2_rn(make_float2(ab1.x, ab1.x), pss[nt], o1);
-          O[mt][nt][0] = __ffma2_rn(make_float2(ab0.y, ab0.y), make_float2(u[nt][0], u[nt][1]), o0);
-          O[mt][nt][1] = __ffma2_rn(make_float2(ab1.y, ab1.y), make_float2(u[nt][2], u[nt][3]), o1);
+          if (rescale) {
+            p0 = __fmul2_rn(p0, cr[nt]);
+            p1 = __fmul2_rn(p1, cr[nt]);
+          }
+          p0 = __ffma2_rn(make_float2(ab0.x, ab0.x), pss[nt], p0);
+          p1 = __ffma2_rn(make_float2(ab1.x, ab1.x), pss[nt], p1);
+          p0 = __ffma2_rn(make_float2(ab0.y, ab0.y), make_float2(u[nt][0], u[nt][1]), p0);
+          p1 = __ffma2_rn(make_float2(ab1.y, ab1.y), make_float2(u[nt][2], u[nt][3]), p1);
+          if (kTmem) {
+            ov[4 * nt] = __float_as_uint(p0.x);
+            ov[4 * nt + 1] = __float_as_uint(p0.y);
+            ov[4 * nt + 2] = __float_as_uint(p1.x);
+            ov[4 * nt + 3] = __float_as_uint(p1.y);
+          } else {
+            O[kTmem ? 0 : mt][nt & 1][0] = p0;
+            O[kTmem ? 0 : mt][nt & 1][1] = p1;
+          }
         }
+        if (kTmem) tmem_st16(t_warp + 16u * mt, ov);
       }
       __syncwarp();
       if (L == 0) mbar_arrive(bar_empty + 8 * sV);
     }
+    if (kTmem) tmem_wait_st();
     if (failed && L == 0) {
       atomicExch(a.status, 1);
       *s_flag = 1;
     }
   }
 
-  // ================= merge the 8 chunk states (the ring is idle now)
+  // ================= merge the 8 chunk states (the ring is idle now), 16 rows at a time
+  if (kTmem) tmem_fence_before_sync();
   __syncthreads();
-  if (*reinterpret_cast<volatile int*>(s_flag) != 0) return;
+  if (kTmem) tmem_fence_after_sync();
+  const bool ok = *reinterpret_cast<volatile int*>(s_flag) == 0;
   float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
   float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
-  if (warp < kConsumers) {
+  if (ok && warp < kConsumers) {
 #pragma unroll
-    for (int rh = 0; rh < 2; ++rh) {
+    for (int rh = 0; rh < NR; ++rh) {
       float lw = l_run[rh];
       lw += __shfl_xor_sync(0xffffffffu, lw, 1);
       lw += __shfl_xor_sync(0xffffffffu, lw, 2);
       if (t == 0) {
-        mm[warp * R + g + 8 * rh] = m_run[rh];
-        ml[warp * R + g + 8 * rh] = lw;
+        mm[warp * R + 8 * rh + g] = m_run[rh];
+        ml[warp * R + 8 * rh + g] = lw;
       }
     }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int r = warp * R + 8 * nt + 2 * t;
-        const int c0 = 16 * mt + g;
-        mo[r * kH + c0] = O[mt][nt][0].x;
-        mo[(r + 1) * kH + c0] = O[mt][nt][0].y;
-        mo[r * kH + c0 + 8] = O[mt][nt][1].x;
-        mo[(r + 1) * kH + c0 + 8] = O[mt][nt][1].y;
-      }
   }
-  __syncthreads();
-  for (int i = tid; i < R * kH; i += kThreadsQ) {
-    const int r = i >> 7, d = i & 127;
-    const int row = row0 + r;
-    const int rg4 = row >> 2;
-    if (rg4 >= a.n_rg) continue;
-    float mstar = -CUDART_INF_F;
 #pragma unroll
-    for (int ww = 0; ww < kConsumers; ++ww) mstar = fmaxf(mstar, mm[ww * R + r]);
-    float o = 0.0f, l = 0.0f;
-    if (mstar != -CUDART_INF_F) {
+  for (int hf = 0; hf < MT; ++hf) {
+    if (!ok) break;
+    // the 16 rows 16 hf .. 16 hf + 15: n-tiles 2 hf and 2 hf + 1
+    if (warp < kConsumers) {
 #pragma unroll
-      for (int ww = 0; ww < kConsumers; ++ww) {
-        const float mw = mm[ww * R + r];
-        if (mw == -CUDART_INF_F) continue;
-        const float f = exp2f(mw - mstar);
-        o += mo[(ww * R + r) * kH + d] * f;
-        l += ml[ww * R + r] * f;
+      for (int mt = 0; mt < 8; ++mt) {
+        float2 q[2][2];
+        if (kTmem) {
+          uint32_t ov[16];
+          tmem_ld16(t_warp + 16u * mt, ov);
+          tmem_wait_ld(ov);
+#pragma unroll
+          for (int n2 = 0; n2 < 2; ++n2) {
+            const int nt = 2 * hf + n2;
+            q[n2][0] = make_float2(__uint_as_float(ov[4 * nt]), __uint_as_float(ov[4 * nt + 1]));
+            q[n2][1] = make_float2(__uint_as_float(ov[4 * nt + 2]), __uint_as_float(ov[4 * nt + 3]));
+          }
+        } else {
+#pragma unroll
+          for (int n2 = 0; n2 < 2; ++n2) {
+            q[n2][0] = O[kTmem ? 0 : mt][n2][0];
+            q[n2][1] = O[kTmem ? 0 : mt][n2][1];
+          }
+        }
+#pragma unroll
+        for (int n2 = 0; n2 < 2; ++n2) {
+          const int r = warp * 16 + 8 * n2 + 2 * t;
+          const int c0 = 16 * mt + g;
+          mo[r * kH + c0] = q[n2][0].x;
+          mo[(r + 1) * kH + c0] = q[n2][0].y;
+          mo[r * kH + c0 + 8] = q[n2][1].x;
+          mo[(r + 1) * kH + c0 + 8] = q[n2][1].y;
+        }
       }
     }
-    // the 2^10 scale of the probabilities cancels in o / l; remove it from both
-    const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
-    float* ws = a.ws + cta * kWsPerCta;
-    ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
-    if (d == 0) {
-      ws[kRows * kH + (row & 3)] = mstar;
-      ws[kRows * kH + kRows + (row & 3)] = l * (1.0f / 1024.0f);
+    __syncthreads();
+    for (int i = tid; i < 16 * kH; i += kThreadsQ) {
+      const int rr = i >> 7, d = i & 127;
+      const int r = 16 * hf + rr;
+      const int row = row0 + r;
+      const int rg4 = row >> 2;
+      if (rg4 >= a.n_rg) continue;
+      float mstar = -CUDART_INF_F;
+#pragma unroll
+      for (int ww = 0; ww < kConsumers; ++ww) mstar = fmaxf(mstar, mm[ww * R + r]);
+      float o = 0.0f, l = 0.0f;
+      if (mstar != -CUDART_INF_F) {
+#pragma unroll
+        for (int ww = 0; ww < kConsumers; ++ww) {
+          const float mw = mm[ww * R + r];
+          if (mw == -CUDART_INF_F) continue;
+          const float f = exp2f(mw - mstar);
+          o += mo[(ww * 16 + rr) * kH + d] * f;
+          l += ml[ww * R + r] * f;
+        }
+      }
+      // the 2^10 scale of the probabilities cancels in o / l; remove it from both
+      const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
+      float* ws = a.ws + cta * kWsPerCta;
+      ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
+      if (d == 0) {
+        ws[kRows * kH + (row & 3)] = mstar;
+        ws[kRows * kH + kRows + (row & 3)] = l * (1.0f / 1024.0f);
+      }
+    }
+    __syncthreads();
+  }
+  // every TMEM access of every warp has completed (each waited for its own
+  // loads and stores) before the columns are freed
+  if (kTmem) {
+    tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+      tmem_fence_after_sync();
+      tmem_dealloc(tmem, kTmemCols);
     }
   }
 }
 
-template <bool FULL>
+// rows per CTA: 32 for the full codes when more than 16 rows share a KV head
+// (each key is dequantised once for 32 rows), else 16
+constexpr bool tc_wide(int rows, bool full) { return full && rows > 16; }
+
+template <bool FULL, int R>
 cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
-  constexpr int kSmem = TLayout<FULL>::kAlloc;
+  constexpr int kSmem = TLayout<FULL, R>::kAlloc;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FULL>,
+    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FULL, R>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -515,18 +681,19 @@ cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s)
     tkr = tka;
     tvr = tva;
   }
-  dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + kTcRows - 1) / kTcRows), a.B);
-  decode_tc_kernel<FULL><<<grid, kThreadsQ, kSmem, s>>>(a, *lut, tka, tva, tkr, tvr);
+  dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + R - 1) / R), a.B);
+  decode_tc_kernel<FULL, R><<<grid, kThreadsQ, kSmem, s>>>(a, *lut, tka, tva, tkr, tvr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool use_tc_rows(int rows) { return rows >= 12; }
-int tc_rows_per_cta(int) { return kTcRows; }
+int tc_rows_per_cta(int rows, bool full) { return tc_wide(rows, full) ? 32 : 16; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
-  return full ? launch_tc<true>(a, lut, s) : launch_tc<false>(a, lut, s);
+  if (!full) return launch_tc<false, 16>(a, lut, s);
+  return tc_wide(a.T * a.G, true) ? launch_tc<true, 32>(a, lut, s) : launch_tc<true, 16>(a, lut, s);
 }
 
 }  // namespace lynx

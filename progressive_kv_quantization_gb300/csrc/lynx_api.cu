@@ -316,9 +316,14 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
 
 size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages) {
   if (check_decode_shape(B, T, Hq, Hkv, head_dim, max_pages) != LYNX_OK) return 0;
-  const size_t q = plan_decode(B, T, Hq, Hkv, max_pages, kModeAnchor).ws_bytes;
-  const size_t f = plan_decode(B, T, Hq, Hkv, max_pages, kModeBf16).ws_bytes;
-  return q > f ? q : f;
+  // the split count depends on the kind of pages (rows per CTA differ), so the
+  // size covers all three
+  size_t ws = 0;
+  for (int mode : {kModeAnchor, kModeFull, kModeBf16}) {
+    const size_t m = plan_decode(B, T, Hq, Hkv, max_pages, mode).ws_bytes;
+    ws = m > ws ? m : ws;
+  }
+  return ws;
 }
 
 int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
