@@ -724,10 +724,10 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
   const int G = Hq / Hkv;
   pl.n_rg = (T * G + kRows - 1) / kRows;
   const int64_t units = (int64_t)B * Hkv * pl.n_rg;
-  // CTAs per split: the tensor-core kernel takes 16 or 32 query rows per CTA
-  const bool tc = mode != kModeBf16 && use_tc_rows(T * G);
-  const int tc_rows = tc ? tc_rows_per_cta(T * G, mode == kModeFull) : kRows;
-  const int64_t cta_units = tc ? (int64_t)B * Hkv * ((T * G + tc_rows - 1) / tc_rows) : units;
+  // CTAs per split: the quantised kernels take 8, 16 or 32 query rows per CTA
+  const bool quant = mode != kModeBf16;
+  const int q_rows = !quant ? kRows : use_tc_rows(T * G) ? tc_rows_per_cta(T * G, mode == kModeFull) : kNarrowRows;
+  const int64_t cta_units = quant ? (int64_t)B * Hkv * ((T * G + q_rows - 1) / q_rows) : units;
   const int64_t resident = device_sm_count();   // one CTA per SM (shared-memory bound)
   int best_s = 1;
   double best = 1e300;

@@ -1,12 +1,13 @@
-// Shared pieces of the two quantised-KV decode kernels (CUDA-core and
-// tensor-core): the page-unit geometry of the shared-memory ring, PTX helpers
-// for mbarriers, TMA and bulk copies, and the producer lane that streams a
+// Shared pieces of the quantised-KV decode kernels: the page-unit geometry of
+// the shared-memory ring, PTX helpers for mbarriers, TMA, bulk copies and
+// mma.sync, the value-table addressing, and the producer lane that streams a
 // split's K and V units through the ring.
 #pragma once
 
 #include "lynx_internal.cuh"
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 namespace lynx {
@@ -29,9 +30,6 @@ struct QGeo {
   static constexpr int kUnit = FULL ? 2 * kPlaneBytes + kMetaBytes : kPlaneBytes + kMetaBytes;
   static constexpr int kResOff = kPlaneBytes;
   static constexpr int kMetaOff = FULL ? 2 * kPlaneBytes : kPlaneBytes;
-  // anchor: byte -> (value of low nibble, value of high nibble), 32 copies (entry stride 256 B)
-  // full:   8-bit code -> value, 32 copies (entry stride 128 B)
-  static constexpr int kLutBytes = FULL ? 256 * 32 * 4 : 256 * 32 * 8;
 };
 static_assert(QGeo<false>::kUnit % 1024 == 0 && QGeo<true>::kUnit % 1024 == 0,
               "ring slots must keep the 1024-byte alignment of swizzled tiles");
@@ -109,6 +107,53 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T>
 __device__ __forceinline__ T lds(const uint8_t* smem, uint32_t off) {
   return *reinterpret_cast<const T*>(smem + off);
+}
+
+// ---------------------------------------------------------------- tensor-core helpers
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// TF32 head (low 13 mantissa bits cleared) and the exact float32 remainder
+__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+__device__ __forceinline__ uint32_t tf32_lo(float x) {
+  return __float_as_uint(x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u));
+}
+
+// fp16 pair, `lo` in the low half (the lower k index of a fragment register)
+__device__ __forceinline__ uint32_t h2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t h2(__half lo, __half hi) {
+  const __half2 v = __halves2half2(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// table offset for byte j of `word`: the byte in bits 8..15, the lane's copy
+// offset (< 256) in bits 0..7
+__device__ __forceinline__ uint32_t byte_sel(uint32_t j) { return 0x5504u | (j << 4); }
+__device__ __forceinline__ uint32_t lut_off(uint32_t word, uint32_t lane_off, uint32_t sel) {
+  return prmt(word, lane_off, sel);
+}
+
+// full codes (anchor nibble | residual nibble << 4) of the even and of the odd
+// tokens of the four bytes of an anchor word and its residual word
+__device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& ev, uint32_t& od) {
+  ev = (wa & 0x0F0F0F0Fu) | ((wr << 4) & 0xF0F0F0F0u);
+  od = ((wa >> 4) & 0x0F0F0F0Fu) | (wr & 0xF0F0F0F0u);
 }
 
 // Producer lane of a decode CTA: streams the K and V units of pages

@@ -4,7 +4,7 @@
 // or (full codes) R = 32 of the query rows that share one KV head (T tokens x
 // Hq/Hkv heads) per CTA.  A 32-row CTA dequantises each key once for 32 rows.
 //
-// CTA skeleton as in the CUDA-core kernel: a producer lane streams the split's
+// CTA skeleton as in the narrow kernel: a producer lane streams the split's
 // K and V page units through a 3-slot shared-memory ring (2-D TMA tile for the
 // planes, bulk copy for the metadata); 8 consumer warps, warp w owning the
 // 32-token chunk w of every page with its own online softmax; one merge of the
@@ -51,8 +51,6 @@
 // least ~21 bits, sums are float32.
 
 #include "decode_common.cuh"
-
-#include <cuda_fp16.h>
 
 namespace lynx {
 namespace {
@@ -135,51 +133,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// TF32 head (low 13 mantissa bits cleared) and the exact float32 remainder
-__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
-__device__ __forceinline__ uint32_t tf32_lo(float x) {
-  return __float_as_uint(x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u));
-}
-
-// fp16 pair, `lo` in the low half (the lower k index of a fragment register)
-__device__ __forceinline__ uint32_t h2(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-__device__ __forceinline__ uint32_t h2(__half lo, __half hi) {
-  const __half2 v = __halves2half2(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// table offset for byte j of `word`: the byte in bits 8..15, the lane's copy
-// offset (< 256) in bits 0..7
-__device__ __forceinline__ uint32_t byte_sel(uint32_t j) { return 0x5504u | (j << 4); }
-__device__ __forceinline__ uint32_t lut_off(uint32_t word, uint32_t lane_off, uint32_t sel) {
-  return prmt(word, lane_off, sel);
-}
-
-// full codes (anchor nibble | residual nibble << 4) of the even and of the odd
-// tokens of the four bytes of an anchor word and its residual word
-__device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& ev, uint32_t& od) {
-  ev = (wa & 0x0F0F0F0Fu) | ((wr << 4) & 0xF0F0F0F0u);
-  od = ((wa >> 4) & 0x0F0F0F0Fu) | (wr & 0xF0F0F0F0u);
-}
 
 template <bool FULL, int R>
 __global__ void __launch_bounds__(kThreadsQ, 1)

@@ -96,9 +96,12 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode);
 bool n_pool_too_large(int64_t n_pool);
 // tensor-core decode kernel: used for `rows` = T * (Hq / Hkv) query rows per
 // (sequence, KV head) when use_tc_rows(rows); one CTA takes
-// tc_rows_per_cta(rows, full) of them
+// tc_rows_per_cta(rows, full) of them.  Fewer rows go to the narrow tensor-core
+// kernel, kNarrowRows per CTA.
 bool use_tc_rows(int rows);
 int tc_rows_per_cta(int rows, bool full);
+constexpr int kNarrowRows = 8;
+cudaError_t launch_decode_narrow(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);

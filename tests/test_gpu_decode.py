@@ -328,11 +328,13 @@ def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, T):
 def test_extreme_row_counts_and_alpha(cuda_device, mode):
     """The largest supported row count per KV head (T = 32, G = 8: 256 rows in 16
     16-row tensor-core tiles for the anchor codes, 8 32-row tiles for the full
-    codes), plain multi-head attention (G = 1) at T = 1 (CUDA-core
-    kernel) and at T = 12 (the smallest row count the tensor-core kernel takes),
-    over pools encoded at alpha = 1e4."""
+    codes), plain multi-head attention (G = 1) at T = 1 and eight query heads
+    per KV head at T = 1 (one row, and all 8 rows, of a narrow-kernel tile) and
+    at T = 12 (the smallest row count the wide tensor-core kernel takes), over
+    pools encoded at alpha = 1e4."""
     pools = Pools(2, 2048, 9, alpha=1e4)
     for B, T, Hq, Hkv, causal, ctx in ((1, 32, 16, 2, True, [2048]), (2, 1, 2, 2, False, [1500, 2048]),
+                                       (2, 1, 16, 2, False, [2048, 1100]),
                                        (2, 12, 2, 2, True, [700, 2048])):
         table = np.stack([contiguous_table(1, Hkv, 8, 8, offset=b)[0] for b in range(B)])
         ctx = np.array(ctx)
