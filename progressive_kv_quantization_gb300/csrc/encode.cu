@@ -59,6 +59,13 @@ __device__ __forceinline__ float div1(float x, float d, float r) {
   return __fmaf_rn(e, r, q);
 }
 
+// max(a, b, c) in one instruction (three-input max of sm_100 and later)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -110,7 +117,7 @@ __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8
     d[u] = __ffma2_rn(qc.c2, lg, nry);                           // c lg - round(c lg)
     ib[2 * u] = __float_as_uint(r.x);
     ib[2 * u + 1] = __float_as_uint(r.y);
-    dmax = fmaxf(dmax, fmaxf(fabsf(d[u].x), fabsf(d[u].y)));
+    dmax = max3(dmax, fabsf(d[u].x), fabsf(d[u].y));
   }
   if (dmax > qc.edge) {
 #pragma unroll
