@@ -13,15 +13,21 @@
 // Each chunk's two contractions run on the tensor cores (mma.sync, float32
 // accumulation); the rows sharing one KV head make both a dense contraction.
 //
-//   K side   S[R rows x 32 tokens] = Q K^T as TF32 m16n8k8 over 16 k-steps of
-//            8 channels.  Q (BF16) is exact in TF32.  k = A + B l~ is
-//            dequantised in float32 (A = gamma_min + (gamma_scale + eps) mu,
+//   K side   S[R rows x 32 tokens] = Q K^T as fp16 m16n8k16 over 8 k-steps of
+//            16 channels.  k = A + B l~ is dequantised in float32
+//            (A = gamma_min + (gamma_scale + eps) mu,
 //            B = (gamma_scale + eps)(sigma + eps), the chunk's affine
-//            constants) and split into its TF32 head and the float32
-//            remainder, two MMAs, so each product keeps ~21 bits.  Four
+//            constants) and split into an fp16 head (the float truncated to 11
+//            significant bits) and the fp16-rounded remainder, two MMAs, so each
+//            product keeps ~22 bits.  Q (BF16) is exact in fp16.  Both operands
+//            are scaled by powers of two to fill fp16's range -- Q by the CTA
+//            (largest |q| in [2^14, 2^15)), A and B by the chunk (largest
+//            |A| + |B| in [2^14, 2^15)) -- and the scale returns, exactly, in
+//            the softmax scale.  Four
 //            n-tiles per chunk: column n of n-tile k holds token 4n + k, so
 //            lane (g, t) needs bytes 2g and 2g+1 of a channel row, both in one
-//            32-bit plane word, and one table lookup per byte feeds two tiles.
+//            32-bit plane word; its k-slots 2t, 2t+1 and 2t+8, 2t+9 are
+//            channels 16 ks + 2t, + 1, + 8, + 9.
 //   V side   U[128 channels x R rows] = l~ P^T as fp16 m16n8k16, two k-steps
 //            of 16 tokens, then folded into the output with the chunk's
 //            constants: O = O corr + A psum + B U.  l~ comes from a table of
@@ -69,8 +75,9 @@ struct TLayout {
   static constexpr int kLutK = kRing + G::kStages * G::kUnit;
   static constexpr int kLutV = FULL ? kLutK : kLutK + 256 * 256;
   static constexpr int kWarps = kLutV + 256 * 256;
-  static constexpr int kQ = kWarps + kConsumers * kTcWarpBytes;   // uint4 [R/16][16 k-steps][32 lanes]
-  static constexpr int kTmemSlot = kQ + (R / 16) * 16 * 32 * 16;   // u32: TMEM base (R = 32)
+  static constexpr int kQ = kWarps + kConsumers * kTcWarpBytes;   // uint4 [R/16][8 k-steps][32 lanes]
+  static constexpr int kTmemSlot = kQ + (R / 16) * 8 * 32 * 16;    // u32: TMEM base (R = 32)
+  static constexpr int kQmax = kTmemSlot + 4;                       // u32: largest |q| (BF16 bits)
   static constexpr int kFlag = kTmemSlot + 16;
   static constexpr int kBar = kFlag + 16;
   static constexpr int kTotal = kBar + 2 * G::kStages * 8;
@@ -211,14 +218,35 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
     }
   }
-  // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channel 8 ks + t' + 4 (e >> 1); BF16 is exact in TF32
-  for (int i = tid; i < MT * 16 * 32 * 4; i += kThreadsQ) {
-    const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 15, mi = i >> 11;
+  // Q fragments in fp16, scaled by 2^-eq so that the largest |q| of the CTA's rows
+  // lies in [2^14, 2^15) (the other values keep their 8 significant bits unless
+  // they are 2^-28 times smaller than it)
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
+  if (tid == 0) *s_qmax = 0u;
+  __syncthreads();
+  {
+    uint32_t qm = 0u;
+    for (int i = tid; i < R * kH; i += kThreadsQ) {
+      const int row = row0 + (i >> 7);
+      if (row < TG)
+        qm = max(qm, (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + (i & 127)] &
+                         0x7FFFu);
+    }
+    atomicMax(s_qmax, qm);
+  }
+  __syncthreads();
+  const int eq = min(max((int)((*s_qmax >> 7) & 0xFFu) - 127 - 14, -100), 113);
+  const float qscale = __uint_as_float((uint32_t)(127 - eq) << 23);   // 2^-eq
+  // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channels 16 ks + 2t' + 8 (e >> 1) + {0, 1}
+  for (int i = tid; i < MT * 8 * 32 * 4; i += kThreadsQ) {
+    const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 7, mi = i >> 10;
     const int row = row0 + 16 * mi + (ln >> 2) + 8 * (e & 1);
-    const int d = 8 * ks + (ln & 3) + 4 * (e >> 1);
+    const int d = 16 * ks + 2 * (ln & 3) + 8 * (e >> 1);
     uint32_t v = 0u;
-    if (row < TG)
-      v = (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + d] << 16;
+    if (row < TG) {
+      const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+      v = h2(__uint_as_float((uint32_t)qr[d] << 16) * qscale, __uint_as_float((uint32_t)qr[d + 1] << 16) * qscale);
+    }
     reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
   }
   if (tid == 0) {
@@ -280,8 +308,12 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       for (int mt = 0; mt < 8; ++mt) tmem_st16(t_warp + 16u * mt, z);
     }
 
-    auto prep_ab = [&](uint32_t unit) {
+    // (A, B) of the unit's 128 channels; for a key unit scaled by 2^-ek so that
+    // the largest |A| + |B| (a bound on |k|) lies in [2^14, 2^15), ek returned
+    auto prep_ab = [&](uint32_t unit, bool key) -> int {
       const uint32_t mt = unit + G::kMetaOff;
+      float2 ab[4];
+      float mx = 0.0f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int d = L + 32 * k;
@@ -289,9 +321,19 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
         const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
         const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
-        *reinterpret_cast<float2*>(smem + s_ab + 8 * d) =
-            make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+        ab[k] = make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+        mx = fmaxf(mx, fabsf(ab[k].x) + fabsf(ab[k].y));
       }
+      int ek = 0;
+      if (key) {
+        mx = warp_max(mx);
+        ek = min(max((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 14, -100), 100);
+      }
+      const float f = __uint_as_float((uint32_t)(127 - ek) << 23);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float2*>(smem + s_ab + 8 * (L + 32 * k)) = make_float2(ab[k].x * f, ab[k].y * f);
+      return ek;
     };
 
     for (int i = 0; i < np && !failed; ++i) {
@@ -303,10 +345,12 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1));
       if (failed) break;
-      prep_ab(unitK);
+      const int ek = prep_ab(unitK, true);
       __syncwarp();
+      // softmax scale of this chunk's logits: the operands' power-of-two scales return here
+      const float sck = sc * __uint_as_float((uint32_t)min(max(127 + ek + eq, 1), 254) << 23);
 
-      // ---- S = Q K^T over 16 k-steps of channels (t, t + 4) + 8 ks; n-tile k, column n: token 4n + k
+      // ---- S = Q K^T over 8 k-steps of channels 16 ks + 2t + {0, 1, 8, 9}; n-tile k, column n: token 4n + k
       float sacc[MT][4][4];
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi)
@@ -315,50 +359,57 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[mi][n][e] = 0.0f;
 #pragma unroll
-      for (int ks = 0; ks < 16; ++ks) {
+      for (int ks = 0; ks < 8; ++ks) {
         uint4 qf[MT];
 #pragma unroll
-        for (int mi = 0; mi < MT; ++mi) qf[mi] = lds<uint4>(smem, S::kQ + ((mi * 16 + ks) * 32 + L) * 16);
-        const int c0 = 8 * ks + t, c1 = c0 + 4;
-        const float2 ab0 = lds<float2>(smem, s_ab + 8 * c0);
-        const float2 ab1 = lds<float2>(smem, s_ab + 8 * c1);
-        const uint32_t r0 = unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword;
-        const uint32_t r1 = unitK + c1 * 128 + ((w ^ (c1 & 7)) << 4) + kword;
-        const uint32_t wa0 = lds<uint32_t>(smem, r0), wa1 = lds<uint32_t>(smem, r1);
-        // l~ pairs (even, odd token) of bytes 2g (jb 0) and 2g+1 (jb 1) of channels c0, c1
-        float2 l00, l01, l10, l11;
-        if (!FULL) {
-          l00 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel0));
-          l01 = lds<float2>(smem, S::kLutK + lut_off(wa0, lane8, ksel1));
-          l10 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel0));
-          l11 = lds<float2>(smem, S::kLutK + lut_off(wa1, lane8, ksel1));
-        } else {
-          uint32_t e0, o0, e1, o1;
-          full_codes(wa0, lds<uint32_t>(smem, r0 + G::kResOff), e0, o0);
-          full_codes(wa1, lds<uint32_t>(smem, r1 + G::kResOff), e1, o1);
-          auto val = [&](uint32_t codes, uint32_t sel) {
-            return lds<float>(smem, S::kLutK + lut_off(codes, lane4, sel));
-          };
-          l00 = make_float2(val(e0, ksel0), val(o0, ksel0));
-          l01 = make_float2(val(e0, ksel1), val(o0, ksel1));
-          l10 = make_float2(val(e1, ksel0), val(o1, ksel0));
-          l11 = make_float2(val(e1, ksel1), val(o1, ksel1));
+        for (int mi = 0; mi < MT; ++mi) qf[mi] = lds<uint4>(smem, S::kQ + ((mi * 8 + ks) * 32 + L) * 16);
+        const int c0 = 16 * ks + 2 * t;   // channels c0, c0 + 1 (b0) and c0 + 8, c0 + 9 (b1)
+        const float4 abl = lds<float4>(smem, s_ab + 8 * c0);
+        const float4 abh = lds<float4>(smem, s_ab + 8 * (c0 + 8));
+        const float2 A[4] = {make_float2(abl.x, abl.x), make_float2(abl.z, abl.z), make_float2(abh.x, abh.x),
+                             make_float2(abh.z, abh.z)};
+        const float2 B[4] = {make_float2(abl.y, abl.y), make_float2(abl.w, abl.w), make_float2(abh.y, abh.y),
+                             make_float2(abh.w, abh.w)};
+        // k of tokens 4g + {0, 1} (jb 0) and 4g + {2, 3} (jb 1) of the four channels
+        float2 kv[4][2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int ch = c0 + (c & 1) + 8 * (c >> 1);
+          const uint32_t r = unitK + ch * 128 + ((w ^ (ch & 7)) << 4) + kword;
+          const uint32_t wa = lds<uint32_t>(smem, r);
+          float2 l0, l1;
+          if (!FULL) {
+            l0 = lds<float2>(smem, S::kLutK + lut_off(wa, lane8, ksel0));
+            l1 = lds<float2>(smem, S::kLutK + lut_off(wa, lane8, ksel1));
+          } else {
+            uint32_t ev, od;
+            full_codes(wa, lds<uint32_t>(smem, r + G::kResOff), ev, od);
+            auto val = [&](uint32_t codes, uint32_t sel) {
+              return lds<float>(smem, S::kLutK + lut_off(codes, lane4, sel));
+            };
+            l0 = make_float2(val(ev, ksel0), val(od, ksel0));
+            l1 = make_float2(val(ev, ksel1), val(od, ksel1));
+          }
+          kv[c][0] = __ffma2_rn(l0, B[c], A[c]);
+          kv[c][1] = __ffma2_rn(l1, B[c], A[c]);
         }
-        const float2 A0 = make_float2(ab0.x, ab0.x), B0 = make_float2(ab0.y, ab0.y);
-        const float2 A1 = make_float2(ab1.x, ab1.x), B1 = make_float2(ab1.y, ab1.y);
-        const float2 k00 = __ffma2_rn(l00, B0, A0), k01 = __ffma2_rn(l01, B0, A0);
-        const float2 k10 = __ffma2_rn(l10, B1, A1), k11 = __ffma2_rn(l11, B1, A1);
-        // n-tile k = 2 jb + eo: b0 = channel c0, b1 = channel c1
-        const float x0[4] = {k00.x, k00.y, k01.x, k01.y};
-        const float x1[4] = {k10.x, k10.y, k11.x, k11.y};
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          const uint32_t h0 = tf32_hi(x0[n]), h1 = tf32_hi(x1[n]);
-          const uint32_t lo0 = tf32_lo(x0[n]), lo1 = tf32_lo(x1[n]);
+          // n-tile n = token 4g + n: b0 = channels (c0, c0 + 1), b1 = (c0 + 8, c0 + 9)
+          float x[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) x[c] = (n & 1) ? kv[c][n >> 1].y : kv[c][n >> 1].x;
+          float hf[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) hf[c] = __uint_as_float(__float_as_uint(x[c]) & 0xFFFFE000u);
+          const float2 r01 = __ffma2_rn(make_float2(hf[0], hf[1]), make_float2(-1.0f, -1.0f), make_float2(x[0], x[1]));
+          const float2 r23 = __ffma2_rn(make_float2(hf[2], hf[3]), make_float2(-1.0f, -1.0f), make_float2(x[2], x[3]));
+          const uint32_t h0 = h2(hf[0], hf[1]), h1 = h2(hf[2], hf[3]);
+          const uint32_t lo0 = h2(r01.x, r01.y), lo1 = h2(r23.x, r23.y);
 #pragma unroll
           for (int mi = 0; mi < MT; ++mi) {
-            mma_tf32(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, h0, h1);
-            mma_tf32(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, lo0, lo1);
+            mma_f16(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, h0, h1);
+            mma_f16(sacc[mi][n], qf[mi].x, qf[mi].y, qf[mi].z, qf[mi].w, lo0, lo1);
           }
         }
       }
@@ -376,7 +427,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
         float mloc = -CUDART_INF_F;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float sv = sacc[rh >> 1][j & 3][2 * (rh & 1) + (j >> 2)] * sc;
+          float sv = sacc[rh >> 1][j & 3][2 * (rh & 1) + (j >> 2)] * sck;
           if (!all_visible && pos0 + j >= nv[rh]) sv = -CUDART_INF_F;
           pr[rh][j] = sv;
           mloc = fmaxf(mloc, sv);
@@ -425,7 +476,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1));
       if (failed) break;
-      prep_ab(unitV);
+      prep_ab(unitV, false);
       __syncwarp();
       if (kTmem) tmem_wait_st();   // the previous page's O stores have landed
 #pragma unroll

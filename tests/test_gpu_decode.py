@@ -342,3 +342,50 @@ def test_extreme_row_counts_and_alpha(cuda_device, mode):
         o, lse = run(pools, mode, q, table, ctx, Hkv, causal)
         ro, rl = reference(pools, mode, q, table, ctx, Hkv, causal)
         check_attention(o, lse, ro, rl)
+
+
+class ScaledKeys:
+    """A pool whose key pages' gamma_min and gamma_scale are multiplied by 2^e
+    (keys of magnitude ~2^e; the oracle dequantises the same metadata)."""
+
+    def __init__(self, base, e):
+        self.alpha = base.alpha
+        self.base = base
+        a, r, m = base.enc["k"]
+        m = m.copy()
+        m[:, :256] *= np.float32(2.0 ** e)
+        self.km = m
+        self.dev = dict(base.dev)
+        self.dev["k"] = (base.dev["k"][0], base.dev["k"][1], torch.from_numpy(m).cuda())
+
+    def fetch(self, mode):
+        a, r, _ = self.base.enc["k"]
+
+        def f(ids):
+            k = lo.reconstruct(a[ids], r[ids] if mode == "full" else None, self.km[ids], self.alpha, EPS)
+            return k, self.base.pages("v", mode, ids)
+        return f
+
+
+@pytest.mark.parametrize("mode,T", [("anchor", 4), ("full", 4), ("full", 8)])
+def test_extreme_magnitudes(cuda_device, mode, T):
+    """Queries of magnitude 2^24 and 2^-30, keys of magnitude 2^30 and 2^-30
+    (the softmax scale compensates, so the logits stay ordinary): the
+    tensor-core kernels scale their fp16 operands into range by powers of two
+    that return exactly in the softmax scale.  16-row (T = 4) and 32-row
+    (T = 8, full codes) tiles."""
+    base = Pools(2, 2048, 13, lazy=True)
+    B, Hq, Hkv = 2, 8, 2
+    ctx = np.array([2048, 1500])
+    table = np.stack([contiguous_table(1, Hkv, 8, 8, offset=b)[0] for b in range(B)])
+    q0 = lo.bf16_to_f32(inputs.queries_np((B, T, Hq, 128), 950 + T)).astype(np.float64)
+    s0 = 1.0 / math.sqrt(128)
+    for qe, ke in ((24, 0), (-30, 0), (0, 30), (0, -30)):
+        pools = base if ke == 0 else ScaledKeys(base, ke)
+        # a BF16 value times a power of two is a BF16 value: keep the top 16 bits
+        q_bits = ((q0 * 2.0 ** qe).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        scale = s0 * 2.0 ** (-qe - ke)
+        o, lse = run(pools, mode, q_bits, table, ctx, Hkv, True, scale=scale)
+        q = lo.bf16_to_f32(q_bits).astype(np.float64)
+        ro, rl = at.decode_attention(q, pools.fetch(mode), table, ctx, Hkv, scale, True)
+        check_attention(o, lse, ro, rl)
