@@ -259,6 +259,37 @@ def encode_pages(x_bits: np.ndarray, alpha, eps, C: int = 32, return_stages: boo
     return anchor, residual, meta
 
 
+def pages_from_tokens(x_tm_bits: np.ndarray, n_heads: int, H: int = 128, P: int = 256):
+    """KV held token-major, as paged attention keeps it, -> the encoder's pages.
+
+    The paper encodes KV pages in a layout that complies with paged attention
+    (§4.1, "Hierarchical Quantization"); there the cache is token-major: token
+    t's H channels of head h are columns h*H .. h*H + H - 1 of row t.
+    x_tm_bits: BF16 bits [n_tokens, >= n_heads * H] (columns past n_heads * H
+    are ignored).  Returns (pages [n_heads * n_pp, H, P], valid [n_heads * n_pp])
+    with n_pp = ceil(n_tokens / P): page h * n_pp + j holds tokens
+    j*P .. j*P + P - 1 of head h channel-major; the last page of each head holds
+    the remaining tokens, zero padded, and valid counts them.
+    """
+    n_tokens = x_tm_bits.shape[0]
+    n_pp = -(-n_tokens // P)
+    pages = np.zeros((n_heads * n_pp, H, P), dtype=np.uint16)
+    valid = np.zeros(n_heads * n_pp, dtype=np.int32)
+    for h in range(n_heads):
+        for j in range(n_pp):
+            t0, t1 = j * P, min((j + 1) * P, n_tokens)
+            pages[h * n_pp + j, :, :t1 - t0] = x_tm_bits[t0:t1, h * H:(h + 1) * H].T
+            valid[h * n_pp + j] = t1 - t0
+    return pages, valid
+
+
+def encode_tokens(x_tm_bits: np.ndarray, n_heads: int, alpha, eps, C: int = 32):
+    """Algorithm 1 on token-major KV: the pages of pages_from_tokens, each last
+    page of a head encoded over its valid tokens; returns (anchor, residual, meta)."""
+    pages, valid = pages_from_tokens(x_tm_bits, n_heads)
+    return encode_pages(pages, alpha, eps, C, valid=valid)
+
+
 def reconstruct(anchor: np.ndarray, residual, meta: np.ndarray, alpha, eps,
                 H: int = 128, P: int = 256, C: int = 32) -> np.ndarray:
     """Inverse transform, float64 result [N, H, P].

@@ -379,3 +379,33 @@ def test_partial_page_statistics_brute_force():
     assert np.all(st.mu[0, :, 3:] == 0) and np.all(st.sigma[0, :, 3:] == 0)
     assert np.all(st.gmin[1] == 0) and np.all(st.gscale[1] == 0)
     assert np.all(st.mu[1] == 0) and np.all(st.sigma[1] == 0) and np.all(st.I[1] == 0)
+
+
+def test_token_major_pages_brute_force():
+    """pages_from_tokens: every element of a 300-token, 2-head token-major block
+    (with two extra columns per row) lands at page h * n_pp + t // 256, channel
+    c, position t % 256; padding is zero and the valid counts are 256 and 44."""
+    rng = np.random.default_rng(5)
+    n_tokens, n_heads = 300, 2
+    x = rng.integers(0, 1 << 16, size=(n_tokens, n_heads * 128 + 2), dtype=np.uint16)
+    pages, valid = lo.pages_from_tokens(x, n_heads)
+    assert pages.shape == (4, 128, 256) and list(valid) == [256, 44, 256, 44]
+    for t in range(n_tokens):
+        for h in range(n_heads):
+            assert np.array_equal(pages[h * 2 + t // 256, :, t % 256], x[t, h * 128:(h + 1) * 128])
+    assert not pages[1, :, 44:].any() and not pages[3, :, 44:].any()
+
+
+def test_token_major_encode_is_the_page_encode_of_the_same_tokens():
+    """A head whose tokens fill whole pages encodes, through the token-major
+    entry, exactly as those pages do through the page encoder (the layout
+    changes where the values come from, nothing else), and a ragged last page
+    encodes as a partial page of its valid tokens."""
+    x_pages = inputs.kv_pages_np(1, 768, 33, inputs.outlier_pairs(1, 33))   # 3 pages of one head
+    # token-major rows of that head: token t = page t // 256, position t % 256
+    x_tm = np.concatenate([x_pages[j].T for j in range(3)], axis=0)[:612]
+    a, r, m = lo.encode_tokens(x_tm, 1, 100.0, 1e-6)
+    a2, r2, m2 = lo.encode_pages(x_pages[:2], 100.0, 1e-6)
+    assert np.array_equal(a[:2], a2) and np.array_equal(r[:2], r2) and np.array_equal(m[:2], m2)
+    a3, r3, m3 = lo.encode_pages(x_pages[2:], 100.0, 1e-6, valid=np.array([100]))
+    assert np.array_equal(a[2:], a3) and np.array_equal(r[2:], r3) and np.array_equal(m[2:], m3)
