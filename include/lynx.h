@@ -133,6 +133,26 @@ int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t
                               const lynx_params_t* params, uint8_t* anchor, uint8_t* residual,
                               float* meta, void* stream);
 
+/* Algorithm 1 on KV held token-major, the layout of paged attention (the
+ * paper's §4.1 encodes pages "complying with paged attention"): element
+ * (token t, head h, channel c) of one layer's K or V is
+ * x_bf16[t * token_stride + h * 128 + c] (device, BF16, 2-byte aligned;
+ * token_stride >= n_heads * 128 elements, so K and V interleaved per token or
+ * more heads per row are read in place).  Pages are 256 tokens of one head:
+ * page h * n_pp + j (n_pp = ceil(n_tokens / 256)) holds tokens 256 j ..
+ * 256 j + 255 of head h and is written to anchor / residual / meta in the
+ * layouts of lynx_encode_pages (caller-allocated: n_heads * n_pp pages).  The
+ * last page of each head holds the remaining n_tokens - 256 (n_pp - 1) tokens
+ * and is encoded over them as lynx_encode_pages_partial does; every other page
+ * is encoded exactly as lynx_encode_pages encodes the same 256 tokens.
+ * Asynchronous on `stream`.  Errors: INVALID_ARG for negative counts, a
+ * token_stride below n_heads * 128 or a NULL pointer (when there is work);
+ * ALIGNMENT for an odd x or outputs not 16-byte aligned; n_tokens == 0 or
+ * n_heads == 0 is a no-op. */
+int lynx_encode_tokens(const void* x_bf16, int64_t n_tokens, int n_heads, int64_t token_stride,
+                       const lynx_params_t* params, uint8_t* anchor, uint8_t* residual, float* meta,
+                       void* stream);
+
 /* Stage 3 of Algorithm 1 alone: codes[i] = round(127 ln(1 + alpha |a_i|) /
  * ln(1 + alpha)) in 0..127 for float32 magnitudes |a_i| <= 1 (larger values
  * are clamped to 1), decided exactly for the float32 input as in

@@ -10,6 +10,7 @@ from .lynx import (  # noqa: F401
     LynxError,
     Params,
     lynx_attn_merge,
+    lynx_encode_tokens,
     lynx_decode_attn,
     lynx_decode_attn_bf16,
     lynx_decode_attn_workspace_size,

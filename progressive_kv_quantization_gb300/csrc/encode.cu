@@ -136,6 +136,111 @@ __device__ __forceinline__ void load_chunk(const uint4* __restrict__ src, uint4 
   for (int k = 0; k < 4; ++k) raw[k] = __ldg(src + k);
 }
 
+// Extremes of one channel chunk: w[t] holds tokens 2t (low half) and 2t + 1
+// (high half) as BF16; with PARTIAL only the first nc tokens count (min +inf,
+// max -inf when there are none).
+template <bool PARTIAL>
+__device__ __forceinline__ void chunk_extremes(const uint32_t (&w)[16], int nc, float& cmn, float& cmx) {
+  uint32_t wmin[16], wmax[16];   // the pairs with padding replaced by +inf / -inf (PARTIAL)
+  if (PARTIAL) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const bool lo = 2 * t < nc, hi = 2 * t + 1 < nc;
+      wmin[t] = (lo ? (w[t] & 0xFFFFu) : 0x7F80u) | (hi ? (w[t] & 0xFFFF0000u) : 0x7F800000u);
+      wmax[t] = (lo ? (w[t] & 0xFFFFu) : 0xFF80u) | (hi ? (w[t] & 0xFFFF0000u) : 0xFF800000u);
+    }
+  }
+  // on the packed BF16 pairs (exact)
+  __nv_bfloat162 bmn = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[0] : &w[0]);
+  __nv_bfloat162 bmx = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[0] : &w[0]);
+#pragma unroll
+  for (int t = 1; t < 16; ++t) {
+    bmn = __hmin2(bmn, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[t] : &w[t]));
+    bmx = __hmax2(bmx, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[t] : &w[t]));
+  }
+  cmn = fminf(__low2float(bmn), __high2float(bmn));
+  cmx = fmaxf(__low2float(bmx), __high2float(bmx));
+}
+
+// Stages 1-4 of one channel chunk (32 tokens, w as in chunk_extremes), given
+// the row's gamma_min mn and maximum mx and the chunk's extremes cmn, cmx:
+// the packed anchor and residual words of the chunk (16 bytes each) and its
+// gamma_scale, mu and sigma.  PARTIAL: only the first nc tokens are valid
+// (statistics over them; padding gets code 0 with a positive sign).
+template <bool PARTIAL>
+__device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, float mn, float mx, float cmn,
+                                             float cmx, float eps, const float* __restrict__ s_thr,
+                                             const QuantConsts& qc, uint4& anc, uint4& res, float& gscale,
+                                             float& mu, float& sigma) {
+  // ---- Stage 1: x_n = (x - gamma_min) / (gamma_scale + eps)
+  gscale = __fsub_rn(mx, mn);
+  const float dg = __fadd_rn(gscale, eps);
+  const float rg = __frcp_rn(dg);
+  const float2 nmn2 = f2(-mn), ndg2 = f2(-dg), rg2 = f2(rg);
+  float2 xn[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+    if (PARTIAL) {   // padding enters no operation: it becomes gamma_min, so x_n = 0 exactly
+      v.x = 2 * t < nc ? v.x : mn;
+      v.y = 2 * t + 1 < nc ? v.y : mn;
+    }
+    xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
+  }
+
+  // ---- Stage 2: mu (left-to-right sum), sigma, x_f
+  float s = xn[0].x;
+  s = __fadd_rn(s, xn[0].y);
+#pragma unroll
+  for (int t = 1; t < 16; ++t) {
+    s = __fadd_rn(s, xn[t].x);
+    s = __fadd_rn(s, xn[t].y);
+  }
+  // (PARTIAL: padding adds exact zeros, so s is the left-to-right sum of the valid x_n)
+  mu = __fmul_rn(s, 0.03125f);
+  if (PARTIAL && nc < 32) mu = nc == 0 ? 0.0f : div1(s, (float)nc, __frcp_rn((float)nc));
+  const float xn_max = div1(__fsub_rn(cmx, mn), dg, rg);
+  const float xn_min = div1(__fsub_rn(cmn, mn), dg, rg);
+  sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
+  if (PARTIAL && nc == 0) sigma = 0.0f;
+  const float ds = __fadd_rn(sigma, eps);
+  const float rs = __frcp_rn(ds);
+  const float2 nmu2 = f2(-mu), rs2 = f2(rs);
+
+  // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
+  // rounded floats, sign masks, then split and pack
+  uint32_t pa[4], pr[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t ib[8];
+    float xs[8];   // centred values (for their signs)
+    float2 a[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = 4 * q + u;
+      float2 xc = __fadd2_rn(xn[t], nmu2);
+      if (PARTIAL) {   // padding: x_c = +0, hence code 0 with a positive sign
+        xc.x = 2 * t < nc ? xc.x : 0.0f;
+        xc.y = 2 * t + 1 < nc ? xc.y : 0.0f;
+      }
+      xs[2 * u] = xc.x;
+      xs[2 * u + 1] = xc.y;
+      a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
+    }
+    // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
+    quantise8(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
+    // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
+    const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
+    const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
+    // byte m of a packed word: token 2m in the low nibble, token 2m + 1 in the high nibble.
+    // anchor nibble (S>0 ? I : ~I) >> 4 = ((I >> 4) ^ S) & 15; residual (7 - I) mod 16 = (I ^ 7) & 15
+    pa[q] = (((Ie >> 4) ^ Se) & 0x0F0F0F0Fu) | ((Io ^ So) & 0xF0F0F0F0u);
+    pr[q] = ((Ie ^ 0x07070707u) & 0x0F0F0F0Fu) | (((Io << 4) ^ 0x70707070u) & 0xF0F0F0F0u);
+  }
+  anc = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+  res = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+}
+
 // PARTIAL: valid[page] (clamped to 0..256) tokens of each page are valid; the
 // statistics cover them only, padding tokens get code 0 with a positive sign,
 // and a chunk without valid tokens gets mu = sigma = 0 (a partial last page of
@@ -172,28 +277,13 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
 
     // valid tokens of the page and of this lane's chunk
     int v_page = 256, nc = 32;
-    uint32_t wmin[16], wmax[16];   // the pairs with padding replaced by +inf / -inf (PARTIAL)
     if (PARTIAL) {
       v_page = min(max(__ldg(valid + (g >> 5)), 0), 256);
       nc = min(max(v_page - 32 * (lane & 7), 0), 32);
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const bool lo = 2 * t < nc, hi = 2 * t + 1 < nc;
-        wmin[t] = (lo ? (w[t] & 0xFFFFu) : 0x7F80u) | (hi ? (w[t] & 0xFFFF0000u) : 0x7F800000u);
-        wmax[t] = (lo ? (w[t] & 0xFFFFu) : 0xFF80u) | (hi ? (w[t] & 0xFFFF0000u) : 0xFF800000u);
-      }
     }
-
-    // ---- chunk and row extremes on the packed BF16 pairs (exact)
-    __nv_bfloat162 bmn = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[0] : &w[0]);
-    __nv_bfloat162 bmx = *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[0] : &w[0]);
-#pragma unroll
-    for (int t = 1; t < 16; ++t) {
-      bmn = __hmin2(bmn, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmin[t] : &w[t]));
-      bmx = __hmax2(bmx, *reinterpret_cast<const __nv_bfloat162*>(PARTIAL ? &wmax[t] : &w[t]));
-    }
-    const float cmn = fminf(__low2float(bmn), __high2float(bmn));   // chunk min of x
-    const float cmx = fmaxf(__low2float(bmx), __high2float(bmx));   // chunk max of x
+    // ---- chunk and row extremes
+    float cmn, cmx;
+    chunk_extremes<PARTIAL>(w, nc, cmn, cmx);
     float mn = cmn, mx = cmx;
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) {
@@ -205,74 +295,11 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
       mx = 0.0f;
     }
 
-    // ---- Stage 1: x_n = (x - gamma_min) / (gamma_scale + eps)
-    const float gscale = __fsub_rn(mx, mn);
-    const float dg = __fadd_rn(gscale, eps);
-    const float rg = __frcp_rn(dg);
-    const float2 nmn2 = f2(-mn), ndg2 = f2(-dg), rg2 = f2(rg);
-    float2 xn[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
-      if (PARTIAL) {   // padding enters no operation: it becomes gamma_min, so x_n = 0 exactly
-        v.x = 2 * t < nc ? v.x : mn;
-        v.y = 2 * t + 1 < nc ? v.y : mn;
-      }
-      xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
-    }
-
-    // ---- Stage 2: mu (left-to-right sum), sigma, x_f
-    float s = xn[0].x;
-    s = __fadd_rn(s, xn[0].y);
-#pragma unroll
-    for (int t = 1; t < 16; ++t) {
-      s = __fadd_rn(s, xn[t].x);
-      s = __fadd_rn(s, xn[t].y);
-    }
-    // (PARTIAL: padding adds exact zeros, so s is the left-to-right sum of the valid x_n)
-    float mu = __fmul_rn(s, 0.03125f);
-    if (PARTIAL && nc < 32)
-      mu = nc == 0 ? 0.0f : div1(s, (float)nc, __frcp_rn((float)nc));
-    const float xn_max = div1(__fsub_rn(cmx, mn), dg, rg);
-    const float xn_min = div1(__fsub_rn(cmn, mn), dg, rg);
-    float sigma = fmaxf(__fsub_rn(xn_max, mu), __fsub_rn(mu, xn_min));
-    if (PARTIAL && nc == 0) sigma = 0.0f;
-    const float ds = __fadd_rn(sigma, eps);
-    const float rs = __frcp_rn(ds);
-    const float2 nmu2 = f2(-mu), rs2 = f2(rs);
-
-    // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
-    // rounded floats, sign masks, then split and pack
-    uint32_t pa[4], pr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t ib[8];
-      float xs[8];   // centred values (for their signs)
-      float2 a[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = 4 * q + u;
-        float2 xc = __fadd2_rn(xn[t], nmu2);
-        if (PARTIAL) {   // padding: x_c = +0, hence code 0 with a positive sign
-          xc.x = 2 * t < nc ? xc.x : 0.0f;
-          xc.y = 2 * t + 1 < nc ? xc.y : 0.0f;
-        }
-        xs[2 * u] = xc.x;
-        xs[2 * u + 1] = xc.y;
-        a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
-      }
-      // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
-      quantise8(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
-      // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
-      const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
-      const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
-      // byte m of a packed word: token 2m in the low nibble, token 2m + 1 in the high nibble.
-      // anchor nibble (S>0 ? I : ~I) >> 4 = ((I >> 4) ^ S) & 15; residual (7 - I) mod 16 = (I ^ 7) & 15
-      pa[q] = (((Ie >> 4) ^ Se) & 0x0F0F0F0Fu) | ((Io ^ So) & 0xF0F0F0F0u);
-      pr[q] = ((Ie ^ 0x07070707u) & 0x0F0F0F0Fu) | (((Io << 4) ^ 0x70707070u) & 0xF0F0F0F0u);
-    }
-    anchor[g * 32 + lane] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-    residual[g * 32 + lane] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+    uint4 anc, res;
+    float gscale, mu, sigma;
+    encode_chunk<PARTIAL>(w, nc, mn, mx, cmn, cmx, eps, s_thr, qc, anc, res, gscale, mu, sigma);
+    anchor[g * 32 + lane] = anc;
+    residual[g * 32 + lane] = res;
 
     const int64_t page = g >> 5;
     const int rgrp = (int)(g & 31);
@@ -284,6 +311,86 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
     }
     mp[kMetaMuOff + (lane & 7) * kH + ch] = mu;
     mp[kMetaSigmaOff + (lane & 7) * kH + ch] = sigma;
+  }
+}
+
+// Token-major input, the layout of paged attention: token t's 128 channels of
+// head h at x[t * stride + h * 128 ..].  Page (h, j) = tokens 256 j .. 256 j +
+// 255 of head h, written as page h * n_pp + j; the last page of a head may be
+// partial (statistics over its valid tokens, as encode_kernel<true>).
+//
+// Work mapping: one CTA per page (grid-stride); warp w owns chunk w (tokens
+// 32 w .. 32 w + 31 of the page); the channels are taken in four quarters,
+// lane L owning channel 32 q + L of quarter q: its 32 tokens are 32 two-byte
+// loads (a warp reads 64 contiguous bytes of a token row; the rest of the row's
+// line serves the other quarters from cache).  The row extremes of a channel
+// join its 8 chunks' extremes through shared memory (double-buffered by
+// quarter, one barrier per quarter); then each lane runs Stages 1-4 on its
+// channel chunk exactly as encode_kernel does.  One launch covers pages
+// j_begin .. j_begin + j_count - 1 of every head: the full pages (PARTIAL =
+// false) or the ragged last pages (PARTIAL = true).  (Staging each warp's 32
+// token rows in shared memory with 8-byte loads first was measured slower.)
+template <bool PARTIAL>
+__global__ void __launch_bounds__(256, 2)
+encode_tokens_kernel(const uint16_t* __restrict__ x, int64_t n_tokens, int n_heads, int n_pp, int j_begin,
+                     int j_count, int64_t stride, uint4* __restrict__ anchor, uint4* __restrict__ residual,
+                     float* __restrict__ meta, const EncodeTables tab) {
+  __shared__ float s_thr[129];
+  __shared__ float s_mn[2][8][32], s_mx[2][8][32];
+  for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
+  __syncthreads();
+
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const float eps = tab.eps;
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
+  int buf = 0;
+
+  const int64_t n_items = (int64_t)n_heads * j_count;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int64_t h = item / j_count;
+    const int64_t j = j_begin + item % j_count;
+    const int64_t page = h * n_pp + j;
+    const int64_t t0 = j * 256;
+    const int v = PARTIAL ? (int)min(n_tokens - t0, (int64_t)256) : 256;
+    const int nc = PARTIAL ? min(max(v - 32 * w, 0), 32) : 32;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q, buf ^= 1) {
+      const int c = 32 * q + lane;
+      // the chunk's 32 values of channel c as BF16 pairs (token 2t low, 2t + 1 high)
+      const uint16_t* src = x + (t0 + 32 * w) * stride + h * kH + c;
+      uint32_t w16[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w16[i] = (!PARTIAL || i < nc) ? (uint32_t)__ldg(src + i * stride) : 0u;
+      uint32_t wv[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) wv[t] = w16[2 * t] | (w16[2 * t + 1] << 16);
+
+      float cmn, cmx;
+      chunk_extremes<PARTIAL>(wv, nc, cmn, cmx);
+      s_mn[buf][w][lane] = cmn;
+      s_mx[buf][w][lane] = cmx;
+      __syncthreads();
+      float mn = s_mn[buf][0][lane], mx = s_mx[buf][0][lane];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) {
+        mn = fminf(mn, s_mn[buf][k][lane]);
+        mx = fmaxf(mx, s_mx[buf][k][lane]);
+      }
+
+      uint4 anc, res;
+      float gscale, mu, sigma;
+      encode_chunk<PARTIAL>(wv, nc, mn, mx, cmn, cmx, eps, s_thr, qc, anc, res, gscale, mu, sigma);
+      anchor[(page * kH + c) * 8 + w] = anc;
+      residual[(page * kH + c) * 8 + w] = res;
+      float* mp = meta + page * kMetaFloats;
+      if (w == 0) {
+        mp[c] = mn;
+        mp[kH + c] = gscale;
+      }
+      mp[kMetaMuOff + w * kH + c] = mu;
+      mp[kMetaSigmaOff + w * kH + c] = sigma;
+    }
   }
 }
 
@@ -340,6 +447,34 @@ cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8
                           float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s) {
   return valid ? launch_encode_t<true>(x, n_pages, anchor, residual, meta, tab, valid, s)
                : launch_encode_t<false>(x, n_pages, anchor, residual, meta, tab, nullptr, s);
+}
+
+template <bool PARTIAL>
+cudaError_t launch_tokens_t(const void* x, int64_t n_tokens, int n_heads, int n_pp, int j_begin, int j_count,
+                            int64_t stride, uint8_t* anchor, uint8_t* residual, float* meta,
+                            const EncodeTables* tab, cudaStream_t s) {
+  const int64_t n_items = (int64_t)n_heads * j_count;
+  if (n_items == 0) return cudaSuccess;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_tokens_kernel<PARTIAL>, 256, 0);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
+  const int blocks = (int)(n_items < max_blocks ? n_items : max_blocks);
+  encode_tokens_kernel<PARTIAL><<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(x), n_tokens, n_heads, n_pp,
+                                                      j_begin, j_count, stride, reinterpret_cast<uint4*>(anchor),
+                                                      reinterpret_cast<uint4*>(residual), meta, *tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
+                                 uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
+                                 cudaStream_t s) {
+  const int n_pp = (int)((n_tokens + 255) / 256);
+  const int n_full = (int)(n_tokens / 256);
+  cudaError_t e = launch_tokens_t<false>(x, n_tokens, n_heads, n_pp, 0, n_full, stride, anchor, residual, meta,
+                                         tab, s);
+  if (e != cudaSuccess || n_full == n_pp) return e;
+  return launch_tokens_t<true>(x, n_tokens, n_heads, n_pp, n_full, 1, stride, anchor, residual, meta, tab, s);
 }
 
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,

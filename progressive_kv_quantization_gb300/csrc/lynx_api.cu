@@ -211,6 +211,31 @@ int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t
                        "lynx_encode_pages_partial launch");
 }
 
+int lynx_encode_tokens(const void* x_bf16, int64_t n_tokens, int n_heads, int64_t token_stride,
+                       const lynx_params_t* params, uint8_t* anchor, uint8_t* residual, float* meta,
+                       void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (n_tokens < 0 || n_heads < 0)
+    return fail(LYNX_ERR_INVALID_ARG, "n_tokens=%lld, n_heads=%d", (long long)n_tokens, n_heads);
+  if (n_tokens == 0 || n_heads == 0) return LYNX_OK;
+  if (token_stride < (int64_t)n_heads * 128)
+    return fail(LYNX_ERR_INVALID_ARG, "token_stride=%lld < n_heads * 128", (long long)token_stride);
+  if (!x_bf16 || !anchor || !residual || !meta) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if ((reinterpret_cast<uintptr_t>(x_bf16) & 1u) != 0)
+    return fail(LYNX_ERR_ALIGNMENT, "x must be 2-byte aligned");
+  if (misaligned(anchor) || misaligned(residual) || misaligned(meta))
+    return fail(LYNX_ERR_ALIGNMENT, "anchor, residual and meta must be 16-byte aligned");
+  if (n_tokens > ((int64_t)1 << 40) || (int64_t)n_heads * ((n_tokens + 255) / 256) > ((int64_t)1 << 40))
+    return fail(LYNX_ERR_INVALID_ARG, "too many tokens");
+  const EncodeTables* tab = encode_tables(params->alpha, params->eps);
+  cudaError_t e = launch_encode_tokens(x_bf16, n_tokens, n_heads, token_stride, anchor, residual, meta, tab,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_tokens launch");
+  return LYNX_OK;
+}
+
 int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* params,
                              uint8_t* codes, void* stream) {
   g_last_error[0] = '\0';

@@ -51,6 +51,9 @@ int* device_status_ptr();   // device address of this device's error word
 // Launchers (one per kernel family).  Return cudaGetLastError() of the launch.
 cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
                           float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s);
+cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
+                                 uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
+                                 cudaStream_t s);
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,
                             cudaStream_t s);
 cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,

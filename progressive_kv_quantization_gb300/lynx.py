@@ -53,6 +53,7 @@ _PP = ctypes.POINTER(lynx_params_t)
 SIGNATURES = {
     "lynx_encode_pages": (_I32, [_VP, _I64, _PP, _VP, _VP, _VP, _VP]),
     "lynx_encode_pages_partial": (_I32, [_VP, _I64, _VP, _PP, _VP, _VP, _VP, _VP]),
+    "lynx_encode_tokens": (_I32, [_VP, _I64, ctypes.c_int, _I64, _PP, _VP, _VP, _VP, _VP]),
     "lynx_reconstruct": (_I32, [_VP, _VP, _VP, _I64, _PP, _VP, _I32, _VP]),
     "lynx_quantize_magnitudes": (_I32, [_VP, _I64, _PP, _VP, _VP]),
     "lynx_decode_attn": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -140,6 +141,39 @@ def lynx_encode_pages(x, params: Params = Params(), anchor=None, residual=None, 
         return anchor, residual, meta
     _check(load().lynx_encode_pages(_ptr(x), n, ctypes.byref(p), _ptr(anchor), _ptr(residual),
                                     _ptr(meta), _stream(stream)), "lynx_encode_pages")
+    return anchor, residual, meta
+
+
+def lynx_encode_tokens(x, n_heads: int, params: Params = Params(), anchor=None, residual=None, meta=None,
+                       stream=None):
+    """Algorithm 1 on token-major KV (the layout of paged attention): x is a
+    BF16 tensor whose first dimension is the token and whose row holds head h's
+    128 channels at elements h*128 .. h*128 + 127 (e.g. [n_tokens, n_heads, 128],
+    or a row-strided view of a wider buffer).  Returns the pages (n_heads *
+    ceil(n_tokens / 256) of them, page h * n_pp + j = tokens 256 j .. of head h)
+    as lynx_encode_pages does; each head's last page is encoded over its valid
+    tokens."""
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise LynxError("x must be a CUDA bfloat16 tensor")
+    n_tokens = x.shape[0]
+    inner = x[0].numel() if n_tokens > 0 else 0
+    if n_tokens > 0 and (inner < n_heads * H or not x[0].is_contiguous()):
+        raise LynxError("each token row must hold n_heads * 128 contiguous channels")
+    stride = x.stride(0) if n_tokens > 0 else n_heads * H
+    n_pp = (n_tokens + P - 1) // P
+    n = n_heads * n_pp
+    dev = x.device
+    anchor = anchor if anchor is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=dev)
+    residual = residual if residual is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=dev)
+    meta = meta if meta is not None else torch.empty((n, META_FLOATS), dtype=torch.float32, device=dev)
+    for t, nm in ((anchor, "anchor"), (residual, "residual")):
+        _need(t, torch.uint8, nm)
+    _need(meta, torch.float32, "meta")
+    if anchor.numel() < n * PLANE_BYTES or residual.numel() < n * PLANE_BYTES or meta.numel() < n * META_FLOATS:
+        raise LynxError("output buffers too small")
+    p = params.c()
+    _check(load().lynx_encode_tokens(_ptr(x), n_tokens, n_heads, stride, ctypes.byref(p), _ptr(anchor),
+                                     _ptr(residual), _ptr(meta), _stream(stream)), "lynx_encode_tokens")
     return anchor, residual, meta
 
 

@@ -105,3 +105,20 @@ def test_row_limit_merge_and_partial_argument_checks(lynx_lib):
     assert lib.lynx_encode_pages_partial(a, 1, None, ok, a, a, a, None) == -1
     assert lib.lynx_encode_pages_partial(a, 1, odd, ok, a, a, a, None) == -3
     assert lib.lynx_encode_pages_partial(a, 0, None, ok, a, a, a, None) == 0
+
+
+def test_token_major_encode_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 1)
+    ok = ctypes.byref(_p())
+    # token_stride below n_heads * 128, negative counts, NULL, odd x, misaligned outputs, no work
+    assert lib.lynx_encode_tokens(a, 300, 2, 255, ok, a, a, a, None) == -1
+    assert lib.lynx_encode_tokens(a, -1, 2, 256, ok, a, a, a, None) == -1
+    assert lib.lynx_encode_tokens(None, 300, 2, 256, ok, a, a, a, None) == -1
+    assert lib.lynx_encode_tokens(odd, 300, 2, 256, ok, a, a, a, None) == -3
+    assert lib.lynx_encode_tokens(a, 300, 2, 256, ok, ctypes.c_void_p(a.value + 4), a, a, None) == -3
+    assert lib.lynx_encode_tokens(a, 0, 2, 256, ok, None, None, None, None) == 0
+    assert lib.lynx_encode_tokens(a, 300, 0, 0, ok, None, None, None, None) == 0
+    assert lib.lynx_encode_tokens(a, 300, 2, 256, ctypes.byref(_p(alpha=0.0)), a, a, a, None) == -2
