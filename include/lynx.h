@@ -22,6 +22,10 @@
  *   lynx_attn_merge       combines attention over two disjoint key sets by
  *                         their log-sum-exps (the drafts' own uncompressed KV
  *                         joined to the verification over the packed cache).
+ *   lynx_encode_tokens    Algorithm 1 reading token-major (paged-attention) KV.
+ *   lynx_encode_variant, lynx_reconstruct_variant, lynx_decode_attn_int4
+ *                         the single-precision comparators of §6.1 (uniform
+ *                         INT8 / INT4, Lynx-INT8, Lynx-INT4).
  *
  * ---------------------------------------------------------------------------
  * Data layout (all sizes for H = 128 channels, P = 256 tokens, C = 32):
@@ -106,6 +110,33 @@ enum {
 /* Output element types of lynx_reconstruct. */
 enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 };
 
+/* Single-precision variants (paper §6.1: the uniform INT8 / INT4 baselines, and
+ * Lynx-INT8 / Lynx-INT4, the hierarchical quantiser of §4.1 at one precision
+ * without the split stream; §2.3 for the uniform form).
+ *   LYNX_VARIANT_LYNX_INT8     codes [n_pages][128][256] bytes: Algorithm 1's
+ *                              signed 8-bit code S > 0 ? I : -I - 1 (its
+ *                              arithmetic shift by 4 is the Anchor); meta as
+ *                              lynx_encode_pages.  Values = Lynx's full codes.
+ *   LYNX_VARIANT_LYNX_INT4     codes [n_pages][128][128] bytes, two per byte (low
+ *                              nibble = even token): Algorithm 1 with 7 magnitude
+ *                              levels, I4 = round(7 ln(1 + alpha |x_f|) /
+ *                              ln(1 + alpha)), as the sign-aware nibble
+ *                              S > 0 ? I4 : -I4 - 1; meta as lynx_encode_pages;
+ *                              x_f = S ((1 + alpha)^(I4/7) - 1) / alpha.
+ *   LYNX_VARIANT_UNIFORM_INT8  codes [n_pages][128][256] bytes, Q in 0..255;
+ *   LYNX_VARIANT_UNIFORM_INT4  codes [n_pages][128][128] bytes, Q in 0..15, two
+ *                              per byte (low nibble = even token); for both,
+ *                              per channel row of a page S = (max - min) /
+ *                              (2^b - 1), Q = round((x - min) / S) (0 if S = 0),
+ *                              x = min + Q S; meta [n_pages][256] float32 =
+ *                              min[128], S[128]. */
+enum {
+  LYNX_VARIANT_LYNX_INT8 = 1,
+  LYNX_VARIANT_LYNX_INT4 = 2,
+  LYNX_VARIANT_UNIFORM_INT8 = 3,
+  LYNX_VARIANT_UNIFORM_INT4 = 4
+};
+
 /* Algorithm 1 (paper §4.1, all four stages) on n_pages BF16 pages.
  *   x_bf16    [n_pages][128][256] BF16 (read only)
  *   anchor    [n_pages][128][128] uint8, written
@@ -132,6 +163,25 @@ int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* 
 int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t* valid_tokens,
                               const lynx_params_t* params, uint8_t* anchor, uint8_t* residual,
                               float* meta, void* stream);
+
+/* Encode BF16 pages [n_pages][128][256] (device, 16-byte aligned) into one of
+ * the single-precision variants above; codes and meta are caller-allocated
+ * device buffers (16-byte aligned) in the variant's layout.  params is read for
+ * the Lynx variants (alpha, eps; errors as lynx_encode_pages) and ignored for
+ * the uniform ones.  Asynchronous on `stream`.  Errors: INVALID_ARG for an
+ * unknown variant, n_pages < 0 or a NULL pointer; ALIGNMENT; n_pages == 0 is a
+ * no-op. */
+int lynx_encode_variant(const void* x_bf16, int64_t n_pages, int variant, const lynx_params_t* params,
+                        uint8_t* codes, float* meta, void* stream);
+
+/* Dequantise a variant's codes and meta into out [n_pages][128][256], BF16
+ * (LYNX_OUT_BF16, rounded to nearest even) or float32 (LYNX_OUT_F32).  Lynx
+ * variants: fmaf(fmaf(v, sigma+eps, mu), gamma_scale+eps, gamma_min) with v the
+ * code's signed inverse-compander value rounded to float32 (as
+ * lynx_reconstruct); uniform: fmaf(Q, S, min).  Errors as lynx_encode_variant;
+ * INVALID_ARG for an unknown out_dtype. */
+int lynx_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
+                             const lynx_params_t* params, void* out, int out_dtype, void* stream);
 
 /* Algorithm 1 on KV held token-major, the layout of paged attention (the
  * paper's §4.1 encodes pages "complying with paged attention"): element
@@ -240,6 +290,16 @@ int lynx_decode_attn_noalloc(const void* q_bf16, int B, int T, int Hq, int Hkv, 
                              int64_t n_pool_pages, const int32_t* page_table, int max_pages,
                              const int32_t* ctx_len, const lynx_params_t* params, float sm_scale,
                              int causal, float* out, float* lse, void* stream);
+
+/* Decode / verification attention over Lynx-INT4 pages (LYNX_VARIANT_LYNX_INT4
+ * codes and meta): the draft-decode kernels of lynx_decode_attn with the
+ * 7-level value table.  Arguments, workspace and errors as lynx_decode_attn
+ * without a residual pool. */
+int lynx_decode_attn_int4(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                          const uint8_t* k_codes, const float* k_meta, const uint8_t* v_codes,
+                          const float* v_meta, int64_t n_pool_pages, const int32_t* page_table, int max_pages,
+                          const int32_t* ctx_len, const lynx_params_t* params, float sm_scale, int causal,
+                          float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Merge of two attention results over disjoint key sets.  The verification
  * pass (paper §4.3) also attends to the draft tokens' own K and V, which the

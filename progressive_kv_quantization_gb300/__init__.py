@@ -11,6 +11,9 @@ from .lynx import (  # noqa: F401
     Params,
     lynx_attn_merge,
     lynx_encode_tokens,
+    lynx_encode_variant,
+    lynx_reconstruct_variant,
+    lynx_decode_attn_int4,
     lynx_decode_attn,
     lynx_decode_attn_bf16,
     lynx_decode_attn_workspace_size,

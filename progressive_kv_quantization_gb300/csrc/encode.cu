@@ -101,7 +101,7 @@ struct QuantConsts {
 // exact_a(e) returns the correctly rounded magnitude of element e; the rule
 // compares it with the thresholds, while the estimate may start from a value
 // within a relative 2^-22 of it (the margin covers that).
-template <typename ExactA>
+template <int LEVELS = 127, typename ExactA>
 __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8],
                                           const float* __restrict__ s_thr, const QuantConsts& qc,
                                           ExactA exact_a) {
@@ -124,7 +124,7 @@ __device__ __forceinline__ void quantise8(const float2 (&a)[4], uint32_t (&ib)[8
     for (int e = 0; e < 8; ++e) {
       const float de = (e & 1) ? d[e >> 1].y : d[e >> 1].x;
       const float ae = exact_a(e);
-      const int I0 = min(max((int)(ib[e] - kMagicBits), 0), 127);
+      const int I0 = min(max((int)(ib[e] - kMagicBits), 0), LEVELS);
       const int j = I0 + (de > 0.0f ? 1 : 0);
       ib[e] = kMagicBits + (uint32_t)(j - 1 + (ae >= s_thr[j] ? 1 : 0));
     }
@@ -162,15 +162,22 @@ __device__ __forceinline__ void chunk_extremes(const uint32_t (&w)[16], int nc, 
   cmx = fmaxf(__low2float(bmx), __high2float(bmx));
 }
 
+// Output forms of the codes of a chunk
+enum CodeOut { kOutSplit = 0, kOutInt8 = 1, kOutInt4 = 2 };
+
 // Stages 1-4 of one channel chunk (32 tokens, w as in chunk_extremes), given
 // the row's gamma_min mn and maximum mx and the chunk's extremes cmn, cmx:
-// the packed anchor and residual words of the chunk (16 bytes each) and its
-// gamma_scale, mu and sigma.  PARTIAL: only the first nc tokens are valid
-// (statistics over them; padding gets code 0 with a positive sign).
-template <bool PARTIAL>
+// the chunk's codes and its gamma_scale, mu and sigma.  PARTIAL: only the
+// first nc tokens are valid (statistics over them; padding gets code 0 with a
+// positive sign).  OUT: kOutSplit -> out[0..3] the packed anchor words,
+// out[4..7] the packed residual words (16 bytes each); kOutInt8 -> out[0..7]
+// the 32 signed bytes S > 0 ? I : -I - 1 in token order; kOutInt4 -> out[0..3]
+// the sign-aware nibbles of the 7-level codes (qc, s_thr then describe 7
+// levels), two per byte, low nibble = even token.
+template <bool PARTIAL, int OUT = kOutSplit>
 __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, float mn, float mx, float cmn,
                                              float cmx, float eps, const float* __restrict__ s_thr,
-                                             const QuantConsts& qc, uint4& anc, uint4& res, float& gscale,
+                                             const QuantConsts& qc, uint32_t (&out)[8], float& gscale,
                                              float& mu, float& sigma) {
   // ---- Stage 1: x_n = (x - gamma_min) / (gamma_scale + eps)
   gscale = __fsub_rn(mx, mn);
@@ -209,7 +216,6 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
 
   // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
   // rounded floats, sign masks, then split and pack
-  uint32_t pa[4], pr[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t ib[8];
@@ -228,17 +234,25 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
       a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
     }
     // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
-    quantise8(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
+    quantise8<OUT == kOutInt4 ? 7 : 127>(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
     // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
     const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
     const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
-    // byte m of a packed word: token 2m in the low nibble, token 2m + 1 in the high nibble.
-    // anchor nibble (S>0 ? I : ~I) >> 4 = ((I >> 4) ^ S) & 15; residual (7 - I) mod 16 = (I ^ 7) & 15
-    pa[q] = (((Ie >> 4) ^ Se) & 0x0F0F0F0Fu) | ((Io ^ So) & 0xF0F0F0F0u);
-    pr[q] = ((Ie ^ 0x07070707u) & 0x0F0F0F0Fu) | (((Io << 4) ^ 0x70707070u) & 0xF0F0F0F0u);
+    if (OUT == kOutSplit) {
+      // byte m of a packed word: token 2m in the low nibble, token 2m + 1 in the high nibble.
+      // anchor nibble (S>0 ? I : ~I) >> 4 = ((I >> 4) ^ S) & 15; residual (7 - I) mod 16 = (I ^ 7) & 15
+      out[q] = (((Ie >> 4) ^ Se) & 0x0F0F0F0Fu) | ((Io ^ So) & 0xF0F0F0F0u);
+      out[4 + q] = ((Ie ^ 0x07070707u) & 0x0F0F0F0Fu) | (((Io << 4) ^ 0x70707070u) & 0xF0F0F0F0u);
+    } else if (OUT == kOutInt8) {
+      // S > 0 ? I : ~I per byte, even and odd tokens interleaved back into token order
+      const uint32_t e8 = Ie ^ Se, o8 = Io ^ So;
+      out[2 * q] = prmt(e8, o8, 0x5140u);
+      out[2 * q + 1] = prmt(e8, o8, 0x7362u);
+    } else {
+      // 7-level code I4 in 0..7: (S>0 ? I4 : ~I4) & 15, the 4-bit two's complement of S>0 ? I4 : -I4 - 1
+      out[q] = ((Ie ^ Se) & 0x0F0F0F0Fu) | (((Io ^ So) << 4) & 0xF0F0F0F0u);
+    }
   }
-  anc = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-  res = make_uint4(pr[0], pr[1], pr[2], pr[3]);
 }
 
 // PARTIAL: valid[page] (clamped to 0..256) tokens of each page are valid; the
@@ -295,11 +309,11 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
       mx = 0.0f;
     }
 
-    uint4 anc, res;
+    uint32_t o[8];
     float gscale, mu, sigma;
-    encode_chunk<PARTIAL>(w, nc, mn, mx, cmn, cmx, eps, s_thr, qc, anc, res, gscale, mu, sigma);
-    anchor[g * 32 + lane] = anc;
-    residual[g * 32 + lane] = res;
+    encode_chunk<PARTIAL>(w, nc, mn, mx, cmn, cmx, eps, s_thr, qc, o, gscale, mu, sigma);
+    anchor[g * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    residual[g * 32 + lane] = make_uint4(o[4], o[5], o[6], o[7]);
 
     const int64_t page = g >> 5;
     const int rgrp = (int)(g & 31);
@@ -378,11 +392,11 @@ encode_tokens_kernel(const uint16_t* __restrict__ x, int64_t n_tokens, int n_hea
         mx = fmaxf(mx, s_mx[buf][k][lane]);
       }
 
-      uint4 anc, res;
+      uint32_t o[8];
       float gscale, mu, sigma;
-      encode_chunk<PARTIAL>(wv, nc, mn, mx, cmn, cmx, eps, s_thr, qc, anc, res, gscale, mu, sigma);
-      anchor[(page * kH + c) * 8 + w] = anc;
-      residual[(page * kH + c) * 8 + w] = res;
+      encode_chunk<PARTIAL>(wv, nc, mn, mx, cmn, cmx, eps, s_thr, qc, o, gscale, mu, sigma);
+      anchor[(page * kH + c) * 8 + w] = make_uint4(o[0], o[1], o[2], o[3]);
+      residual[(page * kH + c) * 8 + w] = make_uint4(o[4], o[5], o[6], o[7]);
       float* mp = meta + page * kMetaFloats;
       if (w == 0) {
         mp[c] = mn;
@@ -390,6 +404,132 @@ encode_tokens_kernel(const uint16_t* __restrict__ x, int64_t n_tokens, int n_hea
       }
       mp[kMetaMuOff + w * kH + c] = mu;
       mp[kMetaSigmaOff + w * kH + c] = sigma;
+    }
+  }
+}
+
+// Single-precision Lynx variants (the paper's §6.1 "Lynx-INT8" / "Lynx-INT4":
+// Algorithm 1 at one precision, no split stream), full pages, with the work
+// mapping of encode_kernel.  OUT = kOutInt8: one signed byte per token
+// (S > 0 ? I : -I - 1), 256 bytes per channel row; kOutInt4: Stage 3 with 7
+// levels (tab describes them), the sign-aware nibble per token, 128 bytes per
+// row.  The metadata is Lynx's.
+template <int OUT>
+__global__ void __launch_bounds__(256, 2)
+encode_variant_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__ codes,
+                      float* __restrict__ meta, const EncodeTables tab) {
+  __shared__ float s_thr[129];
+  for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const float eps = tab.eps;
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
+  for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < n_groups; g += n_warps) {
+    uint4 raw[4];
+    load_chunk(x + g * 128 + lane * 4, raw);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[4 * k] = raw[k].x;
+      w[4 * k + 1] = raw[k].y;
+      w[4 * k + 2] = raw[k].z;
+      w[4 * k + 3] = raw[k].w;
+    }
+    float cmn, cmx;
+    chunk_extremes<false>(w, 32, cmn, cmx);
+    float mn = cmn, mx = cmx;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    uint32_t o[8];
+    float gscale, mu, sigma;
+    encode_chunk<false, OUT>(w, 32, mn, mx, cmn, cmx, eps, s_thr, qc, o, gscale, mu, sigma);
+    if (OUT == kOutInt8) {   // row group g: 4 rows of 256 bytes; lane = chunk (lane & 7) of row (lane >> 3)
+      codes[g * 64 + 2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      codes[g * 64 + 2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      codes[g * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const int64_t page = g >> 5;
+    float* mp = meta + page * kMetaFloats;
+    const int ch = 4 * (int)(g & 31) + (lane >> 3);
+    if ((lane & 7) == 0) {
+      mp[ch] = mn;
+      mp[kH + ch] = gscale;
+    }
+    mp[kMetaMuOff + (lane & 7) * kH + ch] = mu;
+    mp[kMetaSigmaOff + (lane & 7) * kH + ch] = sigma;
+  }
+}
+
+// Uniform INT-b per channel row of a page (the baseline of the paper's §2.3 and
+// §6.1): S = RN((max - min) / (2^b - 1)), Q = rint(RN((x - min) / S)) clamped to
+// 0 .. 2^b - 1 (Q = 0 when S = 0), each division correctly rounded (reciprocal
+// and one FMA correction step).  Codes: BITS = 8 one byte per token (256 bytes
+// per row), BITS = 4 two per byte, low nibble = even token; meta[page] =
+// min[128], scale[128].  Work mapping of encode_kernel.
+template <int BITS>
+__global__ void __launch_bounds__(256)
+uniform_encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__ codes,
+                      float* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const float levels = (float)((1 << BITS) - 1);
+  for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < n_groups; g += n_warps) {
+    uint4 raw[4];
+    load_chunk(x + g * 128 + lane * 4, raw);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[4 * k] = raw[k].x;
+      w[4 * k + 1] = raw[k].y;
+      w[4 * k + 2] = raw[k].z;
+      w[4 * k + 3] = raw[k].w;
+    }
+    float mn, mx;
+    chunk_extremes<false>(w, 32, mn, mx);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
+    const float rs = __frcp_rn(sc);
+    const float2 nmn2 = f2(-mn), nsc2 = f2(-sc), rs2 = f2(rs);
+    uint32_t q[32];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+      const float2 tq = div2(__fadd2_rn(v, nmn2), nsc2, rs2);
+      q[2 * t] = sc > 0.0f ? (uint32_t)min(max(__float2int_rn(tq.x), 0), (1 << BITS) - 1) : 0u;
+      q[2 * t + 1] = sc > 0.0f ? (uint32_t)min(max(__float2int_rn(tq.y), 0), (1 << BITS) - 1) : 0u;
+    }
+    if (BITS == 8) {
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        o[k] = q[4 * k] | (q[4 * k + 1] << 8) | (q[4 * k + 2] << 16) | (q[4 * k + 3] << 24);
+      codes[g * 64 + 2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      codes[g * 64 + 2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t wd = 0u;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) wd |= q[8 * k + b] << (4 * b);
+        o[k] = wd;
+      }
+      codes[g * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if ((lane & 7) == 0) {
+      const int64_t page = g >> 5;
+      const int ch = 4 * (int)(g & 31) + (lane >> 3);
+      meta[page * 256 + ch] = mn;
+      meta[page * 256 + kH + ch] = sc;
     }
   }
 }
@@ -475,6 +615,42 @@ cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, i
                                          tab, s);
   if (e != cudaSuccess || n_full == n_pp) return e;
   return launch_tokens_t<true>(x, n_tokens, n_heads, n_pp, n_full, 1, stride, anchor, residual, meta, tab, s);
+}
+
+cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, uint8_t* codes, float* meta,
+                                  const EncodeTables* tab, cudaStream_t s) {
+  const int64_t n_groups = n_pages * 32;
+  const int64_t need = (n_groups + 7) / 8;
+  const auto* xp = static_cast<const uint4*>(x);
+  auto* cp = reinterpret_cast<uint4*>(codes);
+  int per_sm = 0;
+  switch (variant) {
+    case kVariantLynxInt8:
+    case kVariantLynxInt4: {
+      const bool i8 = variant == kVariantLynxInt8;
+      if (i8) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_variant_kernel<kOutInt8>, 256, 0);
+      else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_variant_kernel<kOutInt4>, 256, 0);
+      const int64_t cap = (int64_t)device_sm_count() * (per_sm < 1 ? 1 : per_sm);
+      const int blocks = (int)(need < cap ? need : cap);
+      if (i8) encode_variant_kernel<kOutInt8><<<blocks, 256, 0, s>>>(xp, n_groups, cp, meta, *tab);
+      else encode_variant_kernel<kOutInt4><<<blocks, 256, 0, s>>>(xp, n_groups, cp, meta, *tab);
+      break;
+    }
+    case kVariantUniformInt8:
+    case kVariantUniformInt4: {
+      const bool i8 = variant == kVariantUniformInt8;
+      if (i8) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, uniform_encode_kernel<8>, 256, 0);
+      else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, uniform_encode_kernel<4>, 256, 0);
+      const int64_t cap = (int64_t)device_sm_count() * (per_sm < 1 ? 1 : per_sm);
+      const int blocks = (int)(need < cap ? need : cap);
+      if (i8) uniform_encode_kernel<8><<<blocks, 256, 0, s>>>(xp, n_groups, cp, meta);
+      else uniform_encode_kernel<4><<<blocks, 256, 0, s>>>(xp, n_groups, cp, meta);
+      break;
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,

@@ -45,6 +45,30 @@ int check_params(const lynx_params_t* p) {
 double ell(double y, double alpha) {  // inverse compander ((1+alpha)^(y/127) - 1)/alpha
   return expm1(y / 127.0 * log1p(alpha)) / alpha;
 }
+double ell4(double y, double alpha) {  // the same for 7 levels ((1+alpha)^(y/7) - 1)/alpha
+  return expm1(y / 7.0 * log1p(alpha)) / alpha;
+}
+
+// smallest float32 >= x
+float round_up_f32(double x) {
+  float f = (float)x;
+  if ((double)f < x) f = nextafterf(f, INFINITY);
+  return f;
+}
+
+// Margin around a rounding edge inside which the code is decided from the
+// table, for an estimate c * log2(1 + alpha a).  The hardware log2's absolute
+// error on [1, 2^20) stays below 2^-21 * max(1, log2(t)) (measured over every
+// float32 t in that range: at most 2^-22.5 below 4, 2^-20.9 below 256, 2^-19
+// below 2^20); the rounding of 1 + alpha a, of c and of the product add at most
+// c * 1e-7 + 1.6e-5; a magnitude estimate within a relative 2^-22 of the exact
+// one (the encoder's a = RN(x RN(1/d))) moves the estimate by at most
+// c 2^-22 / ln 2 < c * 3.5e-7.  The margin is twice the sum.
+float rounding_edge(double c, double alpha) {
+  const double L = log2(1.0 + alpha);
+  const double err = c * (ldexp(1.0, -21) * (L > 1.0 ? L : 1.0) + 1e-7 + 3.5e-7) + 1.6e-5;
+  return (float)(0.5 - 2.0 * err);
+}
 
 __device__ int g_status;   // per-device error word set by kernels that give up a wait
 
@@ -66,29 +90,31 @@ const EncodeTables* encode_tables(float alpha, float eps) {
   if (alpha == cached_alpha && eps == cached_eps) return &tab;
   const double a = alpha;
   tab.thr[0] = 0.0f;
-  for (int k = 1; k <= 127; ++k) {
-    const double x = ell(k - 0.5, a);      // exact edge between codes k-1 and k
-    float f = (float)x;
-    if ((double)f < x) f = nextafterf(f, INFINITY);
-    tab.thr[k] = f;
-  }
+  for (int k = 1; k <= 127; ++k) tab.thr[k] = round_up_f32(ell(k - 0.5, a));   // edge between codes k-1, k
   tab.thr[128] = INFINITY;
   const double c = 127.0 / log2(1.0 + a);
   tab.c_lg2 = (float)c;
   tab.alpha = alpha;
   tab.eps = eps;
-  // Margin around a rounding edge inside which the code is decided from the
-  // table.  The estimate c * log2(1 + alpha a) uses the hardware log2, whose
-  // absolute error on [1, 2^20) stays below 2^-21 * max(1, log2(t)) (measured
-  // over every float32 t in that range: at most 2^-22.5 below 4, 2^-20.9 below
-  // 256, 2^-19 below 2^20); the rounding of 1 + alpha a, of c and of the
-  // product add at most c * 1e-7 + 1.6e-5; a magnitude estimate within a
-  // relative 2^-22 of the exact one (the encoder's a = RN(x RN(1/d))) moves
-  // the estimate by at most c 2^-22 / ln 2 < c * 3.5e-7.  The margin is twice
-  // the sum.
-  const double L = log2(1.0 + a);
-  const double err = c * (ldexp(1.0, -21) * (L > 1.0 ? L : 1.0) + 1e-7 + 3.5e-7) + 1.6e-5;
-  tab.edge = (float)(0.5 - 2.0 * err);
+  tab.edge = rounding_edge(c, a);
+  cached_alpha = alpha;
+  cached_eps = eps;
+  return &tab;
+}
+
+const EncodeTables* encode_tables4(float alpha, float eps) {
+  thread_local EncodeTables tab;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  if (alpha == cached_alpha && eps == cached_eps) return &tab;
+  const double a = alpha;
+  tab.thr[0] = 0.0f;
+  for (int k = 1; k <= 7; ++k) tab.thr[k] = round_up_f32(ell4(k - 0.5, a));
+  for (int k = 8; k <= 128; ++k) tab.thr[k] = INFINITY;
+  const double c = 7.0 / log2(1.0 + a);
+  tab.c_lg2 = (float)c;
+  tab.alpha = alpha;
+  tab.eps = eps;
+  tab.edge = rounding_edge(c, a);
   cached_alpha = alpha;
   cached_eps = eps;
   return &tab;
@@ -115,6 +141,45 @@ const LutTables* lut_tables(float alpha, float eps) {
   }
   for (int byte = 0; byte < 256; ++byte)
     lut.anc_pair[byte] = make_float2(lut.anc16[byte & 15], lut.anc16[byte >> 4]);
+  lut.eps = eps;
+  cached_alpha = alpha;
+  cached_eps = eps;
+  return &lut;
+}
+
+const LutTables* lut_tables4(float alpha, float eps) {
+  thread_local LutTables lut;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  if (alpha == cached_alpha && eps == cached_eps) return &lut;
+  const double a = alpha;
+  for (int n = 0; n < 16; ++n) {
+    const int q = n >= 8 ? n - 16 : n;           // sign-aware nibble S > 0 ? I4 : -I4 - 1
+    const int S = q < 0 ? -1 : 1;
+    const int I4 = S > 0 ? q : -q - 1;
+    lut.anc16[n] = (float)(S * ell4(I4, a));
+  }
+  for (int c = 0; c < 256; ++c) lut.full[c] = 0.0f;
+  for (int byte = 0; byte < 256; ++byte)
+    lut.anc_pair[byte] = make_float2(lut.anc16[byte & 15], lut.anc16[byte >> 4]);
+  lut.eps = eps;
+  cached_alpha = alpha;
+  cached_eps = eps;
+  return &lut;
+}
+
+const LutTables* lut_tables8(float alpha, float eps) {
+  thread_local LutTables lut;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  if (alpha == cached_alpha && eps == cached_eps) return &lut;
+  const double a = alpha;
+  for (int b = 0; b < 256; ++b) {
+    const int q = b >= 128 ? b - 256 : b;        // signed byte S > 0 ? I : -I - 1
+    const int S = q < 0 ? -1 : 1;
+    const int I = S > 0 ? q : -q - 1;
+    lut.full[b] = (float)(S * ell(I, a));
+  }
+  for (int n = 0; n < 16; ++n) lut.anc16[n] = 0.0f;
+  for (int byte = 0; byte < 256; ++byte) lut.anc_pair[byte] = make_float2(0.0f, 0.0f);
   lut.eps = eps;
   cached_alpha = alpha;
   cached_eps = eps;
@@ -294,7 +359,8 @@ int check_decode_shape(int B, int T, int Hq, int Hkv, int head_dim, int max_page
 int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, int Hkv,
                   int head_dim, int64_t n_pool, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, float sm_scale, int causal, float* out, float* lse,
-                  void* workspace, size_t ws_bytes, float alpha, float eps, void* stream) {
+                  void* workspace, size_t ws_bytes, float alpha, float eps, void* stream,
+                  bool int4 = false) {
   int st = check_decode_shape(B, T, Hq, Hkv, head_dim, max_pages);
   if (st != LYNX_OK) return st;
   if (!q || !page_table || !ctx_len || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
@@ -331,7 +397,7 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.causal = causal;
   a.eps = eps;
-  const LutTables* lut = lut_tables(alpha, eps);
+  const LutTables* lut = int4 ? lut_tables4(alpha, eps) : lut_tables(alpha, eps);
   cudaError_t e = launch_decode(a, mode, lut, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_decode_attn launch");
   return LYNX_OK;
@@ -378,6 +444,79 @@ int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head
   return decode_common(a, mode, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table,
                        max_pages, ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes,
                        params->alpha, params->eps, stream);
+}
+
+int lynx_decode_attn_int4(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
+                          const uint8_t* k_codes, const float* k_meta, const uint8_t* v_codes,
+                          const float* v_meta, int64_t n_pool_pages, const int32_t* page_table, int max_pages,
+                          const int32_t* ctx_len, const lynx_params_t* params, float sm_scale, int causal,
+                          float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (!k_codes || !k_meta || !v_codes || !v_meta) return fail(LYNX_ERR_INVALID_ARG, "NULL page pool");
+  if (misaligned(k_codes) || misaligned(k_meta) || misaligned(v_codes) || misaligned(v_meta))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.k_anc = k_codes;
+  a.k_meta = k_meta;
+  a.v_anc = v_codes;
+  a.v_meta = v_meta;
+  return decode_common(a, kModeAnchor, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table, max_pages,
+                       ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes, params->alpha,
+                       params->eps, stream, true);
+}
+
+int lynx_encode_variant(const void* x_bf16, int64_t n_pages, int variant, const lynx_params_t* params,
+                        uint8_t* codes, float* meta, void* stream) {
+  g_last_error[0] = '\0';
+  if (variant < LYNX_VARIANT_LYNX_INT8 || variant > LYNX_VARIANT_UNIFORM_INT4)
+    return fail(LYNX_ERR_INVALID_ARG, "variant=%d", variant);
+  const bool lynx_kind = variant == LYNX_VARIANT_LYNX_INT8 || variant == LYNX_VARIANT_LYNX_INT4;
+  if (lynx_kind) {
+    int st = check_params(params);
+    if (st != LYNX_OK) return st;
+  }
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!x_bf16 || !codes || !meta) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(x_bf16) || misaligned(codes) || misaligned(meta))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  const EncodeTables* tab = nullptr;
+  if (variant == LYNX_VARIANT_LYNX_INT8) tab = encode_tables(params->alpha, params->eps);
+  if (variant == LYNX_VARIANT_LYNX_INT4) tab = encode_tables4(params->alpha, params->eps);
+  cudaError_t e = launch_encode_variant(x_bf16, n_pages, variant, codes, meta, tab,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_variant launch");
+  return LYNX_OK;
+}
+
+int lynx_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
+                             const lynx_params_t* params, void* out, int out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (variant < LYNX_VARIANT_LYNX_INT8 || variant > LYNX_VARIANT_UNIFORM_INT4)
+    return fail(LYNX_ERR_INVALID_ARG, "variant=%d", variant);
+  const bool lynx_kind = variant == LYNX_VARIANT_LYNX_INT8 || variant == LYNX_VARIANT_LYNX_INT4;
+  if (lynx_kind) {
+    int st = check_params(params);
+    if (st != LYNX_OK) return st;
+  }
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_F32)
+    return fail(LYNX_ERR_INVALID_ARG, "out_dtype=%d (need 0 = BF16 or 1 = F32)", out_dtype);
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!codes || !meta || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(codes) || misaligned(meta) || misaligned(out))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  const LutTables* lut = nullptr;
+  if (variant == LYNX_VARIANT_LYNX_INT8) lut = lut_tables8(params->alpha, params->eps);
+  if (variant == LYNX_VARIANT_LYNX_INT4) lut = lut_tables4(params->alpha, params->eps);
+  cudaError_t e = launch_reconstruct_variant(codes, meta, n_pages, variant, out, out_dtype, lut,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct_variant launch");
+  return LYNX_OK;
 }
 
 int lynx_attn_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,

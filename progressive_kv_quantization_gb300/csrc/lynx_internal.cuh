@@ -43,6 +43,15 @@ struct LutTables {
 
 const EncodeTables* encode_tables(float alpha, float eps);
 const LutTables* lut_tables(float alpha, float eps);
+// the same for the 7-level Lynx-INT4 codes (thr[0..8]; anc16 / anc_pair hold
+// S * l4(I4) of the sign-aware nibble) and for Lynx-INT8 bytes (full[byte] =
+// S * l(I) of the signed byte S > 0 ? I : -I - 1)
+const EncodeTables* encode_tables4(float alpha, float eps);
+const LutTables* lut_tables4(float alpha, float eps);
+const LutTables* lut_tables8(float alpha, float eps);
+
+// single-precision variants (values of lynx.h's LYNX_VARIANT_*)
+enum Variant { kVariantLynxInt8 = 1, kVariantLynxInt4 = 2, kVariantUniformInt8 = 3, kVariantUniformInt4 = 4 };
 
 int device_sm_count();
 int set_error(int status, const char* message);   // records lynx_last_error(), returns status
@@ -51,6 +60,10 @@ int* device_status_ptr();   // device address of this device's error word
 // Launchers (one per kernel family).  Return cudaGetLastError() of the launch.
 cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,
                           float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s);
+cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, uint8_t* codes, float* meta,
+                                  const EncodeTables* tab, cudaStream_t s);
+cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
+                                       void* out, int out_dtype, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
                                  uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
                                  cudaStream_t s);

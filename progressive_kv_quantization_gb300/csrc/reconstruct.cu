@@ -21,11 +21,16 @@
 namespace lynx {
 namespace {
 
-template <bool kFull, bool kF32>
+// kMode: 0 = Anchor plane alone (16-entry table anc16), 1 = Anchor + Residual
+// planes (256-entry table full, code = anchor nibble | residual nibble << 4),
+// 2 = one byte per token (Lynx-INT8; 256-entry table full indexed by the byte,
+// `anchor` points at the 256-byte rows).
+template <int kMode, bool kF32>
 __global__ void __launch_bounds__(256)
 reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restrict__ residual,
                    const float* __restrict__ meta, int64_t n_groups, void* __restrict__ out,
                    const LutTables lut) {
+  constexpr bool kFull = kMode != 0;
   constexpr int kEntries = kFull ? 256 : 16;
   __shared__ float s_lut[kEntries * 32];
   __shared__ float s_meta[2][4][128];      // [buffer][gmin, gscale, mu, sigma][chunk * 16 + row]
@@ -63,8 +68,13 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int64_t row = 16 * o + w + 8 * h;
-      wa_n[h] = __ldg(anchor + row * 32 + lane);
-      if (kFull) wr_n[h] = __ldg(residual + row * 32 + lane);
+      if (kMode == 2) {   // tokens 8L .. 8L+3 and 8L+4 .. 8L+7
+        wa_n[h] = __ldg(anchor + row * 64 + 2 * lane);
+        wr_n[h] = __ldg(anchor + row * 64 + 2 * lane + 1);
+      } else {
+        wa_n[h] = __ldg(anchor + row * 32 + lane);
+        if (kFull) wr_n[h] = __ldg(residual + row * 32 + lane);
+      }
     }
   }
   __syncthreads();
@@ -78,8 +88,13 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int64_t row = 16 * on + w + 8 * h;
-        wa_n[h] = __ldg(anchor + row * 32 + lane);
-        if (kFull) wr_n[h] = __ldg(residual + row * 32 + lane);
+        if (kMode == 2) {
+          wa_n[h] = __ldg(anchor + row * 64 + 2 * lane);
+          wr_n[h] = __ldg(anchor + row * 64 + 2 * lane + 1);
+        } else {
+          wa_n[h] = __ldg(anchor + row * 32 + lane);
+          if (kFull) wr_n[h] = __ldg(residual + row * 32 + lane);
+        }
       }
     }
     const int blk = lane >> 2;
@@ -96,10 +111,18 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
       float2 xv[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint32_t c0 = (wa[h] >> (8 * k)) & 0xFu, c1 = (wa[h] >> (8 * k + 4)) & 0xFu;
-        if (kFull) {
-          c0 |= ((wr[h] >> (8 * k)) & 0xFu) << 4;
-          c1 |= ((wr[h] >> (8 * k + 4)) & 0xFu) << 4;
+        uint32_t c0, c1;
+        if (kMode == 2) {   // tokens 2k, 2k + 1: bytes of the two words in token order
+          const uint32_t wd = k < 2 ? wa[h] : wr[h];
+          c0 = (wd >> (16 * (k & 1))) & 0xFFu;
+          c1 = (wd >> (16 * (k & 1) + 8)) & 0xFFu;
+        } else {
+          c0 = (wa[h] >> (8 * k)) & 0xFu;
+          c1 = (wa[h] >> (8 * k + 4)) & 0xFu;
+          if (kFull) {
+            c0 |= ((wr[h] >> (8 * k)) & 0xFu) << 4;
+            c1 |= ((wr[h] >> (8 * k + 4)) & 0xFu) << 4;
+          }
         }
         const float2 l = make_float2(lut_lane[c0 * 32], lut_lane[c1 * 32]);
         xv[k] = __ffma2_rn(__ffma2_rn(l, ds2, mu2), dg2, gm2);
@@ -123,17 +146,62 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
   }
 }
 
-template <bool kFull, bool kF32>
+// Uniform INT-b codes (min[128], scale[128] per page): x = fmaf(Q, scale, min).
+// One thread per 8 tokens of a row (grid-stride).
+template <int BITS, bool kF32>
+__global__ void __launch_bounds__(256)
+uniform_reconstruct_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ meta, int64_t n_rows,
+                           void* __restrict__ out) {
+  const int64_t n_items = n_rows * 32;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_items; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i >> 5;
+    const int part = (int)(i & 31);
+    const float* mp = meta + (row >> 7) * 256;
+    const int ch = (int)(row & 127);
+    const float mn = __ldg(mp + ch), sc = __ldg(mp + kH + ch);
+    uint32_t q[8];
+    if (BITS == 8) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(codes + row * 256) + part);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        q[k] = (v.x >> (8 * k)) & 0xFFu;
+        q[4 + k] = (v.y >> (8 * k)) & 0xFFu;
+      }
+    } else {
+      const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(codes + row * 128) + part);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) q[k] = (v >> (4 * k)) & 0xFu;
+    }
+    float x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = __fmaf_rn((float)q[k], sc, mn);
+    if (kF32) {
+      float4* op = reinterpret_cast<float4*>(out) + row * 64 + part * 2;
+      op[0] = make_float4(x[0], x[1], x[2], x[3]);
+      op[1] = make_float4(x[4], x[5], x[6], x[7]);
+    } else {
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+        pk[k] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      reinterpret_cast<uint4*>(out)[row * 32 + part] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+}
+
+template <int kMode, bool kF32>
 cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                    int64_t n_pages, void* out, const LutTables* lut, cudaStream_t s) {
   const int64_t n_groups = n_pages * (kH / 16);
   const int threads = 256;
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_kernel<kFull, kF32>, threads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_kernel<kMode, kF32>, threads, 0);
   if (per_sm < 1) per_sm = 1;
   const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
   const int blocks = (int)(n_groups < max_blocks ? n_groups : max_blocks);
-  reconstruct_kernel<kFull, kF32><<<blocks, threads, 0, s>>>(
+  reconstruct_kernel<kMode, kF32><<<blocks, threads, 0, s>>>(
       reinterpret_cast<const uint32_t*>(anchor), reinterpret_cast<const uint32_t*>(residual), meta,
       n_groups, out, *lut);
   return cudaGetLastError();
@@ -147,11 +215,41 @@ cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, c
   const bool full = residual != nullptr;
   const bool f32 = out_dtype == LYNX_OUT_F32;
   if (full) {
-    return f32 ? launch<true, true>(anchor, residual, meta, n_pages, out, lut, s)
-               : launch<true, false>(anchor, residual, meta, n_pages, out, lut, s);
+    return f32 ? launch<1, true>(anchor, residual, meta, n_pages, out, lut, s)
+               : launch<1, false>(anchor, residual, meta, n_pages, out, lut, s);
   }
-  return f32 ? launch<false, true>(anchor, residual, meta, n_pages, out, lut, s)
-             : launch<false, false>(anchor, residual, meta, n_pages, out, lut, s);
+  return f32 ? launch<0, true>(anchor, residual, meta, n_pages, out, lut, s)
+             : launch<0, false>(anchor, residual, meta, n_pages, out, lut, s);
+}
+
+cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
+                                       void* out, int out_dtype, const LutTables* lut, cudaStream_t s) {
+  const bool f32 = out_dtype == LYNX_OUT_F32;
+  switch (variant) {
+    case kVariantLynxInt8:
+      return f32 ? launch<2, true>(codes, nullptr, meta, n_pages, out, lut, s)
+                 : launch<2, false>(codes, nullptr, meta, n_pages, out, lut, s);
+    case kVariantLynxInt4:
+      return f32 ? launch<0, true>(codes, nullptr, meta, n_pages, out, lut, s)
+                 : launch<0, false>(codes, nullptr, meta, n_pages, out, lut, s);
+    case kVariantUniformInt8:
+    case kVariantUniformInt4: {
+      const int64_t n_rows = n_pages * kH;
+      const int64_t blocks_need = (n_rows * 32 + 255) / 256;
+      const int64_t cap = (int64_t)device_sm_count() * 8;
+      const int blocks = (int)(blocks_need < cap ? blocks_need : cap);
+      if (variant == kVariantUniformInt8) {
+        if (f32) uniform_reconstruct_kernel<8, true><<<blocks, 256, 0, s>>>(codes, meta, n_rows, out);
+        else uniform_reconstruct_kernel<8, false><<<blocks, 256, 0, s>>>(codes, meta, n_rows, out);
+      } else {
+        if (f32) uniform_reconstruct_kernel<4, true><<<blocks, 256, 0, s>>>(codes, meta, n_rows, out);
+        else uniform_reconstruct_kernel<4, false><<<blocks, 256, 0, s>>>(codes, meta, n_rows, out);
+      }
+      return cudaGetLastError();
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace lynx

@@ -63,6 +63,10 @@ SIGNATURES = {
     "lynx_decode_attn_noalloc": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                         _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP]),
     "lynx_attn_merge": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]),
+    "lynx_encode_variant": (_I32, [_VP, _I64, _I32, _PP, _VP, _VP, _VP]),
+    "lynx_reconstruct_variant": (_I32, [_VP, _VP, _I64, _I32, _PP, _VP, _I32, _VP]),
+    "lynx_decode_attn_int4": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _I64, _VP, _I32,
+                                     _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "lynx_decode_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lynx_device_status": (_I32, []),
     "lynx_status_string": (ctypes.c_char_p, [_I32]),
@@ -207,6 +211,60 @@ def lynx_reconstruct(anchor, residual, meta, params: Params = Params(), out=None
     return out
 
 
+# single-precision variants (paper §6.1): name -> (LYNX_VARIANT_* value, code bytes per page, meta floats per page)
+VARIANTS = {
+    "lynx_int8": (1, H * P, META_FLOATS),
+    "lynx_int4": (2, H * P // 2, META_FLOATS),
+    "uniform_int8": (3, H * P, 2 * H),
+    "uniform_int4": (4, H * P // 2, 2 * H),
+}
+
+
+def lynx_encode_variant(x, variant: str, params: Params = Params(), codes=None, meta=None, stream=None):
+    """BF16 pages x[N, 128, 256] -> (codes u8[N, code bytes per page], meta f32[N, meta floats])
+    of a single-precision variant: "lynx_int8", "lynx_int4", "uniform_int8" or
+    "uniform_int4" (layouts in lynx.h)."""
+    if variant not in VARIANTS:
+        raise LynxError(f"unknown variant {variant!r}")
+    code, cb, mf = VARIANTS[variant]
+    _need(x, torch.bfloat16, "x")
+    n = x.numel() // (H * P)
+    if x.numel() != n * H * P:
+        raise LynxError("x must hold whole 128 x 256 pages")
+    codes = codes if codes is not None else torch.empty((n, cb), dtype=torch.uint8, device=x.device)
+    meta = meta if meta is not None else torch.empty((n, mf), dtype=torch.float32, device=x.device)
+    _need(codes, torch.uint8, "codes")
+    _need(meta, torch.float32, "meta")
+    if codes.numel() < n * cb or meta.numel() < n * mf:
+        raise LynxError("output buffers too small")
+    p = params.c()
+    _check(load().lynx_encode_variant(_ptr(x), n, code, ctypes.byref(p), _ptr(codes), _ptr(meta),
+                                      _stream(stream)), "lynx_encode_variant")
+    return codes, meta
+
+
+def lynx_reconstruct_variant(codes, meta, variant: str, params: Params = Params(), out=None,
+                             out_dtype=torch.bfloat16, stream=None):
+    """Dequantise a variant's codes and meta -> out[N, 128, 256]."""
+    if variant not in VARIANTS:
+        raise LynxError(f"unknown variant {variant!r}")
+    code, cb, mf = VARIANTS[variant]
+    _need(codes, torch.uint8, "codes")
+    _need(meta, torch.float32, "meta")
+    n = codes.numel() // cb
+    if meta.numel() < n * mf:
+        raise LynxError("meta too small")
+    oc = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}.get(out_dtype)
+    if oc is None:
+        raise LynxError("out_dtype must be torch.bfloat16 or torch.float32")
+    out = out if out is not None else torch.empty((n, H, P), dtype=out_dtype, device=codes.device)
+    _need(out, out_dtype, "out")
+    p = params.c()
+    _check(load().lynx_reconstruct_variant(_ptr(codes), _ptr(meta), n, code, ctypes.byref(p), _ptr(out), oc,
+                                           _stream(stream)), "lynx_reconstruct_variant")
+    return out
+
+
 def lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages) -> int:
     return int(load().lynx_decode_attn_workspace_size(B, T, Hq, Hkv, head_dim, max_pages))
 
@@ -261,6 +319,23 @@ def lynx_decode_attn(q, k_anc, k_res, k_meta, v_anc, v_res, v_meta, page_table, 
         _ptr(v_res), _ptr(v_meta), n_pool, _ptr(page_table), max_pages, _ptr(ctx_len),
         ctypes.byref(p), scale, int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "lynx_decode_attn")
+    return out, lse
+
+
+def lynx_decode_attn_int4(q, k_codes, k_meta, v_codes, v_meta, page_table, ctx_len, n_kv_heads,
+                          params: Params = Params(), sm_scale=None, causal=False, out=None, lse=None,
+                          workspace=None, stream=None):
+    """Attention of q over Lynx-INT4 page pools (lynx_encode_variant(..., "lynx_int4"))."""
+    B, T, Hq, D, max_pages, out, lse, workspace = _decode_prep(q, page_table, ctx_len, n_kv_heads,
+                                                               out, lse, workspace)
+    n_pool = _pool_pages(k_codes.view(-1, H, P // 2), None, k_meta, v_codes.view(-1, H, P // 2), None, v_meta)
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
+    p = params.c()
+    _check(load().lynx_decode_attn_int4(
+        _ptr(q), B, T, Hq, n_kv_heads, D, _ptr(k_codes), _ptr(k_meta), _ptr(v_codes), _ptr(v_meta), n_pool,
+        _ptr(page_table), max_pages, _ptr(ctx_len), ctypes.byref(p), scale, int(bool(causal)), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "lynx_decode_attn_int4")
     return out, lse
 
 

@@ -122,3 +122,22 @@ def test_token_major_encode_argument_checks(lynx_lib):
     assert lib.lynx_encode_tokens(a, 0, 2, 256, ok, None, None, None, None) == 0
     assert lib.lynx_encode_tokens(a, 300, 0, 0, ok, None, None, None, None) == 0
     assert lib.lynx_encode_tokens(a, 300, 2, 256, ctypes.byref(_p(alpha=0.0)), a, a, a, None) == -2
+
+
+def test_variant_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 4)
+    ok = ctypes.byref(_p())
+    for v in (0, 5):   # unknown variants
+        assert lib.lynx_encode_variant(a, 1, v, ok, a, a, None) == -1
+        assert lib.lynx_reconstruct_variant(a, a, 1, v, ok, a, 0, None) == -1
+    assert lib.lynx_encode_variant(a, -1, 3, ok, a, a, None) == -1
+    assert lib.lynx_encode_variant(odd, 1, 3, ok, a, a, None) == -3
+    assert lib.lynx_encode_variant(a, 0, 2, ok, None, None, None) == 0
+    assert lib.lynx_encode_variant(a, 1, 2, ctypes.byref(_p(alpha=0.0)), a, a, None) == -2
+    # uniform variants do not read params
+    assert lib.lynx_encode_variant(a, 0, 4, None, None, None, None) == 0
+    assert lib.lynx_reconstruct_variant(a, a, 1, 1, ok, a, 7, None) == -1
+    assert lib.lynx_reconstruct_variant(None, a, 1, 4, ok, a, 0, None) == -1
