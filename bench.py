@@ -342,6 +342,7 @@ def run_gpu(args, rank, world):
     e2e = run_e2e(torch, L, b, ks, args, dev) if rank == 0 and not args.no_e2e else None
     prog = run_progressive(torch, L, b, dev) if rank == 0 and not args.no_e2e else None
     tok = run_encode_tokens(torch, L, b) if rank == 0 and not args.no_e2e else None
+    cmp_ = run_comparators(torch, L, b, dev) if rank == 0 and not args.no_e2e else None
     if rank != 0:
         return None
     launches = args.steps * sum(k[2] for k in ks)
@@ -360,6 +361,7 @@ def run_gpu(args, rank, world):
         "e2e": e2e,
         "progressive": prog,
         "encode_tokens": tok,
+        "comparators": cmp_,
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -567,6 +569,92 @@ def run_encode_tokens(torch, L, b, reps=5):
             "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3), "identical_to_page_encode": same,
             "layout": f"[{N_TOK} tokens][{n_heads} x 128] BF16 (layer x K/V x KV head per row)",
             "statistic": f"median of {reps}"}
+
+
+def run_comparators(torch, L, b, dev, reps=3):
+    """The Table-3 analogue on the benchmark's synthetic cache: for Lynx (full
+    codes; anchor only, the draft), Lynx-INT8, Lynx-INT4 and uniform INT8 / INT4,
+    the KV vNMSE (mean over token vectors -- one head's 128 channels at one
+    token -- of ||x_hat - x||^2 / ||x||^2, from float32 reconstructions) and the
+    attention vNMSE (the B = 64, T = 1 decode's output rows against the same
+    decode over the BF16 pages; uniform codes through their BF16
+    reconstruction), with each variant's encode time (median of ``reps``
+    CUDA-event timings) and its bytes per KV value."""
+    p = L.Params()
+    x = b["x"]
+    n = x.shape[0]
+    chunk = 8192
+    gbps_peak, _ = peaks()
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts[1:])
+
+    def kv_vnmse(recon_f32):   # recon_f32(lo, hi, out) fills out with pages lo..hi in float32
+        tot, cnt = 0.0, 0
+        buf = torch.empty((chunk, 128, 256), dtype=torch.float32, device=dev)
+        for lo in range(0, n, chunk):
+            hi = min(lo + chunk, n)
+            recon_f32(lo, hi, buf[:hi - lo])
+            xf = x[lo:hi].float()
+            d = (buf[:hi - lo] - xf).pow(2).sum(dim=1) / xf.pow(2).sum(dim=1).clamp_min(1e-30)
+            tot += float(d.double().sum())
+            cnt += d.numel()
+        return tot / cnt
+
+    q, pt, ctx, ws = b["q1"], b["pt1"], b["ctx1"], b["ws1"]
+    kA, vA, kR, vR, kM, vM = b["anc"], b["anc"][PER:], b["res"], b["res"][PER:], b["meta"], b["meta"][PER:]
+    o_ref, _ = L.lynx_decode_attn_bf16(q, x, x[PER:], pt, ctx, HKV, workspace=ws)
+    o_ref = o_ref.clone()
+
+    def attn_vnmse(o):
+        a, r = o.double().reshape(-1, 128), o_ref.double().reshape(-1, 128)
+        return float(((a - r).pow(2).sum(dim=1) / r.pow(2).sum(dim=1)).mean())
+
+    rows = {}
+    # Lynx split stream (the step's encode output): full codes and the Anchor alone
+    t_enc = timed(lambda: L.lynx_encode_pages(x, p, kA, kR, kM))
+    full_o, _ = L.lynx_decode_attn(q, kA, kR, kM, vA, vR, vM, pt, ctx, HKV, p, workspace=ws)
+    rows["lynx_full"] = {"bytes_per_value": 1.0 + 9216 / 32768, "encode_ms": round(t_enc, 4),
+                         "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct(
+                             kA[lo:hi], kR[lo:hi], kM[lo:hi], p, out=o, out_dtype=torch.float32)),
+                         "attn_vnmse": attn_vnmse(full_o)}
+    anc_o, _ = L.lynx_decode_attn(q, kA, None, kM, vA, None, vM, pt, ctx, HKV, p, workspace=ws)
+    rows["lynx_anchor"] = {"bytes_per_value": 0.5 + 9216 / 32768, "encode_ms": round(t_enc, 4),
+                           "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct(
+                               kA[lo:hi], None, kM[lo:hi], p, out=o, out_dtype=torch.float32)),
+                           "attn_vnmse": attn_vnmse(anc_o)}
+    for name in ("lynx_int8", "lynx_int4", "uniform_int8", "uniform_int4"):
+        _, cb, mf = L.VARIANTS[name]
+        codes = torch.empty((n, cb), dtype=torch.uint8, device=dev)
+        meta = torch.empty((n, mf), dtype=torch.float32, device=dev)
+        t = timed(lambda: L.lynx_encode_variant(x, name, p, codes, meta))
+        ent = {"bytes_per_value": (cb + 4 * mf) / 32768, "encode_ms": round(t, 4),
+               "encode_frac_of_hbm": round((n * (PAGE + cb + 4 * mf)) / t / 1e6 / gbps_peak, 3),
+               "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct_variant(
+                   codes[lo:hi], meta[lo:hi], name, p, out=o, out_dtype=torch.float32))}
+        if name == "lynx_int4":
+            o4, _ = L.lynx_decode_attn_int4(q, codes, meta, codes[PER:], meta[PER:], pt, ctx, HKV, p, workspace=ws)
+            ent["attn_vnmse"] = attn_vnmse(o4)
+        else:
+            rec = L.lynx_reconstruct_variant(codes, meta, name, p)
+            o8, _ = L.lynx_decode_attn_bf16(q, rec, rec[PER:], pt, ctx, HKV, workspace=ws)
+            ent["attn_vnmse"] = attn_vnmse(o8)
+            del rec
+        rows[name] = ent
+        del codes, meta
+    for r in rows.values():
+        r["kv_vnmse"] = float(f"{r['kv_vnmse']:.4g}")
+        r["attn_vnmse"] = float(f"{r['attn_vnmse']:.4g}")
+    return {"rows": rows, "attention": "B=64, T=1 decode vs the same decode over the BF16 pages",
+            "kv": "token vectors of the 64-layer cache, float32 reconstructions"}
 
 
 # ------------------------------------------------------------------ oracle arm
