@@ -23,6 +23,8 @@
  *                         their log-sum-exps (the drafts' own uncompressed KV
  *                         joined to the verification over the packed cache).
  *   lynx_encode_tokens    Algorithm 1 reading token-major (paged-attention) KV.
+ *   lynx_encode_split, lynx_reconstruct_split
+ *                         the split stream at other Anchor / Residual widths.
  *   lynx_encode_variant, lynx_reconstruct_variant, lynx_decode_attn_int4
  *                         the single-precision comparators of §6.1 (uniform
  *                         INT8 / INT4, Lynx-INT8, Lynx-INT4).
@@ -163,6 +165,27 @@ int lynx_encode_pages(const void* x_bf16, int64_t n_pages, const lynx_params_t* 
 int lynx_encode_pages_partial(const void* x_bf16, int64_t n_pages, const int32_t* valid_tokens,
                               const lynx_params_t* params, uint8_t* anchor, uint8_t* residual,
                               float* meta, void* stream);
+
+/* The split stream at other widths: an A-bit Anchor (sign included) and an
+ * R = 8 - A bit Residual of Algorithm 1's 8-bit code, 2 <= A <= 6 (the paper's
+ * §8 leaves widths other than 4 + 4 to future work).  With q8 = S > 0 ? I :
+ * -I - 1 and V = I >> R:  Anchor = q8 >> R (arithmetic), Anchor-only index
+ * V 2^R + 2^(R-1) - 1, Residual = that index - I.  Planes: per channel row 8
+ * chunks, each a little-endian bit string of its 32 tokens' two's-complement
+ * codes (token t at bits A t .. A t + A - 1), so an Anchor row is 32 A bytes
+ * and a Residual row 32 R bytes ([n_pages][128][32 A] and [n_pages][128][32 R]);
+ * with A = 4 the planes are exactly those of lynx_encode_pages.  Metadata as
+ * lynx_encode_pages.  Errors as lynx_encode_pages; UNSUPPORTED for anchor_bits
+ * outside 2..6. */
+int lynx_encode_split(const void* x_bf16, int64_t n_pages, int anchor_bits, const lynx_params_t* params,
+                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream);
+
+/* Reconstruction of lynx_encode_split's planes (residual == NULL: Anchor only),
+ * into out as lynx_reconstruct does (the same float32 arithmetic; with A = 4 the
+ * same result).  Errors as lynx_reconstruct; UNSUPPORTED for anchor_bits outside
+ * 2..6. */
+int lynx_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
+                           int anchor_bits, const lynx_params_t* params, void* out, int out_dtype, void* stream);
 
 /* Encode BF16 pages [n_pages][128][256] (device, 16-byte aligned) into one of
  * the single-precision variants above; codes and meta are caller-allocated

@@ -12,6 +12,8 @@ from .lynx import (  # noqa: F401
     lynx_attn_merge,
     lynx_encode_tokens,
     lynx_encode_variant,
+    lynx_encode_split,
+    lynx_reconstruct_split,
     lynx_reconstruct_variant,
     lynx_decode_attn_int4,
     lynx_decode_attn,

@@ -162,8 +162,18 @@ __device__ __forceinline__ void chunk_extremes(const uint32_t (&w)[16], int nc, 
   cmx = fmaxf(__low2float(bmx), __high2float(bmx));
 }
 
-// Output forms of the codes of a chunk
-enum CodeOut { kOutSplit = 0, kOutInt8 = 1, kOutInt4 = 2 };
+// Output forms of the codes of a chunk; kOutSplitBits + A: the split stream
+// with an A-bit Anchor and an (8 - A)-bit Residual (2 <= A <= 6)
+enum CodeOut { kOutSplit = 0, kOutInt8 = 1, kOutInt4 = 2, kOutSplitBits = 10 };
+
+// OR a `bits`-wide code into a chunk's little-endian bit string held in words
+// w[0..], at bit position pos (compile-time after unrolling)
+template <int BITS>
+__device__ __forceinline__ void put_bits(uint32_t* w, int pos, uint32_t code) {
+  const int wi = pos >> 5, sh = pos & 31;
+  w[wi] |= code << sh;
+  if (sh + BITS > 32) w[wi + 1] |= code >> (32 - sh);
+}
 
 // Stages 1-4 of one channel chunk (32 tokens, w as in chunk_extremes), given
 // the row's gamma_min mn and maximum mx and the chunk's extremes cmn, cmx:
@@ -173,7 +183,11 @@ enum CodeOut { kOutSplit = 0, kOutInt8 = 1, kOutInt4 = 2 };
 // out[4..7] the packed residual words (16 bytes each); kOutInt8 -> out[0..7]
 // the 32 signed bytes S > 0 ? I : -I - 1 in token order; kOutInt4 -> out[0..3]
 // the sign-aware nibbles of the 7-level codes (qc, s_thr then describe 7
-// levels), two per byte, low nibble = even token.
+// levels), two per byte, low nibble = even token; kOutSplitBits + A ->
+// out[0..A-1] the chunk's A-bit Anchors as a little-endian bit string (token t
+// at bits A t ..), out[A..7] its (8 - A)-bit Residuals likewise: Anchor
+// = q8 >> R, Residual = V 2^R + 2^(R-1) - 1 - I with q8 = S > 0 ? I : -I - 1,
+// V = I >> R, R = 8 - A (the 4+4 form is the paper's split).
 template <bool PARTIAL, int OUT = kOutSplit>
 __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, float mn, float mx, float cmn,
                                              float cmx, float eps, const float* __restrict__ s_thr,
@@ -216,6 +230,10 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
 
   // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
   // rounded floats, sign masks, then split and pack
+  if (OUT >= kOutSplitBits) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = 0u;
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t ib[8];
@@ -235,6 +253,22 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
     }
     // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
     quantise8<OUT == kOutInt4 ? 7 : 127>(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
+    if (OUT >= kOutSplitBits) {
+      constexpr int A = OUT - kOutSplitBits, R = 8 - A;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = 8 * q + e;
+        const uint32_t I = ib[e] & 0xFFu;
+        const bool neg = __float_as_uint(xs[e]) >> 31;
+        const uint32_t q8 = neg ? (~I & 0xFFu) : I;
+        const uint32_t anc = (uint32_t)(((int32_t)(q8 << 24) >> (24 + R)) & ((1 << A) - 1));
+        const uint32_t ihat = ((I >> R) << R) + (1u << (R - 1)) - 1u;
+        const uint32_t res = (ihat - I) & ((1u << R) - 1u);
+        put_bits<A>(out, A * t, anc);
+        put_bits<R>(out + A, R * t, res);
+      }
+      continue;
+    }
     // codes I (0..127) and sign bytes S of the even tokens 0, 2, 4, 6 and odd tokens 1, 3, 5, 7
     const uint32_t Ie = gather4(ib[0], ib[2], ib[4], ib[6]), Io = gather4(ib[1], ib[3], ib[5], ib[7]);
     const uint32_t Se = signs4(xs[0], xs[2], xs[4], xs[6]), So = signs4(xs[1], xs[3], xs[5], xs[7]);
@@ -465,6 +499,61 @@ encode_variant_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __re
   }
 }
 
+// The split stream with an A-bit Anchor (2 <= A <= 6), full pages, work mapping
+// of encode_kernel: a channel row of the Anchor plane holds 8 chunks x 4A
+// bytes, of the Residual plane 8 x 4(8 - A); lane = chunk (lane & 7) of row
+// (lane >> 3) of the warp's row group.
+template <int A>
+__global__ void __launch_bounds__(256, 2)
+encode_split_kernel(const uint4* __restrict__ x, int64_t n_groups, uint32_t* __restrict__ anchor,
+                    uint32_t* __restrict__ residual, float* __restrict__ meta, const EncodeTables tab) {
+  constexpr int R = 8 - A;
+  __shared__ float s_thr[129];
+  for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const float eps = tab.eps;
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
+  for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < n_groups; g += n_warps) {
+    uint4 raw[4];
+    load_chunk(x + g * 128 + lane * 4, raw);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[4 * k] = raw[k].x;
+      w[4 * k + 1] = raw[k].y;
+      w[4 * k + 2] = raw[k].z;
+      w[4 * k + 3] = raw[k].w;
+    }
+    float cmn, cmx;
+    chunk_extremes<false>(w, 32, cmn, cmx);
+    float mn = cmn, mx = cmx;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    uint32_t o[8];
+    float gscale, mu, sigma;
+    encode_chunk<false, kOutSplitBits + A>(w, 32, mn, mx, cmn, cmx, eps, s_thr, qc, o, gscale, mu, sigma);
+    const int64_t row = (g >> 5) * kH + 4 * (g & 31) + (lane >> 3);   // channel row of the pool
+    const int k = lane & 7;
+#pragma unroll
+    for (int i = 0; i < A; ++i) anchor[row * 8 * A + A * k + i] = o[i];
+#pragma unroll
+    for (int i = 0; i < R; ++i) residual[row * 8 * R + R * k + i] = o[A + i];
+    float* mp = meta + (g >> 5) * kMetaFloats;
+    const int ch = 4 * (int)(g & 31) + (lane >> 3);
+    if (k == 0) {
+      mp[ch] = mn;
+      mp[kH + ch] = gscale;
+    }
+    mp[kMetaMuOff + k * kH + ch] = mu;
+    mp[kMetaSigmaOff + k * kH + ch] = sigma;
+  }
+}
+
 // Uniform INT-b per channel row of a page (the baseline of the paper's §2.3 and
 // §6.1): S = RN((max - min) / (2^b - 1)), Q = rint(RN((x - min) / S)) clamped to
 // 0 .. 2^b - 1 (Q = 0 when S = 0), each division correctly rounded (reciprocal
@@ -651,6 +740,33 @@ cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, u
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <int A>
+cudaError_t launch_split_t(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual, float* meta,
+                           const EncodeTables* tab, cudaStream_t s) {
+  const int64_t n_groups = n_pages * 32;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_split_kernel<A>, 256, 0);
+  const int64_t cap = (int64_t)device_sm_count() * (per_sm < 1 ? 1 : per_sm);
+  const int64_t need = (n_groups + 7) / 8;
+  const int blocks = (int)(need < cap ? need : cap);
+  encode_split_kernel<A><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), n_groups,
+                                               reinterpret_cast<uint32_t*>(anchor),
+                                               reinterpret_cast<uint32_t*>(residual), meta, *tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_split(const void* x, int64_t n_pages, int anchor_bits, uint8_t* anchor,
+                                uint8_t* residual, float* meta, const EncodeTables* tab, cudaStream_t s) {
+  switch (anchor_bits) {
+    case 2: return launch_split_t<2>(x, n_pages, anchor, residual, meta, tab, s);
+    case 3: return launch_split_t<3>(x, n_pages, anchor, residual, meta, tab, s);
+    case 4: return launch_split_t<4>(x, n_pages, anchor, residual, meta, tab, s);
+    case 5: return launch_split_t<5>(x, n_pages, anchor, residual, meta, tab, s);
+    case 6: return launch_split_t<6>(x, n_pages, anchor, residual, meta, tab, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,

@@ -186,6 +186,26 @@ const LutTables* lut_tables8(float alpha, float eps) {
   return &lut;
 }
 
+const SplitTables* split_tables(float alpha, float eps, int anchor_bits) {
+  thread_local SplitTables st;
+  thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
+  thread_local int cached_bits = -1;
+  if (alpha == cached_alpha && eps == cached_eps && anchor_bits == cached_bits) return &st;
+  const int A = anchor_bits, R = 8 - A;
+  for (int n = 0; n < 64; ++n) st.anc[n] = 0.0f;
+  for (int n = 0; n < (1 << A); ++n) {
+    const int q = n >= (1 << (A - 1)) ? n - (1 << A) : n;   // A-bit two's complement
+    const int S = q < 0 ? -1 : 1;
+    const int V = S > 0 ? q : -q - 1;
+    st.anc[n] = (float)(S * ell((V << R) + (1 << (R - 1)) - 1, alpha));
+  }
+  st.eps = eps;
+  cached_alpha = alpha;
+  cached_eps = eps;
+  cached_bits = anchor_bits;
+  return &st;
+}
+
 int set_error(int status, const char* message) { return fail(status, "%s", message); }
 
 int device_sm_count() {
@@ -516,6 +536,47 @@ int lynx_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_
   cudaError_t e = launch_reconstruct_variant(codes, meta, n_pages, variant, out, out_dtype, lut,
                                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct_variant launch");
+  return LYNX_OK;
+}
+
+int lynx_encode_split(const void* x_bf16, int64_t n_pages, int anchor_bits, const lynx_params_t* params,
+                      uint8_t* anchor, uint8_t* residual, float* meta, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (anchor_bits < 2 || anchor_bits > 6)
+    return fail(LYNX_ERR_UNSUPPORTED, "anchor_bits=%d outside 2..6", anchor_bits);
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!x_bf16 || !anchor || !residual || !meta) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(x_bf16) || misaligned(anchor) || misaligned(residual) || misaligned(meta))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  cudaError_t e = launch_encode_split(x_bf16, n_pages, anchor_bits, anchor, residual, meta,
+                                      encode_tables(params->alpha, params->eps), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_split launch");
+  return LYNX_OK;
+}
+
+int lynx_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
+                           int anchor_bits, const lynx_params_t* params, void* out, int out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_params(params);
+  if (st != LYNX_OK) return st;
+  if (anchor_bits < 2 || anchor_bits > 6)
+    return fail(LYNX_ERR_UNSUPPORTED, "anchor_bits=%d outside 2..6", anchor_bits);
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_F32)
+    return fail(LYNX_ERR_INVALID_ARG, "out_dtype=%d (need 0 = BF16 or 1 = F32)", out_dtype);
+  if (n_pages < 0) return fail(LYNX_ERR_INVALID_ARG, "n_pages=%lld < 0", (long long)n_pages);
+  if (n_pages == 0) return LYNX_OK;
+  if (!anchor || !meta || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(anchor) || misaligned(meta) || misaligned(out) || (residual && misaligned(residual)))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
+  cudaError_t e = launch_reconstruct_split(anchor, residual, meta, n_pages, anchor_bits, out, out_dtype,
+                                           split_tables(params->alpha, params->eps, anchor_bits),
+                                           lut_tables8(params->alpha, params->eps), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct_split launch");
   return LYNX_OK;
 }
 

@@ -50,6 +50,14 @@ const EncodeTables* encode_tables4(float alpha, float eps);
 const LutTables* lut_tables4(float alpha, float eps);
 const LutTables* lut_tables8(float alpha, float eps);
 
+// anchor-only values of an A-bit Anchor (S * l(V 2^R + 2^(R-1) - 1) for the
+// A-bit two's-complement code, 2 <= A <= 6), rounded to float32
+struct SplitTables {
+  float anc[64];
+  float eps;
+};
+const SplitTables* split_tables(float alpha, float eps, int anchor_bits);
+
 // single-precision variants (values of lynx.h's LYNX_VARIANT_*)
 enum Variant { kVariantLynxInt8 = 1, kVariantLynxInt4 = 2, kVariantUniformInt8 = 3, kVariantUniformInt4 = 4 };
 
@@ -64,6 +72,11 @@ cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, u
                                   const EncodeTables* tab, cudaStream_t s);
 cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
                                        void* out, int out_dtype, const LutTables* lut, cudaStream_t s);
+cudaError_t launch_encode_split(const void* x, int64_t n_pages, int anchor_bits, uint8_t* anchor,
+                                uint8_t* residual, float* meta, const EncodeTables* tab, cudaStream_t s);
+cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,
+                                     int64_t n_pages, int anchor_bits, void* out, int out_dtype,
+                                     const SplitTables* st, const LutTables* lut8, cudaStream_t s);
 cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
                                  uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
                                  cudaStream_t s);

@@ -191,6 +191,114 @@ uniform_reconstruct_kernel(const uint8_t* __restrict__ codes, const float* __res
   }
 }
 
+// the `bits`-wide two's-complement code at bit position pos of a little-endian
+// bit string held in words w[], sign-extended
+template <int BITS>
+__device__ __forceinline__ int get_bits(const uint32_t* w, int pos) {
+  const int wi = pos >> 5, sh = pos & 31;
+  uint32_t v = w[wi] >> sh;
+  if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
+  return (int)(v << (32 - BITS)) >> (32 - BITS);
+}
+
+// The split stream with an A-bit Anchor (2 <= A <= 6): rows of 8 chunks x 4A
+// bytes (Anchor) and 8 x 4(8 - A) bytes (Residual), each chunk's codes a
+// little-endian bit string.  One thread per (channel row, chunk): 32 tokens.
+// Anchor only: x_f from the 2^A-entry table; full: I = V 2^R + 2^(R-1) - 1 -
+// Q_res and x_f = S l(I) from the 256-entry table of signed bytes.  Then
+// x = fmaf(fmaf(x_f, sigma+eps, mu), gamma_scale+eps, gamma_min) as for the
+// 4+4 split.  Tables replicated per lane in shared memory (no bank conflicts).
+template <int A, bool FULL, bool kF32>
+__global__ void __launch_bounds__(256)
+reconstruct_split_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restrict__ residual,
+                         const float* __restrict__ meta, int64_t n_rows, void* __restrict__ out,
+                         const SplitTables st, const LutTables lut8) {
+  constexpr int R = 8 - A;
+  constexpr int kEntries = FULL ? 256 : (1 << A);
+  __shared__ float s_lut[kEntries * 32];
+  for (int i = threadIdx.x; i < kEntries * 32; i += blockDim.x)
+    s_lut[i] = FULL ? lut8.full[i >> 5] : st.anc[i >> 5];
+  __syncthreads();
+  const float* lut_lane = s_lut + (threadIdx.x & 31);
+  const float eps = st.eps;
+  const int64_t n_items = n_rows * 8;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < n_items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = it >> 3;
+    const int k = (int)(it & 7);
+    uint32_t aw[A], rw[R > 0 ? R : 1];
+#pragma unroll
+    for (int i = 0; i < A; ++i) aw[i] = __ldg(anchor + row * 8 * A + A * k + i);
+    if (FULL) {
+#pragma unroll
+      for (int i = 0; i < R; ++i) rw[i] = __ldg(residual + row * 8 * R + R * k + i);
+    }
+    const float* mp = meta + (row >> 7) * kMetaFloats;
+    const int ch = (int)(row & 127);
+    const float gmin = __ldg(mp + ch);
+    const float dg = __fadd_rn(__ldg(mp + kH + ch), eps);
+    const float mu = __ldg(mp + kMetaMuOff + k * kH + ch);
+    const float ds = __fadd_rn(__ldg(mp + kMetaSigmaOff + k * kH + ch), eps);
+    float x[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int qa = get_bits<A>(aw, A * t);
+      float l;
+      if (FULL) {
+        const int V = qa < 0 ? -qa - 1 : qa;
+        const int I = (V << R) + (1 << (R - 1)) - 1 - get_bits<R>(rw, R * t);
+        const int q8 = qa < 0 ? -I - 1 : I;
+        l = lut_lane[(q8 & 0xFF) * 32];
+      } else {
+        l = lut_lane[(qa & ((1 << A) - 1)) * 32];
+      }
+      x[t] = __fmaf_rn(__fmaf_rn(l, ds, mu), dg, gmin);
+    }
+    if (kF32) {
+      float4* op = reinterpret_cast<float4*>(out) + row * 64 + k * 8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) op[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    } else {
+      uint4* op = reinterpret_cast<uint4*>(out) + row * 32 + k * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(x[8 * j + 2 * u], x[8 * j + 2 * u + 1]);
+          pk[u] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        op[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+  }
+}
+
+template <int A, bool FULL, bool kF32>
+cudaError_t launch_split(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
+                         void* out, const SplitTables* st, const LutTables* lut8, cudaStream_t s) {
+  const int64_t n_rows = n_pages * kH;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_split_kernel<A, FULL, kF32>, 256, 0);
+  const int64_t cap = (int64_t)device_sm_count() * (per_sm < 1 ? 1 : per_sm);
+  const int64_t need = (n_rows * 8 + 255) / 256;
+  const int blocks = (int)(need < cap ? need : cap);
+  reconstruct_split_kernel<A, FULL, kF32><<<blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint32_t*>(anchor), reinterpret_cast<const uint32_t*>(residual), meta, n_rows, out,
+      *st, *lut8);
+  return cudaGetLastError();
+}
+
+template <int A>
+cudaError_t launch_split_a(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
+                           void* out, bool f32, const SplitTables* st, const LutTables* lut8, cudaStream_t s) {
+  if (residual)
+    return f32 ? launch_split<A, true, true>(anchor, residual, meta, n_pages, out, st, lut8, s)
+               : launch_split<A, true, false>(anchor, residual, meta, n_pages, out, st, lut8, s);
+  return f32 ? launch_split<A, false, true>(anchor, residual, meta, n_pages, out, st, lut8, s)
+             : launch_split<A, false, false>(anchor, residual, meta, n_pages, out, st, lut8, s);
+}
+
 template <int kMode, bool kF32>
 cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                    int64_t n_pages, void* out, const LutTables* lut, cudaStream_t s) {
@@ -220,6 +328,20 @@ cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, c
   }
   return f32 ? launch<0, true>(anchor, residual, meta, n_pages, out, lut, s)
              : launch<0, false>(anchor, residual, meta, n_pages, out, lut, s);
+}
+
+cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,
+                                     int64_t n_pages, int anchor_bits, void* out, int out_dtype,
+                                     const SplitTables* st, const LutTables* lut8, cudaStream_t s) {
+  const bool f32 = out_dtype == LYNX_OUT_F32;
+  switch (anchor_bits) {
+    case 2: return launch_split_a<2>(anchor, residual, meta, n_pages, out, f32, st, lut8, s);
+    case 3: return launch_split_a<3>(anchor, residual, meta, n_pages, out, f32, st, lut8, s);
+    case 4: return launch_split_a<4>(anchor, residual, meta, n_pages, out, f32, st, lut8, s);
+    case 5: return launch_split_a<5>(anchor, residual, meta, n_pages, out, f32, st, lut8, s);
+    case 6: return launch_split_a<6>(anchor, residual, meta, n_pages, out, f32, st, lut8, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,

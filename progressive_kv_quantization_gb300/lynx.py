@@ -64,6 +64,8 @@ SIGNATURES = {
                                         _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP]),
     "lynx_attn_merge": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]),
     "lynx_encode_variant": (_I32, [_VP, _I64, _I32, _PP, _VP, _VP, _VP]),
+    "lynx_encode_split": (_I32, [_VP, _I64, _I32, _PP, _VP, _VP, _VP, _VP]),
+    "lynx_reconstruct_split": (_I32, [_VP, _VP, _VP, _I64, _I32, _PP, _VP, _I32, _VP]),
     "lynx_reconstruct_variant": (_I32, [_VP, _VP, _I64, _I32, _PP, _VP, _I32, _VP]),
     "lynx_decode_attn_int4": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _I64, _VP, _I32,
                                      _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
@@ -262,6 +264,50 @@ def lynx_reconstruct_variant(codes, meta, variant: str, params: Params = Params(
     p = params.c()
     _check(load().lynx_reconstruct_variant(_ptr(codes), _ptr(meta), n, code, ctypes.byref(p), _ptr(out), oc,
                                            _stream(stream)), "lynx_reconstruct_variant")
+    return out
+
+
+def lynx_encode_split(x, anchor_bits: int, params: Params = Params(), anchor=None, residual=None, meta=None,
+                      stream=None):
+    """The split stream with an A-bit Anchor (2..6): BF16 pages x[N, 128, 256] ->
+    (anchor u8[N, 128, 32 A], residual u8[N, 128, 32 (8 - A)], meta f32[N, 2304])."""
+    _need(x, torch.bfloat16, "x")
+    n = x.numel() // (H * P)
+    if x.numel() != n * H * P:
+        raise LynxError("x must hold whole 128 x 256 pages")
+    A, R = int(anchor_bits), 8 - int(anchor_bits)
+    dev = x.device
+    anchor = anchor if anchor is not None else torch.empty((n, H, 32 * A), dtype=torch.uint8, device=dev)
+    residual = residual if residual is not None else torch.empty((n, H, 32 * R), dtype=torch.uint8, device=dev)
+    meta = meta if meta is not None else torch.empty((n, META_FLOATS), dtype=torch.float32, device=dev)
+    for t, nm, nb in ((anchor, "anchor", 32 * A), (residual, "residual", 32 * R)):
+        _need(t, torch.uint8, nm)
+        if t.numel() < n * H * nb:
+            raise LynxError(f"{nm} too small")
+    _need(meta, torch.float32, "meta")
+    p = params.c()
+    _check(load().lynx_encode_split(_ptr(x), n, A, ctypes.byref(p), _ptr(anchor), _ptr(residual), _ptr(meta),
+                                    _stream(stream)), "lynx_encode_split")
+    return anchor, residual, meta
+
+
+def lynx_reconstruct_split(anchor, residual, meta, anchor_bits: int, params: Params = Params(), out=None,
+                           out_dtype=torch.bfloat16, stream=None):
+    """Anchor-only (residual=None) or full reconstruction of lynx_encode_split's planes."""
+    _need(anchor, torch.uint8, "anchor")
+    if residual is not None:
+        _need(residual, torch.uint8, "residual")
+    _need(meta, torch.float32, "meta")
+    A = int(anchor_bits)
+    n = anchor.numel() // (H * 32 * A)
+    code = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}.get(out_dtype)
+    if code is None:
+        raise LynxError("out_dtype must be torch.bfloat16 or torch.float32")
+    out = out if out is not None else torch.empty((n, H, P), dtype=out_dtype, device=anchor.device)
+    _need(out, out_dtype, "out")
+    p = params.c()
+    _check(load().lynx_reconstruct_split(_ptr(anchor), _ptr(residual), _ptr(meta), n, A, ctypes.byref(p),
+                                         _ptr(out), code, _stream(stream)), "lynx_reconstruct_split")
     return out
 
 

@@ -141,3 +141,17 @@ def test_variant_argument_checks(lynx_lib):
     assert lib.lynx_encode_variant(a, 0, 4, None, None, None, None) == 0
     assert lib.lynx_reconstruct_variant(a, a, 1, 1, ok, a, 7, None) == -1
     assert lib.lynx_reconstruct_variant(None, a, 1, 4, ok, a, 0, None) == -1
+
+
+def test_split_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    ok = ctypes.byref(_p())
+    for bits in (1, 7):
+        assert lib.lynx_encode_split(a, 1, bits, ok, a, a, a, None) == -2
+        assert lib.lynx_reconstruct_split(a, a, a, 1, bits, ok, a, 0, None) == -2
+    assert lib.lynx_encode_split(a, -1, 3, ok, a, a, a, None) == -1
+    assert lib.lynx_encode_split(a, 0, 3, ok, None, None, None, None) == 0
+    assert lib.lynx_encode_split(ctypes.c_void_p(a.value + 2), 1, 3, ok, a, a, a, None) == -3
+    assert lib.lynx_reconstruct_split(a, None, a, 1, 3, ok, a, 9, None) == -1
