@@ -577,9 +577,10 @@ def run_comparators(torch, L, b, dev, reps=3):
     the KV vNMSE (mean over token vectors -- one head's 128 channels at one
     token -- of ||x_hat - x||^2 / ||x||^2, from float32 reconstructions) and the
     attention vNMSE (the B = 64, T = 1 decode's output rows against the same
-    decode over the BF16 pages; uniform codes through their BF16
-    reconstruction), with each variant's encode time (median of ``reps``
-    CUDA-event timings) and its bytes per KV value."""
+    decode over the BF16 pages; uniform codes and the other split widths'
+    Anchors through their BF16 reconstruction), with each variant's encode time
+    (median of ``reps`` CUDA-event timings) and its bytes per KV value; then the
+    Anchor alone of the split stream at widths 2, 3, 5 and 6 bits."""
     p = L.Params()
     x = b["x"]
     n = x.shape[0]
@@ -650,6 +651,21 @@ def run_comparators(torch, L, b, dev, reps=3):
             del rec
         rows[name] = ent
         del codes, meta
+    # the split stream at other widths: the draft (Anchor-only) accuracy against its size
+    for A in (2, 3, 5, 6):
+        R = 8 - A
+        an = torch.empty((n, 128, 32 * A), dtype=torch.uint8, device=dev)
+        rs = torch.empty((n, 128, 32 * R), dtype=torch.uint8, device=dev)
+        mt = torch.empty_like(b["meta"])
+        t = timed(lambda: L.lynx_encode_split(x, A, p, an, rs, mt))
+        rec = L.lynx_reconstruct_split(an, None, mt, A, p)
+        oa, _ = L.lynx_decode_attn_bf16(q, rec, rec[PER:], pt, ctx, HKV, workspace=ws)
+        rows[f"lynx_split_{A}+{R}_anchor"] = {
+            "bytes_per_value": (32 * A * 128 + 9216) / 32768, "encode_ms": round(t, 4),
+            "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct_split(
+                an[lo:hi], None, mt[lo:hi], A, p, out=o, out_dtype=torch.float32)),
+            "attn_vnmse": attn_vnmse(oa)}
+        del an, rs, mt, rec
     for r in rows.values():
         r["kv_vnmse"] = float(f"{r['kv_vnmse']:.4g}")
         r["attn_vnmse"] = float(f"{r['attn_vnmse']:.4g}")
