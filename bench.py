@@ -343,6 +343,11 @@ def run_gpu(args, rank, world):
     prog = run_progressive(torch, L, b, dev) if rank == 0 and not args.no_e2e else None
     tok = run_encode_tokens(torch, L, b) if rank == 0 and not args.no_e2e else None
     cmp_ = run_comparators(torch, L, b, dev) if rank == 0 and not args.no_e2e else None
+    other = None
+    if rank == 0 and not args.no_e2e and N_LAYERS == 64:
+        from progressive_kv_quantization_gb300 import inputs as inp
+        other = {"decode_sweep": run_decode_sweep(torch, L, inp, dev),
+                 "qwen235b": run_qwen235b(torch, L, inp, dev)}
     if rank != 0:
         return None
     launches = args.steps * sum(k[2] for k in ks)
@@ -362,6 +367,7 @@ def run_gpu(args, rank, world):
         "progressive": prog,
         "encode_tokens": tok,
         "comparators": cmp_,
+        "other_workloads": other,
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -671,6 +677,124 @@ def run_comparators(torch, L, b, dev, reps=3):
         r["attn_vnmse"] = float(f"{r['attn_vnmse']:.4g}")
     return {"rows": rows, "attention": "B=64, T=1 decode vs the same decode over the BF16 pages",
             "kv": "token vectors of the 64-layer cache, float32 reconstructions"}
+
+
+def _median_ms(torch, fn, reps):
+    ts = []
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts[1:])
+
+
+def run_decode_sweep(torch, L, inputs, dev, reps=5):
+    """The decode-attention sweep workload: 8 KV heads x 128, 32 query heads,
+    contexts 4K / 16K / 128K tokens x batch 1 / 16 x T = 1 / 8 / 32 (causal for
+    T > 1), over Anchor-only planes, Anchor + Residual planes and BF16 pages;
+    every sequence has its own pages (16 x 128K-token caches, 131,072 pages).
+    GB/s = KV bytes read (packed planes + metadata, or BF16) / time; median of
+    ``reps`` CUDA-event timings."""
+    Hkv, Hq, n_max, B_max = 8, 32, 131072, 16
+    npph = n_max // 256
+    outl = inputs.outlier_pairs(Hkv, 5)
+    per_seq = 2 * Hkv * npph                        # K then V pages of one sequence
+    n = B_max * per_seq
+    x = torch.empty((n, 128, 256), dtype=torch.bfloat16, device=dev)
+    for b in range(B_max):
+        for t in range(2):
+            i = b * per_seq + t * Hkv * npph
+            x[i:i + Hkv * npph] = inputs.kv_pages_torch(Hkv, n_max, 900 + 2 * b + t, outl, dev)
+    a, r, m = L.lynx_encode_pages(x)
+    gbps_peak, _ = peaks()
+    rows = []
+    for ctx_len in (4096, 16384, 131072):
+        mp = ctx_len // 256
+        for B in (1, 16):
+            pt = torch.tensor([[[b * per_seq + h * npph + j for j in range(mp)] for h in range(Hkv)]
+                               for b in range(B)], dtype=torch.int32, device=dev)
+            ctx = torch.full((B,), ctx_len, dtype=torch.int32, device=dev)
+            for T in (1, 8, 32):
+                q = inputs.queries_torch((B, T, Hq, 128), 50 + T, dev)
+                nb = L.lynx_decode_attn_workspace_size(B, T, Hq, Hkv, 128, mp)
+                ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+                o = torch.empty((B, T, Hq, 128), dtype=torch.float32, device=dev)
+                l_ = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+                causal = T > 1
+                vo = Hkv * npph
+                calls = {
+                    "anchor": (lambda: L.lynx_decode_attn(q, a, None, m, a[vo:], None, m[vo:], pt, ctx, Hkv,
+                                                          causal=causal, out=o, lse=l_, workspace=ws), 25600),
+                    "full": (lambda: L.lynx_decode_attn(q, a, r, m, a[vo:], r[vo:], m[vo:], pt, ctx, Hkv,
+                                                        causal=causal, out=o, lse=l_, workspace=ws), 41984),
+                    "bf16": (lambda: L.lynx_decode_attn_bf16(q, x, x[vo:], pt, ctx, Hkv, causal=causal, out=o,
+                                                             lse=l_, workspace=ws), 65536),
+                }
+                for mode, (fn, page_bytes) in calls.items():
+                    ms = _median_ms(torch, fn, reps)
+                    moved = 2 * B * Hkv * mp * page_bytes
+                    rows.append({"ctx": ctx_len, "B": B, "T": T, "kv": mode, "ms": round(ms, 4),
+                                 "GBps": round(moved / ms / 1e6, 1),
+                                 "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3)})
+    del x, a, r, m
+    return {"rows": rows, "statistic": f"median of {reps}",
+            "l2": "KV read per call 0.1-21 GB: the 4K contexts at B = 1 (25-65 MB) fit in L2"}
+
+
+def run_qwen235b(torch, L, inputs, dev, reps=3):
+    """The Qwen3-235B-shaped workload: 94 layers x K, V x 4 KV heads x 128 x
+    131,072 tokens (385,024 pages, 25.2e9 BF16 bytes), 16 query heads: the
+    layer-streamed encode (one lynx_encode_pages call per layer, 4,096 pages) and
+    the Anchor-only decode at B = 1 over the full context (one call per layer),
+    each timed over all 94 layers (CUDA events around the 94 calls; median of
+    ``reps``)."""
+    n_layers, Hkv, Hq, n_tok = 94, 4, 16, 131072
+    npph = n_tok // 256
+    per_layer = 2 * Hkv * npph
+    n = n_layers * per_layer
+    outl = inputs.outlier_pairs(Hkv, 7)
+    x = torch.empty((n, 128, 256), dtype=torch.bfloat16, device=dev)
+    for layer in range(n_layers):
+        for t in range(2):
+            i = layer * per_layer + t * Hkv * npph
+            x[i:i + Hkv * npph] = inputs.kv_pages_torch(Hkv, n_tok, inputs.layer_seed(7, layer, t), outl, dev)
+    a = torch.empty((n, 128, 128), dtype=torch.uint8, device=dev)
+    r = torch.empty_like(a)
+    m = torch.empty((n, L.META_FLOATS), dtype=torch.float32, device=dev)
+    p = L.Params()
+
+    def encode_all():
+        for layer in range(n_layers):
+            sl = slice(layer * per_layer, (layer + 1) * per_layer)
+            L.lynx_encode_pages(x[sl], p, a[sl], r[sl], m[sl])
+    t_enc = _median_ms(torch, encode_all, reps)
+    q = inputs.queries_torch((1, 1, Hq, 128), 77, dev)
+    pt = torch.arange(Hkv * npph, dtype=torch.int32, device=dev).view(1, Hkv, npph)
+    ctx = torch.full((1,), n_tok, dtype=torch.int32, device=dev)
+    nb = L.lynx_decode_attn_workspace_size(1, 1, Hq, Hkv, 128, npph)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    o = torch.empty((1, 1, Hq, 128), dtype=torch.float32, device=dev)
+    l_ = torch.empty((1, 1, Hq), dtype=torch.float32, device=dev)
+    layers = [(a[k * per_layer:], m[k * per_layer:], a[k * per_layer + Hkv * npph:], m[k * per_layer + Hkv * npph:])
+              for k in range(n_layers)]
+
+    def decode_all():
+        for ka, km, va, vm in layers:
+            L.lynx_decode_attn(q, ka, None, km, va, None, vm, pt, ctx, Hkv, p, out=o, lse=l_, workspace=ws)
+    t_dec = _median_ms(torch, decode_all, reps)
+    gbps_peak, _ = peaks()
+    enc_moved, dec_moved = n * BYTES["encode"][1], n * BYTES["decode_anchor"][1]
+    del x, a, r, m
+    return {"pages": n, "bf16_bytes": n * PAGE,
+            "encode": {"ms": round(t_enc, 3), "GBps_bf16_in": round(n * PAGE / t_enc / 1e6, 1),
+                       "frac_of_hbm": round(enc_moved / t_enc / 1e6 / gbps_peak, 3), "launches": n_layers},
+            "decode_anchor_b1": {"ms": round(t_dec, 3), "GBps_packed": round(dec_moved / t_dec / 1e6, 1),
+                                 "frac_of_hbm": round(dec_moved / t_dec / 1e6 / gbps_peak, 3),
+                                 "launches": 2 * n_layers},
+            "statistic": f"median of {reps} passes over the 94 layers"}
 
 
 # ------------------------------------------------------------------ oracle arm

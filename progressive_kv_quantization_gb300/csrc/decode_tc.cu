@@ -1,7 +1,7 @@
 // Tensor-core verification attention over Lynx-encoded pages: the attention
 // of the Lynx paper (§2.1) run on the KV that the Anchor phase (draft) or the
 // Anchor and Residual phases (verification) of §4.2-4.3 deliver, for R = 16
-// or (full codes) R = 32 of the query rows that share one KV head (T tokens x
+// or R = 32 of the query rows that share one KV head (T tokens x
 // Hq/Hkv heads) per CTA.  A 32-row CTA dequantises each key once for 32 rows.
 //
 // CTA skeleton as in the narrow kernel: a producer lane streams the split's
@@ -92,6 +92,7 @@ struct TLayout {
 static_assert(TLayout<false, 16>::kAlloc <= 232448, "shared memory (anchor, tensor core)");
 static_assert(TLayout<true, 16>::kAlloc <= 232448, "shared memory (full, tensor core)");
 static_assert(TLayout<true, 32>::kAlloc <= 232448, "shared memory (full, tensor core, 32 rows)");
+static_assert(TLayout<false, 32>::kAlloc <= 232448, "shared memory (anchor, tensor core, 32 rows)");
 
 // ---- tensor memory (cta_group::1).  Column allocation by one whole warp; the
 // allocated base address is written to shared memory.
@@ -658,9 +659,9 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   }
 }
 
-// rows per CTA: 32 for the full codes when more than 16 rows share a KV head
-// (each key is dequantised once for 32 rows), else 16
-constexpr bool tc_wide(int rows, bool full) { return full && rows > 16; }
+// rows per CTA: 32 when more than 16 rows share a KV head (each key is
+// dequantised once for 32 rows), else 16
+constexpr bool tc_wide(int rows, bool) { return rows > 16; }
 
 template <bool FULL, int R>
 cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
@@ -696,8 +697,9 @@ bool use_tc_rows(int rows) { return rows >= 12; }
 int tc_rows_per_cta(int rows, bool full) { return tc_wide(rows, full) ? 32 : 16; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
-  if (!full) return launch_tc<false, 16>(a, lut, s);
-  return tc_wide(a.T * a.G, true) ? launch_tc<true, 32>(a, lut, s) : launch_tc<true, 16>(a, lut, s);
+  const bool wide = tc_wide(a.T * a.G, full);
+  if (!full) return wide ? launch_tc<false, 32>(a, lut, s) : launch_tc<false, 16>(a, lut, s);
+  return wide ? launch_tc<true, 32>(a, lut, s) : launch_tc<true, 16>(a, lut, s);
 }
 
 }  // namespace lynx

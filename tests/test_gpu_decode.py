@@ -305,9 +305,10 @@ def test_vnmse_of_anchor_and_full_codes(cuda_device, llama_pools):
         assert vf_r * 100 < va_r and vf_g * 100 < va_g
 
 
+@pytest.mark.parametrize("mode", ["anchor", "full"])
 @pytest.mark.parametrize("T", [9, 12])
-def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, T):
-    """Full codes, G = 4, T = 9 or 12: 36 or 48 query rows per KV head, i.e. one
+def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, mode, T):
+    """G = 4, T = 9 or 12: 36 or 48 query rows per KV head, i.e. one
     full 32-row tensor-core tile (output accumulators in tensor memory) and a
     second one holding 4 or 16 rows; contexts include 0 keys, fewer keys than T
     and partial pages."""
@@ -317,8 +318,8 @@ def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, T):
     table = np.stack([contiguous_table(1, Hkv, 24, 64, offset=7 * b)[0] for b in range(B)])
     q = inputs.queries_np((B, T, Hq, 128), 400 + T)
     for causal in (False, True):
-        o, lse = run(llama_pools, "full", q, table, ctx, Hkv, causal)
-        ro, rl = reference(llama_pools, "full", q, table, ctx, Hkv, causal)
+        o, lse = run(llama_pools, mode, q, table, ctx, Hkv, causal)
+        ro, rl = reference(llama_pools, mode, q, table, ctx, Hkv, causal)
         empty = np.isnan(ro[..., 0])
         assert np.all(o[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
         check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
@@ -326,9 +327,8 @@ def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, T):
 
 @pytest.mark.parametrize("mode", ["anchor", "full"])
 def test_extreme_row_counts_and_alpha(cuda_device, mode):
-    """The largest supported row count per KV head (T = 32, G = 8: 256 rows in 16
-    16-row tensor-core tiles for the anchor codes, 8 32-row tiles for the full
-    codes), plain multi-head attention (G = 1) at T = 1 and eight query heads
+    """The largest supported row count per KV head (T = 32, G = 8: 256 rows in 8
+    32-row tensor-core tiles), plain multi-head attention (G = 1) at T = 1 and eight query heads
     per KV head at T = 1 (one row, and all 8 rows, of a narrow-kernel tile) and
     at T = 12 (the smallest row count the wide tensor-core kernel takes), over
     pools encoded at alpha = 1e4."""
