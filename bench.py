@@ -691,13 +691,45 @@ def _median_ms(torch, fn, reps):
     return statistics.median(ts[1:])
 
 
+def _graph_ms(torch, fn, reps):
+    """Median over ``reps`` replays of a CUDA graph holding the launches of one
+    ``fn()`` call (captured after an eager warm-up call), each replay bracketed
+    by CUDA events: the GPU time of the call without the host-side cost of the
+    Python binding, as a decode loop that replays a captured graph sees it."""
+    fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    del g
+    return statistics.median(ts)
+
+
 def run_decode_sweep(torch, L, inputs, dev, reps=5):
     """The decode-attention sweep workload: 8 KV heads x 128, 32 query heads,
     contexts 4K / 16K / 128K tokens x batch 1 / 16 x T = 1 / 8 / 32 (causal for
     T > 1), over Anchor-only planes, Anchor + Residual planes and BF16 pages;
     every sequence has its own pages (16 x 128K-token caches, 131,072 pages).
     GB/s = KV bytes read (packed planes + metadata, or BF16) / time; median of
-    ``reps`` CUDA-event timings."""
+    ``reps`` CUDA-event timings of a CUDA-graph replay of the call ("ms") and of
+    the eager Python call ("eager_ms", which adds the binding's host-side time
+    wherever the GPU finishes before the host has issued the launches)."""
     Hkv, Hq, n_max, B_max = 8, 32, 131072, 16
     npph = n_max // 256
     outl = inputs.outlier_pairs(Hkv, 5)
@@ -734,13 +766,14 @@ def run_decode_sweep(torch, L, inputs, dev, reps=5):
                                                              lse=l_, workspace=ws), 65536),
                 }
                 for mode, (fn, page_bytes) in calls.items():
-                    ms = _median_ms(torch, fn, reps)
+                    eager = _median_ms(torch, fn, reps)
+                    ms = _graph_ms(torch, fn, reps)
                     moved = 2 * B * Hkv * mp * page_bytes
                     rows.append({"ctx": ctx_len, "B": B, "T": T, "kv": mode, "ms": round(ms, 4),
-                                 "GBps": round(moved / ms / 1e6, 1),
+                                 "eager_ms": round(eager, 4), "GBps": round(moved / ms / 1e6, 1),
                                  "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3)})
     del x, a, r, m
-    return {"rows": rows, "statistic": f"median of {reps}",
+    return {"rows": rows, "statistic": f"median of {reps}; ms = CUDA-graph replay, eager_ms = Python call",
             "l2": "KV read per call 0.1-21 GB: the 4K contexts at B = 1 (25-65 MB) fit in L2"}
 
 
@@ -750,7 +783,7 @@ def run_qwen235b(torch, L, inputs, dev, reps=3):
     layer-streamed encode (one lynx_encode_pages call per layer, 4,096 pages) and
     the Anchor-only decode at B = 1 over the full context (one call per layer),
     each timed over all 94 layers (CUDA events around the 94 calls; median of
-    ``reps``)."""
+    ``reps``); the decode also as one CUDA graph of the 94 calls ("graph_ms")."""
     n_layers, Hkv, Hq, n_tok = 94, 4, 16, 131072
     npph = n_tok // 256
     per_layer = 2 * Hkv * npph
@@ -785,6 +818,7 @@ def run_qwen235b(torch, L, inputs, dev, reps=3):
         for ka, km, va, vm in layers:
             L.lynx_decode_attn(q, ka, None, km, va, None, vm, pt, ctx, Hkv, p, out=o, lse=l_, workspace=ws)
     t_dec = _median_ms(torch, decode_all, reps)
+    t_graph = _graph_ms(torch, decode_all, reps)
     gbps_peak, _ = peaks()
     enc_moved, dec_moved = n * BYTES["encode"][1], n * BYTES["decode_anchor"][1]
     del x, a, r, m
@@ -793,6 +827,9 @@ def run_qwen235b(torch, L, inputs, dev, reps=3):
                        "frac_of_hbm": round(enc_moved / t_enc / 1e6 / gbps_peak, 3), "launches": n_layers},
             "decode_anchor_b1": {"ms": round(t_dec, 3), "GBps_packed": round(dec_moved / t_dec / 1e6, 1),
                                  "frac_of_hbm": round(dec_moved / t_dec / 1e6 / gbps_peak, 3),
+                                 "graph_ms": round(t_graph, 3),
+                                 "graph_GBps_packed": round(dec_moved / t_graph / 1e6, 1),
+                                 "graph_frac_of_hbm": round(dec_moved / t_graph / 1e6 / gbps_peak, 3),
                                  "launches": 2 * n_layers},
             "statistic": f"median of {reps} passes over the 94 layers"}
 

@@ -19,6 +19,7 @@ bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool);
 namespace {
 
 constexpr int kConsumers = 8;
+constexpr int kConsumerThreads = kConsumers * 32;
 constexpr int kThreadsQ = (kConsumers + 1) * 32;
 constexpr int kRows = 4;
 constexpr int kWsPerCta = kRows * kH + 2 * kRows;

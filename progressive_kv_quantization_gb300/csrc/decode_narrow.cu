@@ -124,34 +124,8 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   const uint32_t bar_empty = bar_full + 8 * kSt;
   int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
 
-  // ---- prologue: value tables, Q^T fragments, barriers
-  for (int i = tid; i < 256 * 32; i += kThreadsQ) {
-    const int e = i >> 5, ln = i & 31;
-    if (!FULL) {
-      const float2 v = lut.anc_pair[e];
-      const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
-      const __half lx = __float2half_rn(v.x - __half2float(hx));
-      const __half ly = __float2half_rn(v.y - __half2float(hy));
-      *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
-      *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
-    } else {
-      const float v = lut.full[e];
-      const __half hv = __float2half_rn(v);
-      const __half lv = __float2half_rn(v - __half2float(hv));
-      *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
-      *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
-    }
-  }
-  // entry (ks, lane, e): query row g' (= lane >> 2), channel 8 ks + t' + 4e; BF16 is exact in TF32
-  for (int i = tid; i < 16 * 32 * 2; i += kThreadsQ) {
-    const int e = i & 1, ln = (i >> 1) & 31, ks = i >> 6;
-    const int row = row0 + (ln >> 2);
-    const int d = 8 * ks + (ln & 3) + 4 * e;
-    uint32_t v = 0u;
-    if (row < TG)
-      v = (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + d] << 16;
-    reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
-  }
+  // ---- prologue: barriers first, so that the producer lane starts streaming
+  // pages while the consumer warps fill the value tables and the Q^T fragments
   if (tid == 0) {
     for (int st = 0; st < kSt; ++st) {
       mbar_init(bar_full + 8 * st, 1);
@@ -174,6 +148,37 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
+    // value tables and Q^T fragments, by the 8 consumer warps only; they meet at
+    // named barrier 1 (the producer warp never takes part in it)
+    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
+      const int e = i >> 5, ln = i & 31;
+      if (!FULL) {
+        const float2 v = lut.anc_pair[e];
+        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+        const __half lx = __float2half_rn(v.x - __half2float(hx));
+        const __half ly = __float2half_rn(v.y - __half2float(hy));
+        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+      } else {
+        const float v = lut.full[e];
+        const __half hv = __float2half_rn(v);
+        const __half lv = __float2half_rn(v - __half2float(hv));
+        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+      }
+    }
+    // entry (ks, lane, e): query row g' (= lane >> 2), channel 8 ks + t' + 4e; BF16 is exact in TF32
+    for (int i = tid; i < 16 * 32 * 2; i += kConsumerThreads) {
+      const int e = i & 1, ln = (i >> 1) & 31, ks = i >> 6;
+      const int row = row0 + (ln >> 2);
+      const int d = 8 * ks + (ln & 3) + 4 * e;
+      uint32_t v = 0u;
+      if (row < TG)
+        v = (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + d] << 16;
+      reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+
     const int w = warp;
     const uint32_t s_ab = S::kWarps + w * kNrWarpBytes;
     const uint32_t lane8 = 8u * L, lane4 = 4u * L, lane4v = 128u + 4u * L;

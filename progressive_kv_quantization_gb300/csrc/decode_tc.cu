@@ -201,61 +201,17 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   const uint32_t bar_empty = bar_full + 8 * kSt;
   int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
 
-  // ---- prologue: value tables, Q fragments, barriers, TMEM
-  for (int i = tid; i < 256 * 32; i += kThreadsQ) {
-    const int e = i >> 5, ln = i & 31;
-    if (!FULL) {
-      const float2 v = lut.anc_pair[e];
-      const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
-      const __half lx = __float2half_rn(v.x - __half2float(hx));
-      const __half ly = __float2half_rn(v.y - __half2float(hy));
-      *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
-      *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
-    } else {
-      const float v = lut.full[e];
-      const __half hv = __float2half_rn(v);
-      const __half lv = __float2half_rn(v - __half2float(hv));
-      *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
-      *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
-    }
-  }
-  // Q fragments in fp16, scaled by 2^-eq so that the largest |q| of the CTA's rows
-  // lies in [2^14, 2^15) (the other values keep their 8 significant bits unless
-  // they are 2^-28 times smaller than it)
+  // ---- prologue: barriers and TMEM first, so that the producer lane starts
+  // streaming pages while the consumer warps fill the value tables and the Q
+  // fragments
   uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
-  if (tid == 0) *s_qmax = 0u;
-  __syncthreads();
-  {
-    uint32_t qm = 0u;
-    for (int i = tid; i < R * kH; i += kThreadsQ) {
-      const int row = row0 + (i >> 7);
-      if (row < TG)
-        qm = max(qm, (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + (i & 127)] &
-                         0x7FFFu);
-    }
-    atomicMax(s_qmax, qm);
-  }
-  __syncthreads();
-  const int eq = min(max((int)((*s_qmax >> 7) & 0xFFu) - 127 - 14, -100), 113);
-  const float qscale = __uint_as_float((uint32_t)(127 - eq) << 23);   // 2^-eq
-  // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channels 16 ks + 2t' + 8 (e >> 1) + {0, 1}
-  for (int i = tid; i < MT * 8 * 32 * 4; i += kThreadsQ) {
-    const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 7, mi = i >> 10;
-    const int row = row0 + 16 * mi + (ln >> 2) + 8 * (e & 1);
-    const int d = 16 * ks + 2 * (ln & 3) + 8 * (e >> 1);
-    uint32_t v = 0u;
-    if (row < TG) {
-      const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
-      v = h2(__uint_as_float((uint32_t)qr[d] << 16) * qscale, __uint_as_float((uint32_t)qr[d + 1] << 16) * qscale);
-    }
-    reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
-  }
   if (tid == 0) {
     for (int st = 0; st < kSt; ++st) {
       mbar_init(bar_full + 8 * st, 1);
       mbar_init(bar_empty + 8 * st, kConsumers);
     }
     *s_flag = 0;
+    *s_qmax = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (kTmem && warp == 0) {
@@ -288,6 +244,55 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
+    // value tables, then the Q fragments, by the 8 consumer warps only; they
+    // meet at named barrier 1 (the producer warp never takes part in it)
+    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
+      const int e = i >> 5, ln = i & 31;
+      if (!FULL) {
+        const float2 v = lut.anc_pair[e];
+        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+        const __half lx = __float2half_rn(v.x - __half2float(hx));
+        const __half ly = __float2half_rn(v.y - __half2float(hy));
+        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+      } else {
+        const float v = lut.full[e];
+        const __half hv = __float2half_rn(v);
+        const __half lv = __float2half_rn(v - __half2float(hv));
+        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+      }
+    }
+    // Q fragments in fp16, scaled by 2^-eq so that the largest |q| of the CTA's rows
+    // lies in [2^14, 2^15) (the other values keep their 8 significant bits unless
+    // they are 2^-28 times smaller than it)
+    {
+      uint32_t qm = 0u;
+      for (int i = tid; i < R * kH; i += kConsumerThreads) {
+        const int row = row0 + (i >> 7);
+        if (row < TG)
+          qm = max(qm, (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + (i & 127)] &
+                           0x7FFFu);
+      }
+      atomicMax(s_qmax, qm);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+    const int eq = min(max((int)((*s_qmax >> 7) & 0xFFu) - 127 - 14, -100), 113);
+    const float qscale = __uint_as_float((uint32_t)(127 - eq) << 23);   // 2^-eq
+    // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channels 16 ks + 2t' + 8 (e >> 1) + {0, 1}
+    for (int i = tid; i < MT * 8 * 32 * 4; i += kConsumerThreads) {
+      const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 7, mi = i >> 10;
+      const int row = row0 + 16 * mi + (ln >> 2) + 8 * (e & 1);
+      const int d = 16 * ks + 2 * (ln & 3) + 8 * (e >> 1);
+      uint32_t v = 0u;
+      if (row < TG) {
+        const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+        v = h2(__uint_as_float((uint32_t)qr[d] << 16) * qscale, __uint_as_float((uint32_t)qr[d + 1] << 16) * qscale);
+      }
+      reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+
     const int w = warp;
     const uint32_t s_ab = S::kWarps + w * kTcWarpBytes;
     const uint32_t lane8 = 8u * L, lane4 = 4u * L, lane4v = 128u + 4u * L;
