@@ -79,6 +79,13 @@
  *     LYNX_ERR_UNSUPPORTED.
  *   - Thread safety: entry points may be called from several host threads;
  *     lynx_last_error() is per host thread.
+ *   - CUDA graphs: the first call of each entry point on a device configures
+ *     its kernels (shared-memory limits, the status word's address); every
+ *     later call only launches kernels on `stream`, so it may be captured in a
+ *     CUDA graph and replayed.  Tensor maps and launch shapes are fixed at
+ *     capture: a replay reads the same buffers, page-table and context-length
+ *     arrays (whose contents may change between replays within the captured
+ *     max_pages and shapes).
  */
 #ifndef LYNX_H_
 #define LYNX_H_

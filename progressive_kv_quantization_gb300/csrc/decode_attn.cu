@@ -608,6 +608,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
     return;
   }
 
+  allow_dependent_launch();   // the split combine may be scheduled once every CTA is here
   // reduce the 8 chunk lanes of each channel, write this split's partials
 #pragma unroll
   for (int k = 0; k < 4; ++k)
@@ -634,8 +635,19 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
   }
 }
 
-// Merge the splits of one query row: grid (n_rg * 4, Hkv, B), 128 threads.
+// Merge the splits of one query row: grid (n_rg * 4, Hkv, B), 128 threads
+// (thread d = output channel d).  The splits' maxima and denominators are
+// gathered by all threads at once (split s by thread s mod 128) and reduced
+// across the block; each split's weight 2^(m_s - m*) goes to shared memory;
+// then thread d sums its channel over the splits in order, eight loads in
+// flight.  A split that saw no key (m_s = -inf) has weight 0 and its partial
+// output is not read into the sum.
+constexpr int kMaxSplits = 1024;
+
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[2][4];
+  wait_prerequisite_grids();
   const int r = blockIdx.x & 3;
   const int rg = blockIdx.x >> 2;
   const int h = blockIdx.y;
@@ -644,24 +656,53 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   if (row >= a.T * a.G) return;
   const int t = row / a.G, hq = h * a.G + row % a.G;
   const int d = threadIdx.x;
-  const int64_t cta0 = (((int64_t)b * a.Hkv + h) * a.n_rg + rg) * a.n_splits;
+  const int warp = d >> 5, lane = d & 31;
+  const int n = a.n_splits;
+  const int64_t cta0 = (((int64_t)b * a.Hkv + h) * a.n_rg + rg) * n;
   const float* ws = a.ws + cta0 * kWsPerCta;
-  float mstar = -CUDART_INF_F;
-  for (int s = 0; s < a.n_splits; ++s) mstar = fmaxf(mstar, ws[s * kWsPerCta + kRows * kH + r]);
   const int64_t o_idx = (((int64_t)b * a.T + t) * a.Hq + hq);
+
+  float mloc = -CUDART_INF_F;
+  for (int s = d; s < n; s += kH) mloc = fmaxf(mloc, ws[(int64_t)s * kWsPerCta + kRows * kH + r]);
+  mloc = warp_max(mloc);
+  if (lane == 0) s_red[0][warp] = mloc;
+  __syncthreads();
+  const float mstar = fmaxf(fmaxf(s_red[0][0], s_red[0][1]), fmaxf(s_red[0][2], s_red[0][3]));
   if (mstar == -CUDART_INF_F) {
     a.out[o_idx * kH + d] = 0.0f;
     if (d == 0 && a.lse) a.lse[o_idx] = -CUDART_INF_F;
     return;
   }
-  float l = 0.0f, o = 0.0f;
-  for (int s = 0; s < a.n_splits; ++s) {
-    const float* w = ws + s * kWsPerCta;
+  float lloc = 0.0f;
+  for (int s = d; s < n; s += kH) {
+    const float* w = ws + (int64_t)s * kWsPerCta;
     const float ms = w[kRows * kH + r];
-    if (ms == -CUDART_INF_F) continue;
-    const float f = exp2f(ms - mstar);
-    l += w[kRows * kH + kRows + r] * f;
-    o += w[r * kH + d] * f;
+    const float f = (ms == -CUDART_INF_F) ? 0.0f : exp2f(ms - mstar);
+    s_w[s] = f;
+    if (f != 0.0f) lloc = fmaf(w[kRows * kH + kRows + r], f, lloc);
+  }
+  lloc = warp_sum(lloc);
+  if (lane == 0) s_red[1][warp] = lloc;
+  __syncthreads();
+  const float l = (s_red[1][0] + s_red[1][1]) + (s_red[1][2] + s_red[1][3]);
+
+  const float* od = ws + r * kH + d;
+  float o = 0.0f;
+  int s = 0;
+  for (; s + 8 <= n; s += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = od[(int64_t)(s + k) * kWsPerCta];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float f = s_w[s + k];
+      o = (f != 0.0f) ? fmaf(v[k], f, o) : o;
+    }
+  }
+  for (; s < n; ++s) {
+    const float f = s_w[s];
+    const float v = od[(int64_t)s * kWsPerCta];
+    o = (f != 0.0f) ? fmaf(v, f, o) : o;
   }
   a.out[o_idx * kH + d] = o / l;
   if (d == 0 && a.lse) a.lse[o_idx] = (mstar + log2f(l)) * 0.6931471805599453f;
@@ -696,6 +737,8 @@ attn_merge_kernel(const float* __restrict__ oa, const float* __restrict__ la,
   }
 }
 
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+
 template <int MODE>
 cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
   constexpr int kSmem = Layout<MODE>::kTotal;
@@ -712,9 +755,23 @@ cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t 
   decode_split_kernel<MODE><<<grid, kThreads, kSmem, s>>>(a, *lut);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 g2(a.n_rg * kRows, a.Hkv, a.B);
-  decode_combine_kernel<<<g2, kH, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_combine(a, s);
+}
+
+// The combine of a decode call, launched as a programmatic dependent of the
+// decode kernel just issued on s (it waits for that grid inside the kernel).
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_rg * kRows, a.Hkv, a.B);
+  cfg.blockDim = dim3(kH, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
 }
 
 }  // namespace
@@ -731,7 +788,7 @@ DecodePlan plan_decode(int B, int T, int Hq, int Hkv, int max_pages, int mode) {
   const int64_t resident = device_sm_count();   // one CTA per SM (shared-memory bound)
   int best_s = 1;
   double best = 1e300;
-  const int s_max = max_pages < 1024 ? max_pages : 1024;
+  const int s_max = max_pages < kMaxSplits ? max_pages : kMaxSplits;
   for (int s = 1; s <= s_max; ++s) {
     const int pps = (max_pages + s - 1) / s;
     const int s_eff = (max_pages + pps - 1) / pps;
@@ -760,11 +817,9 @@ cudaError_t launch_attn_merge(const float* oa, const float* la, const float* ob,
 
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s) {
   if (mode == kModeBf16) return launch_mode<kModeBf16>(a, lut, s);
-  cudaError_t e = launch_decode_quant(a, mode == kModeFull, lut, s);
+  const cudaError_t e = launch_decode_quant(a, mode == kModeFull, lut, s);
   if (e != cudaSuccess) return e;
-  dim3 g2(a.n_rg * kRows, a.Hkv, a.B);
-  decode_combine_kernel<<<g2, kH, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_combine(a, s);
 }
 
 }  // namespace lynx

@@ -382,6 +382,7 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
 
   // ================= merge the 8 chunk states (the ring is idle now)
   __syncthreads();
+  allow_dependent_launch();   // the split combine may be scheduled once every CTA is here
   if (*reinterpret_cast<volatile int*>(s_flag) != 0) return;
   float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);

@@ -568,6 +568,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   if (kTmem) tmem_fence_before_sync();
   __syncthreads();
   if (kTmem) tmem_fence_after_sync();
+  allow_dependent_launch();   // the split combine may be scheduled once every CTA is here
   const bool ok = *reinterpret_cast<volatile int*>(s_flag) == 0;
   float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);

@@ -8,6 +8,20 @@
 
 namespace lynx {
 
+#ifdef __CUDACC__
+// Programmatic dependent launch.  A decode kernel calls allow_dependent_launch()
+// when its main loop is done, so that the split-combine kernel behind it in the
+// stream is scheduled while the last CTAs finish; the combine calls wait_prerequisite_grids() before its first
+// read, which returns once the decode grid has completed and its writes are
+// visible.  Where nothing was launched with the programmatic attribute both are
+// no-ops.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisite_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
+
 // Page geometry (H channels x P tokens, C-token chunks).
 constexpr int kH = 128;
 constexpr int kP = 256;

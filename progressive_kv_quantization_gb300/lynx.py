@@ -344,8 +344,8 @@ def _decode_prep(q, page_table, ctx_len, n_kv_heads, out, lse, workspace):
     out = out if out is not None else torch.empty((B, T, Hq, D), dtype=torch.float32, device=dev)
     lse = lse if lse is not None else torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
     _need(out, torch.float32, "out")
-    ws_bytes = lynx_decode_attn_workspace_size(B, T, Hq, n_kv_heads, D, max_pages)
     if workspace is None:
+        ws_bytes = lynx_decode_attn_workspace_size(B, T, Hq, n_kv_heads, D, max_pages)
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     return B, T, Hq, D, max_pages, out, lse, workspace
 

@@ -389,3 +389,56 @@ def test_extreme_magnitudes(cuda_device, mode, T):
         q = lo.bf16_to_f32(q_bits).astype(np.float64)
         ro, rl = at.decode_attention(q, pools.fetch(mode), table, ctx, Hkv, scale, True)
         check_attention(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("entry", ["anchor", "full_t8", "bf16", "noalloc"])
+def test_decode_replays_in_cuda_graph(cuda_device, llama_pools, entry):
+    """A decode call captured in a CUDA graph (after one eager call on the
+    device) replays to the eager call's results bit for bit: the calls issue
+    only kernel launches on the caller's stream.  Draft decode (narrow tiles),
+    T = 8 causal verification over full codes (32-row tiles), the BF16 kernel
+    and the no-workspace entry point."""
+    B, Hq, Hkv = 2, 32, 8
+    T = 8 if entry == "full_t8" else 1
+    table = torch.from_numpy(np.stack([contiguous_table(1, Hkv, 16, 64, offset=9 * b)[0]
+                                       for b in range(B)])).cuda()
+    ctx = torch.tensor([4096, 3000], dtype=torch.int32).cuda()
+    q = torch.from_numpy(inputs.queries_np((B, T, Hq, 128), 610 + T).view(np.int16)).view(torch.bfloat16).cuda()
+    ka, kr, km = llama_pools.dev["k"]
+    va, vr, vm = llama_pools.dev["v"]
+    ws = torch.empty(max(L.lynx_decode_attn_workspace_size(B, T, Hq, Hkv, 128, 16), 16), dtype=torch.uint8,
+                     device="cuda")
+
+    def call(o, lse):
+        if entry == "bf16":
+            L.lynx_decode_attn_bf16(q, llama_pools.dev_bf16["k"], llama_pools.dev_bf16["v"], table, ctx, Hkv,
+                                    out=o, lse=lse, workspace=ws)
+        elif entry == "noalloc":
+            L.lynx_decode_attn_noalloc(q, ka, None, km, va, None, vm, table, ctx, Hkv, out=o, lse=lse)
+        else:
+            full = entry == "full_t8"
+            L.lynx_decode_attn(q, ka, kr if full else None, km, va, vr if full else None, vm, table, ctx, Hkv,
+                               causal=full, out=o, lse=lse, workspace=ws)
+
+    mk = lambda: (torch.empty((B, T, Hq, 128), dtype=torch.float32, device="cuda"),
+                  torch.empty((B, T, Hq), dtype=torch.float32, device="cuda"))
+    o_e, l_e = mk()
+    call(o_e, l_e)
+    torch.cuda.synchronize()
+    o_g, l_g = mk()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(o_g, l_g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    o_g.zero_()
+    l_g.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(o_g, l_g)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e)
