@@ -1,20 +1,17 @@
 // Shared pieces of the quantised-KV decode kernels: the page-unit geometry of
-// the shared-memory ring, PTX helpers for mbarriers, TMA, bulk copies and
-// mma.sync, the value-table addressing, and the producer lane that streams a
-// split's K and V units through the ring.
+// the shared-memory ring, mma.sync and conversion helpers, the value-table
+// addressing, and the producer lane that streams a split's K and V units
+// through the ring (the mbarrier and TMA helpers are in tma_ptx.cuh).
 #pragma once
 
 #include "lynx_internal.cuh"
+#include "tma_ptx.cuh"
 
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
 namespace lynx {
-
-// 2-D tensor map over a pool of 4-bit planes (rows of 128 bytes, one 128 x 128
-// tile per page, 128-byte swizzle); false if the driver refuses it
-bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool);
 
 namespace {
 
@@ -23,7 +20,6 @@ constexpr int kConsumerThreads = kConsumers * 32;
 constexpr int kThreadsQ = (kConsumers + 1) * 32;
 constexpr int kRows = 4;
 constexpr int kWsPerCta = kRows * kH + 2 * kRows;
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 template <bool FULL, int STAGES = 3>
 struct QGeo {
@@ -35,61 +31,6 @@ struct QGeo {
 static_assert(QGeo<false>::kUnit % 1024 == 0 && QGeo<true>::kUnit % 1024 == 0,
               "ring slots must keep the 1024-byte alignment of swizzled tiles");
 
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// gives up after kWaitNs (clock checked every 256 polls) or 2^26 polls
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_tile_g2s(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

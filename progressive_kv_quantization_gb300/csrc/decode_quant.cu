@@ -47,6 +47,21 @@ bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool token_map(CUtensorMap* m, const void* x, int64_t n_tokens, int64_t row_elems, int64_t stride) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || stride % 8 != 0 || row_elems % 64 != 0) return false;
+  // TMA coordinates are signed 32-bit: the channel and token offsets must fit
+  if (row_elems > ((int64_t)1 << 31) - 64 || n_tokens > ((int64_t)1 << 31) - 256) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+  const cuuint32_t box[2] = {64, 256};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // the TMA row coordinate (page id * 128) is a signed 32-bit value
 bool n_pool_too_large(int64_t n_pool) { return n_pool <= 0 || n_pool * kH > ((int64_t)1 << 31) - 1; }
 

@@ -35,6 +35,7 @@
 // even tokens in the low and odd tokens in the high nibbles.
 
 #include "lynx_internal.cuh"
+#include "tma_ptx.cuh"
 
 #include <cuda_bf16.h>
 
@@ -253,7 +254,7 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
     }
     // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
     quantise8<OUT == kOutInt4 ? 7 : 127>(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
-    if (OUT >= kOutSplitBits) {
+    if constexpr (OUT >= kOutSplitBits) {
       constexpr int A = OUT - kOutSplitBits, R = 8 - A;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -439,6 +440,134 @@ encode_tokens_kernel(const uint16_t* __restrict__ x, int64_t n_tokens, int n_hea
       mp[kMetaMuOff + w * kH + c] = mu;
       mp[kMetaSigmaOff + w * kH + c] = sigma;
     }
+  }
+}
+
+// Token-major input staged through shared memory by TMA.  An item is one half
+// page: 64 channels (64 h-local channels 64 k .. 64 k + 63 of head h) x the
+// page's 256 tokens, one 32 KB box [256 tokens][64 channels] with 128-byte
+// rows, loaded by one TMA copy into a three-slot ring; thread 0 keeps the
+// ring full.  Warp w owns chunk w (tokens 32 w .. 32 w + 31); lane L owns the
+// channel pair 2L, 2L + 1 of the half: one 4-byte shared load per token gives
+// both channels' values, and a byte permute turns two such words (tokens 2i,
+// 2i + 1) into the two channels' token pairs, the register form encode_chunk
+// takes.  At a fixed token the 32 lanes read 128 contiguous bytes (no bank
+// conflict).  The row extremes join the 8 chunks' extremes through shared
+// memory (double-buffered by item parity, one barrier per item; the slot is
+// handed back to TMA at that barrier, once every lane holds its values).
+// Tokens past n_tokens arrive as zeros and count as padding (PARTIAL).
+constexpr int kTokSlots = 3;
+constexpr int kTokBox = 256 * 64 * 2;
+constexpr int kTokSmem = kTokSlots * kTokBox + 64;
+
+template <bool PARTIAL>
+__global__ void __launch_bounds__(256, 2)
+encode_tokens_tma_kernel(const __grid_constant__ CUtensorMap tm, int64_t n_tokens, int n_heads, int n_pp,
+                         int j_begin, int j_count, uint4* __restrict__ anchor, uint4* __restrict__ residual,
+                         float* __restrict__ meta, const EncodeTables tab, int* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_thr[129];
+  __shared__ float2 s_mn[2][8][32], s_mx[2][8][32];   // [parity][chunk][lane]: channels 2L, 2L + 1
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bars = ring + kTokSlots * kTokBox;
+  const int tid = threadIdx.x;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t n_items = (int64_t)n_heads * j_count * 2;
+
+  // item -> (head, page, half): consecutive items are the two halves of a page
+  auto coords = [&](int64_t item, int64_t& h, int64_t& j, int& half) {
+    half = (int)(item & 1);
+    const int64_t hp = item >> 1;
+    h = hp / j_count;
+    j = j_begin + hp % j_count;
+  };
+  auto issue = [&](int64_t item, int slot) {
+    int64_t h, j;
+    int half;
+    coords(item, h, j, half);
+    const uint32_t bar = bars + 8 * slot;
+    mbar_expect_tx(bar, kTokBox);
+    tma_tile_g2s(ring + slot * kTokBox, &tm, (int)(h * kH + 64 * half), (int)(j * 256), bar);
+  };
+
+  if (tid == 0) {
+    for (int k = 0; k < kTokSlots; ++k) mbar_init(bars + 8 * k, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = tid; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < kTokSlots; ++k)
+      if (blockIdx.x + (int64_t)k * gridDim.x < n_items) issue(blockIdx.x + (int64_t)k * gridDim.x, k);
+
+  const float eps = tab.eps;
+  const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
+  int k = 0;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+    const int slot = k % kTokSlots, par = k & 1;
+    const bool ok = mbar_wait(bars + 8 * slot, (uint32_t)((k / kTokSlots) & 1));
+    if (__syncthreads_or(!ok)) {
+      // a copy never landed: record it, wait (bounded) for the copies in flight, leave
+      if (tid == 0) {
+        atomicExch(status, 1);
+        for (int u = 1; u < kTokSlots; ++u)
+          if (item + (int64_t)u * gridDim.x < n_items)
+            mbar_wait(bars + 8 * ((k + u) % kTokSlots), (uint32_t)(((k + u) / kTokSlots) & 1));
+      }
+      return;
+    }
+    int64_t h, j;
+    int half;
+    coords(item, h, j, half);
+    const int64_t page = h * n_pp + j;
+    const int64_t t0 = j * 256;
+    const int v = PARTIAL ? (int)min(n_tokens - t0, (int64_t)256) : 256;
+    const int nc = PARTIAL ? min(max(v - 32 * w, 0), 32) : 32;
+
+    // the chunk's 32 tokens of channels 2L and 2L + 1 as BF16 token pairs
+    const uint8_t* tile = smem + slot * kTokBox + (32 * w) * 128 + 4 * lane;
+    uint32_t wa[16], wb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t e = *reinterpret_cast<const uint32_t*>(tile + (2 * i) * 128);
+      const uint32_t o = *reinterpret_cast<const uint32_t*>(tile + (2 * i + 1) * 128);
+      wa[i] = prmt(e, o, 0x5410u);
+      wb[i] = prmt(e, o, 0x7632u);
+    }
+    float2 cmn, cmx;
+    chunk_extremes<PARTIAL>(wa, nc, cmn.x, cmx.x);
+    chunk_extremes<PARTIAL>(wb, nc, cmn.y, cmx.y);
+    s_mn[par][w][lane] = cmn;
+    s_mx[par][w][lane] = cmx;
+    __syncthreads();
+    // every lane holds its values: the slot takes the item kTokSlots ahead
+    if (tid == 0 && item + (int64_t)kTokSlots * gridDim.x < n_items)
+      issue(item + (int64_t)kTokSlots * gridDim.x, slot);
+    float2 mn = s_mn[par][0][lane], mx = s_mx[par][0][lane];
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float2 a = s_mn[par][c][lane], b = s_mx[par][c][lane];
+      mn = make_float2(fminf(mn.x, a.x), fminf(mn.y, a.y));
+      mx = make_float2(fmaxf(mx.x, b.x), fmaxf(mx.y, b.y));
+    }
+    float* mp = meta + page * kMetaFloats;
+    auto encode_one = [&](const uint32_t (&wv)[16], float rmn, float rmx, float chmn, float chmx, int c) {
+      uint32_t o[8];
+      float gscale, mu, sigma;
+      encode_chunk<PARTIAL>(wv, nc, rmn, rmx, chmn, chmx, eps, s_thr, qc, o, gscale, mu, sigma);
+      anchor[(page * kH + c) * 8 + w] = make_uint4(o[0], o[1], o[2], o[3]);
+      residual[(page * kH + c) * 8 + w] = make_uint4(o[4], o[5], o[6], o[7]);
+      if (w == 0) {
+        mp[c] = rmn;
+        mp[kH + c] = gscale;
+      }
+      mp[kMetaMuOff + w * kH + c] = mu;
+      mp[kMetaSigmaOff + w * kH + c] = sigma;
+    };
+    const int c0 = 64 * half + 2 * lane;
+    encode_one(wa, mn.x, mx.x, cmn.x, cmx.x, c0);
+    encode_one(wb, mn.y, mx.y, cmn.y, cmx.y, c0 + 1);
   }
 }
 
@@ -695,11 +824,44 @@ cudaError_t launch_tokens_t(const void* x, int64_t n_tokens, int n_heads, int n_
   return cudaGetLastError();
 }
 
+template <bool PARTIAL>
+cudaError_t launch_tokens_tma(const CUtensorMap& tm, int64_t n_tokens, int n_heads, int n_pp, int j_begin,
+                              int j_count, uint8_t* anchor, uint8_t* residual, float* meta,
+                              const EncodeTables* tab, cudaStream_t s) {
+  const int64_t n_items = (int64_t)n_heads * j_count * 2;
+  if (n_items == 0) return cudaSuccess;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(encode_tokens_tma_kernel<PARTIAL>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTokSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int64_t max_blocks = (int64_t)device_sm_count() * 2;
+  const int blocks = (int)(n_items < max_blocks ? n_items : max_blocks);
+  encode_tokens_tma_kernel<PARTIAL><<<blocks, 256, kTokSmem, s>>>(
+      tm, n_tokens, n_heads, n_pp, j_begin, j_count, reinterpret_cast<uint4*>(anchor),
+      reinterpret_cast<uint4*>(residual), meta, *tab, device_status_ptr());
+  return cudaGetLastError();
+}
+
+// Token-major encode: through the TMA-staged kernel when the input admits a
+// tensor map (16-byte aligned, token stride a multiple of 8 elements), else
+// through the kernel that reads the channels straight from global memory.
 cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
                                  uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
                                  cudaStream_t s) {
   const int n_pp = (int)((n_tokens + 255) / 256);
   const int n_full = (int)(n_tokens / 256);
+  CUtensorMap tm;
+  if (token_map(&tm, x, n_tokens, (int64_t)n_heads * kH, stride)) {
+    cudaError_t e = launch_tokens_tma<false>(tm, n_tokens, n_heads, n_pp, 0, n_full, anchor, residual, meta,
+                                            tab, s);
+    if (e != cudaSuccess || n_full == n_pp) return e;
+    return launch_tokens_tma<true>(tm, n_tokens, n_heads, n_pp, n_full, 1, anchor, residual, meta, tab, s);
+  }
   cudaError_t e = launch_tokens_t<false>(x, n_tokens, n_heads, n_pp, 0, n_full, stride, anchor, residual, meta,
                                          tab, s);
   if (e != cudaSuccess || n_full == n_pp) return e;

@@ -33,16 +33,27 @@ def to_dev(bits: np.ndarray):
 
 
 @pytest.mark.parametrize("n_tokens", [1, 31, 300, 512, 700])
-def test_token_major_parity_against_oracle(cuda_device, n_tokens):
-    """2 heads, token rows wider than the heads (64 unrelated channels per row):
-    codes and metadata against the oracle's encoding of the same tokens, for
-    tails at and around chunk edges and for whole pages."""
+@pytest.mark.parametrize("layout", ["aligned", "unaligned"])
+def test_token_major_parity_against_oracle(cuda_device, n_tokens, layout):
+    """2 heads, token rows wider than the heads: codes and metadata against the
+    oracle's encoding of the same tokens, for tails at and around chunk edges
+    and for whole pages.  "aligned": 64 unrelated channels per row (a
+    16-byte-aligned start and a stride of 320 elements, the TMA-staged kernel);
+    "unaligned": the heads start one element into the row and the stride is
+    259 elements (the kernel that reads global memory directly)."""
     rng = np.random.default_rng(n_tokens)
     n_heads = 2
     n_pp = -(-n_tokens // 256)
     pages = inputs.kv_pages_np(n_heads, 256 * n_pp, 70 + n_tokens, inputs.outlier_pairs(n_heads, 70))
-    rows = token_major(pages, n_heads, n_tokens, 64, rng)
-    a, r, m = L.lynx_encode_tokens(to_dev(rows)[:, :], n_heads)
+    if layout == "aligned":
+        rows = token_major(pages, n_heads, n_tokens, 64, rng)
+        x = to_dev(rows)
+    else:
+        rows = token_major(pages, n_heads, n_tokens, 2, rng)
+        wide = np.concatenate([rng.integers(0, 1 << 16, (n_tokens, 1), dtype=np.uint16), rows], axis=1)
+        x = to_dev(wide)[:, 1:]
+        assert x.stride(0) == 259 and x.data_ptr() % 16 != 0
+    a, r, m = L.lynx_encode_tokens(x, n_heads)
     torch.cuda.synchronize()
     L.lynx_device_status()
     opages, valid = lo.pages_from_tokens(rows, n_heads)
