@@ -233,6 +233,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
   const int TG = a.T * a.G;
   const int max_keys = a.max_pages * kP;
 
+  wait_prerequisite_grids();   // every global-memory access of this kernel follows it
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
     if (tid == 0) atomicExch(a.status, 3);
@@ -647,6 +648,7 @@ constexpr int kMaxSplits = 1024;
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
   __shared__ float s_w[kMaxSplits];
   __shared__ float s_red[2][4];
+  allow_dependent_launch();
   wait_prerequisite_grids();
   const int r = blockIdx.x & 3;
   const int rg = blockIdx.x >> 2;
@@ -752,8 +754,7 @@ cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t 
     configured[dev] = true;
   }
   dim3 grid(a.n_splits, a.Hkv * a.n_rg, a.B);
-  decode_split_kernel<MODE><<<grid, kThreads, kSmem, s>>>(a, *lut);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_programmatic(decode_split_kernel<MODE>, grid, dim3(kThreads), kSmem, s, a, *lut);
   if (e != cudaSuccess) return e;
   return launch_combine(a, s);
 }
@@ -761,17 +762,7 @@ cudaError_t launch_mode(const DecodeArgs& a, const LutTables* lut, cudaStream_t 
 // The combine of a decode call, launched as a programmatic dependent of the
 // decode kernel just issued on s (it waits for that grid inside the kernel).
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_rg * kRows, a.Hkv, a.B);
-  cfg.blockDim = dim3(kH, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
+  return launch_programmatic(decode_combine_kernel, dim3(a.n_rg * kRows, a.Hkv, a.B), dim3(kH), 0, s, a);
 }
 
 }  // namespace

@@ -96,6 +96,47 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   const int b = blockIdx.z;
   const int max_keys = a.max_pages * kP;
 
+  const uint32_t s_ring = base + S::kRing;
+  const uint32_t bar_full = base + S::kBar;
+  const uint32_t bar_empty = bar_full + 8 * kSt;
+  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
+
+  // ---- prologue: barriers first; the producer lane starts streaming pages
+  // while the consumer warps fill the value tables and the Q^T fragments
+  if (tid == 0) {
+    for (int st = 0; st < kSt; ++st) {
+      mbar_init(bar_full + 8 * st, 1);
+      mbar_init(bar_empty + 8 * st, kConsumers);
+    }
+    *s_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // value tables (kernel parameters only), by the consumer warps, before the
+  // wait on the kernel ahead in the stream: with a programmatic launch this
+  // overlaps that kernel's tail
+  if (warp < kConsumers) {
+    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
+      const int e = i >> 5, ln = i & 31;
+      if (!FULL) {
+        const float2 v = lut.anc_pair[e];
+        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+        const __half lx = __float2half_rn(v.x - __half2float(hx));
+        const __half ly = __float2half_rn(v.y - __half2float(hy));
+        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+      } else {
+        const float v = lut.full[e];
+        const __half hv = __float2half_rn(v);
+        const __half lv = __float2half_rn(v - __half2float(hv));
+        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+      }
+    }
+  }
+  // every global-memory access of this kernel follows this wait
+  wait_prerequisite_grids();
+
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
     if (tid == 0) atomicExch(a.status, 3);
@@ -119,23 +160,6 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
   const int32_t* pt_row = a.page_table + ((int64_t)b * a.Hkv + h) * a.max_pages;
 
-  const uint32_t s_ring = base + S::kRing;
-  const uint32_t bar_full = base + S::kBar;
-  const uint32_t bar_empty = bar_full + 8 * kSt;
-  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
-
-  // ---- prologue: barriers first, so that the producer lane starts streaming
-  // pages while the consumer warps fill the value tables and the Q^T fragments
-  if (tid == 0) {
-    for (int st = 0; st < kSt; ++st) {
-      mbar_init(bar_full + 8 * st, 1);
-      mbar_init(bar_empty + 8 * st, kConsumers);
-    }
-    *s_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
   float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};   // query rows 2t, 2t + 1
   float l_run[2] = {0.0f, 0.0f};
   // O[mt]: (channel 16 mt + g, rows 2t, 2t+1), (channel 16 mt + g + 8, rows 2t, 2t+1)
@@ -148,25 +172,8 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
-    // value tables and Q^T fragments, by the 8 consumer warps only; they meet at
-    // named barrier 1 (the producer warp never takes part in it)
-    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
-      const int e = i >> 5, ln = i & 31;
-      if (!FULL) {
-        const float2 v = lut.anc_pair[e];
-        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
-        const __half lx = __float2half_rn(v.x - __half2float(hx));
-        const __half ly = __float2half_rn(v.y - __half2float(hy));
-        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
-        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
-      } else {
-        const float v = lut.full[e];
-        const __half hv = __float2half_rn(v);
-        const __half lv = __float2half_rn(v - __half2float(hv));
-        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
-        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
-      }
-    }
+    // the Q^T fragments; the consumer warps meet at named barrier 1 (the
+    // producer warp never takes part in it)
     // entry (ks, lane, e): query row g' (= lane >> 2), channel 8 ks + t' + 4e; BF16 is exact in TF32
     for (int i = tid; i < 16 * 32 * 2; i += kConsumerThreads) {
       const int e = i & 1, ln = (i >> 1) & 31, ks = i >> 6;
@@ -464,8 +471,8 @@ cudaError_t launch_narrow(const DecodeArgs& a, const LutTables* lut, cudaStream_
     tvr = tva;
   }
   dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + kNr - 1) / kNr), a.B);
-  decode_narrow_kernel<FULL><<<grid, kThreadsQ, kSmem, s>>>(a, *lut, tka, tva, tkr, tvr);
-  return cudaGetLastError();
+  return launch_programmatic(decode_narrow_kernel<FULL>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
+                             tvr);
 }
 
 }  // namespace

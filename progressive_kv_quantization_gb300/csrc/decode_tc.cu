@@ -171,6 +171,59 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   const int b = blockIdx.z;
   const int max_keys = a.max_pages * kP;
 
+  const uint32_t s_ring = base + S::kRing;
+  const uint32_t bar_full = base + S::kBar;
+  const uint32_t bar_empty = bar_full + 8 * kSt;
+  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
+
+  // ---- prologue: barriers and TMEM first; the producer lane starts streaming
+  // pages while the consumer warps fill the value tables and the Q fragments
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
+  if (tid == 0) {
+    for (int st = 0; st < kSt; ++st) {
+      mbar_init(bar_full + 8 * st, 1);
+      mbar_init(bar_empty + 8 * st, kConsumers);
+    }
+    *s_flag = 0;
+    *s_qmax = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (kTmem && warp == 0) {
+    tmem_alloc(base + S::kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (kTmem) tmem_fence_before_sync();
+  __syncthreads();
+  if (kTmem) tmem_fence_after_sync();
+  uint32_t tmem = 0u;
+  if (kTmem) tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kTmemSlot);
+  // this warp's 128 columns of its lane quadrant
+  const uint32_t t_warp = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128u * (uint32_t)(warp >> 2);
+  // value tables (kernel parameters only), by the consumer warps, before the
+  // wait on the kernel ahead in the stream: with a programmatic launch this
+  // overlaps that kernel's tail
+  if (warp < kConsumers) {
+    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
+      const int e = i >> 5, ln = i & 31;
+      if (!FULL) {
+        const float2 v = lut.anc_pair[e];
+        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+        const __half lx = __float2half_rn(v.x - __half2float(hx));
+        const __half ly = __float2half_rn(v.y - __half2float(hy));
+        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+      } else {
+        const float v = lut.full[e];
+        const __half hv = __float2half_rn(v);
+        const __half lv = __float2half_rn(v - __half2float(hv));
+        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+      }
+    }
+  }
+  // every global-memory access of this kernel follows this wait
+  wait_prerequisite_grids();
+
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
     if (tid == 0) atomicExch(a.status, 3);
@@ -196,36 +249,6 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
   const int32_t* pt_row = a.page_table + ((int64_t)b * a.Hkv + h) * a.max_pages;
 
-  const uint32_t s_ring = base + S::kRing;
-  const uint32_t bar_full = base + S::kBar;
-  const uint32_t bar_empty = bar_full + 8 * kSt;
-  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
-
-  // ---- prologue: barriers and TMEM first, so that the producer lane starts
-  // streaming pages while the consumer warps fill the value tables and the Q
-  // fragments
-  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
-  if (tid == 0) {
-    for (int st = 0; st < kSt; ++st) {
-      mbar_init(bar_full + 8 * st, 1);
-      mbar_init(bar_empty + 8 * st, kConsumers);
-    }
-    *s_flag = 0;
-    *s_qmax = 0u;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (kTmem && warp == 0) {
-    tmem_alloc(base + S::kTmemSlot, kTmemCols);
-    tmem_relinquish();
-  }
-  if (kTmem) tmem_fence_before_sync();
-  __syncthreads();
-  if (kTmem) tmem_fence_after_sync();
-  uint32_t tmem = 0u;
-  if (kTmem) tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kTmemSlot);
-  // this warp's 128 columns of its lane quadrant
-  const uint32_t t_warp = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128u * (uint32_t)(warp >> 2);
-
   float m_run[NR], l_run[NR];
 #pragma unroll
   for (int rh = 0; rh < NR; ++rh) {
@@ -244,25 +267,8 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
-    // value tables, then the Q fragments, by the 8 consumer warps only; they
-    // meet at named barrier 1 (the producer warp never takes part in it)
-    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
-      const int e = i >> 5, ln = i & 31;
-      if (!FULL) {
-        const float2 v = lut.anc_pair[e];
-        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
-        const __half lx = __float2half_rn(v.x - __half2float(hx));
-        const __half ly = __float2half_rn(v.y - __half2float(hy));
-        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
-        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
-      } else {
-        const float v = lut.full[e];
-        const __half hv = __float2half_rn(v);
-        const __half lv = __float2half_rn(v - __half2float(hv));
-        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
-        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
-      }
-    }
+    // the Q fragments, by the 8 consumer warps only; they meet at named
+    // barrier 1 (the producer warp never takes part in it)
     // Q fragments in fp16, scaled by 2^-eq so that the largest |q| of the CTA's rows
     // lies in [2^14, 2^15) (the other values keep their 8 significant bits unless
     // they are 2^-28 times smaller than it)
@@ -693,8 +699,8 @@ cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s)
     tvr = tva;
   }
   dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + R - 1) / R), a.B);
-  decode_tc_kernel<FULL, R><<<grid, kThreadsQ, kSmem, s>>>(a, *lut, tka, tva, tkr, tvr);
-  return cudaGetLastError();
+  return launch_programmatic(decode_tc_kernel<FULL, R>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
+                             tvr);
 }
 
 }  // namespace

@@ -11,15 +11,37 @@ namespace lynx {
 #ifdef __CUDACC__
 // Programmatic dependent launch.  A decode kernel calls allow_dependent_launch()
 // when its main loop is done, so that the split-combine kernel behind it in the
-// stream is scheduled while the last CTAs finish; the combine calls wait_prerequisite_grids() before its first
-// read, which returns once the decode grid has completed and its writes are
-// visible.  Where nothing was launched with the programmatic attribute both are
-// no-ops.
+// stream is scheduled while the last CTAs finish; the combine calls it as it
+// starts, so that the next decode call can fill its value tables meanwhile.
+// Each of these kernels calls wait_prerequisite_grids() before its first access
+// to global memory; it returns once the kernel ahead in the stream has
+// completed and its writes are visible.  Where nothing was launched with the
+// programmatic attribute both are no-ops.
 __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void wait_prerequisite_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 #endif
+
+// Launch of kernel k on stream s as a programmatic dependent of the kernel
+// ahead of it in the stream: k may start once that kernel's CTAs have all
+// called allow_dependent_launch() (or exited), and must call
+// wait_prerequisite_grids() before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
 
 
 // Page geometry (H channels x P tokens, C-token chunks).
