@@ -442,3 +442,49 @@ def test_decode_replays_in_cuda_graph(cuda_device, llama_pools, entry):
     torch.cuda.synchronize()
     L.lynx_device_status()
     assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e)
+
+
+def test_back_to_back_calls_share_workspace(cuda_device, llama_pools):
+    """Decode calls issued back to back on one stream with one workspace, each
+    call's queries written by a kernel right before it: every output equals the
+    same call made alone after a device synchronisation.  The decode kernels and
+    the split combine are programmatic dependents of the kernel ahead of them;
+    this checks that no call reads its inputs or reuses the workspace before the
+    kernel ahead has finished."""
+    B, Hq, Hkv = 2, 32, 8
+    table = torch.from_numpy(np.stack([contiguous_table(1, Hkv, 32, 64, offset=5 * b)[0]
+                                       for b in range(B)])).cuda()
+    ctx = torch.tensor([8192, 7000], dtype=torch.int32).cuda()
+    ka, kr, km = llama_pools.dev["k"]
+    va, vr, vm = llama_pools.dev["v"]
+    cases = [("anchor", 1), ("full", 8), ("anchor", 4), ("full", 1)]
+    qs = [torch.from_numpy(inputs.queries_np((B, T, Hq, 128), 640 + i).view(np.int16)).view(torch.bfloat16).cuda()
+          for i, (_, T) in enumerate(cases)]
+    n_ws = max(L.lynx_decode_attn_workspace_size(B, T, Hq, Hkv, 128, 32) for _, T in cases)
+    ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device="cuda")
+
+    def call(i, q, o, lse):
+        mode, T = cases[i]
+        full = mode == "full"
+        L.lynx_decode_attn(q, ka, kr if full else None, km, va, vr if full else None, vm, table, ctx, Hkv,
+                           causal=T > 1, out=o, lse=lse, workspace=ws)
+
+    outs = [(torch.empty((B, T, Hq, 128), dtype=torch.float32, device="cuda"),
+             torch.empty((B, T, Hq), dtype=torch.float32, device="cuda")) for _, T in cases]
+    alone = []
+    for i in range(len(cases)):
+        call(i, qs[i], *outs[i])
+        torch.cuda.synchronize()
+        alone.append((outs[i][0].clone(), outs[i][1].clone()))
+    scratch = [torch.empty_like(q) for q in qs]
+    for o, lse in outs:
+        o.zero_()
+        lse.zero_()
+    torch.cuda.synchronize()
+    for i in range(len(cases)):
+        scratch[i].copy_(qs[i])      # a kernel writes this call's queries just before it
+        call(i, scratch[i], *outs[i])
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    for (o, lse), (oa, la) in zip(outs, alone):
+        assert torch.equal(o, oa) and torch.equal(lse, la)
