@@ -76,6 +76,24 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s for a kernel timed alone (the measured
+    burst figure), and where it came from."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def attn_flops(B, T, G, Hkv, n_keys):
+    """Algorithmic attention FLOPs of a decode call: Q K^T and P V, 2 * 128 each
+    per query row per key (4 D T G per token per KV head)."""
+    return 4.0 * 128 * T * G * n_keys * Hkv * B
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -325,6 +343,10 @@ def run_gpu(args, rank, world):
     ms_total = reduce_max(t0.elapsed_time(t1), world, dist if world > 1 else None, dev)
     ms_step = ms_total / args.steps
     gbps_peak, peak_kind = peaks()
+    tflops_peak, _ = tensor_peak()
+    # (B, T) of the decode calls, G = 4, 8 KV heads, 16,384 keys
+    attn_shape = {"decode_anchor_b1": (N_LAYERS, 1), "decode_anchor_b8": (8 * N_LAYERS, 1),
+                  "verify_full_t8": (N_LAYERS, 8), "decode_bf16_b1": (N_LAYERS, 1)}
     kern = {}
     for name, _, launches, head, moved in ks:
         ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[name])
@@ -332,6 +354,11 @@ def run_gpu(args, rank, world):
                       "GBps_moved": round(moved / ms / 1e6, 1),
                       "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3), "launches": launches,
                       "headline_bytes": head, "moved_bytes": moved}
+        if name in attn_shape:
+            B, T = attn_shape[name]
+            tf = attn_flops(B, T, HQ // HKV, HKV, N_TOK) / ms / 1e9
+            kern[name]["attn_tflops"] = round(tf, 1)
+            kern[name]["frac_of_bf16_tensor"] = round(tf / tflops_peak, 4)
     head_total = sum(k[3] for k in ks)
     value = job_value(head_total, world, ms_step)
     dom = max(kern, key=lambda n: kern[n]["ms"])
@@ -742,6 +769,7 @@ def run_decode_sweep(torch, L, inputs, dev, reps=5):
             x[i:i + Hkv * npph] = inputs.kv_pages_torch(Hkv, n_max, 900 + 2 * b + t, outl, dev)
     a, r, m = L.lynx_encode_pages(x)
     gbps_peak, _ = peaks()
+    tflops_peak, _ = tensor_peak()
     rows = []
     for ctx_len in (4096, 16384, 131072):
         mp = ctx_len // 256
@@ -769,11 +797,15 @@ def run_decode_sweep(torch, L, inputs, dev, reps=5):
                     eager = _median_ms(torch, fn, reps)
                     ms = _graph_ms(torch, fn, reps)
                     moved = 2 * B * Hkv * mp * page_bytes
+                    tf = attn_flops(B, T, Hq // Hkv, Hkv, ctx_len) / ms / 1e9
                     rows.append({"ctx": ctx_len, "B": B, "T": T, "kv": mode, "ms": round(ms, 4),
                                  "eager_ms": round(eager, 4), "GBps": round(moved / ms / 1e6, 1),
-                                 "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3)})
+                                 "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3),
+                                 "attn_tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / tflops_peak, 4)})
     del x, a, r, m
     return {"rows": rows, "statistic": f"median of {reps}; ms = CUDA-graph replay, eager_ms = Python call",
+            "tensor_roof": "attn_tflops = 4 * 128 * T * G FLOPs per key per KV head per sequence / ms, against the "
+                           "measured dense bf16 peak (MEASURED_PEAKS bf16_tflops)",
             "l2": "KV read per call 0.1-21 GB: the 4K contexts at B = 1 (25-65 MB) fit in L2"}
 
 
