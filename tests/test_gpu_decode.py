@@ -488,3 +488,17 @@ def test_back_to_back_calls_share_workspace(cuda_device, llama_pools):
     L.lynx_device_status()
     for (o, lse), (oa, la) in zip(outs, alone):
         assert torch.equal(o, oa) and torch.equal(lse, la)
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full"])
+def test_more_than_128_splits(cuda_device, llama_pools, mode):
+    """One KV head whose page table lists the pool's 512 key pages twice
+    (262,144 keys), 8 query heads, B = 1: the plan takes 147 splits of 7 pages,
+    so the split combine gathers more splits than it has threads."""
+    ids = np.concatenate([np.arange(512), np.arange(512)]).astype(np.int32)
+    table = ids[None, None, :]
+    ctx = np.array([262144])
+    q = inputs.queries_np((1, 1, 8, 128), 660)
+    o, lse = run(llama_pools, mode, q, table, ctx, 1, False)
+    ro, rl = reference(llama_pools, mode, q, table, ctx, 1, False)
+    check_attention(o, lse, ro, rl)
