@@ -31,6 +31,7 @@
 // partial outputs across pages; lanes of one channel are reduced at the end.
 
 #include "lynx_internal.cuh"
+#include "tma_ptx.cuh"
 
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -41,7 +42,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 4;
 constexpr int kWsPerCta = kRows * kH + 2 * kRows;   // o[4][128], m[4], l[4]
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per bounded wait
 
 template <int MODE>
 struct Geo;
@@ -97,59 +97,10 @@ static_assert(Layout<kModeBf16>::kTotal <= 232448, "shared memory");
 
 // ---------------------------------------------------------------- PTX helpers
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
+// (mbarrier, bulk-copy and bounded-wait helpers: tma_ptx.cuh)
 
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: gives up after kWaitNs (checked every 256 polls) or 2^26 polls.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -185,7 +136,7 @@ __device__ __forceinline__ void issue_unit(const DecodeArgs& a, int u, int p_beg
     atomicExch(a.status, 2);
     id = 0;
   }
-  const uint32_t dst = smem_addr(ring + slot * G::kUnit);
+  const uint32_t dst = smem_u32(ring + slot * G::kUnit);
   const uint32_t bar = bar0 + slot * 8;
   mbar_expect_tx(bar, G::kUnit);
   if (MODE == kModeBf16) {
@@ -220,7 +171,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
   float* s_redmax = reinterpret_cast<float*>(smem + S::kRedMax);
   float* s_redsum = reinterpret_cast<float*>(smem + S::kRedSum);
   float* s_qs = reinterpret_cast<float*>(smem + S::kQs);
-  const uint32_t bar0 = smem_addr(smem + S::kBar);
+  const uint32_t bar0 = smem_u32(smem + S::kBar);
 
   const int tid = threadIdx.x;
   const int w = tid >> 5;
@@ -315,7 +266,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
     const uint8_t* unitV = ring + (uV % kSt) * G::kUnit;
 
     // ---------------- K unit: per-chunk coefficients
-    if (!mbar_wait_bounded(bar0 + 8 * (uK % kSt), (uK / kSt) & 1)) failed = true;
+    if (!mbar_wait(bar0 + 8 * (uK % kSt), (uK / kSt) & 1)) failed = true;
     if (MODE != kModeBf16 && !failed) {
       const float* km = reinterpret_cast<const float*>(unitK + G::kMetaOff);
       const int blk = w;
@@ -492,7 +443,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
     }
 
     // ---------------- V phase
-    if (!mbar_wait_bounded(bar0 + 8 * (uV % kSt), (uV / kSt) & 1)) failed = true;
+    if (!mbar_wait(bar0 + 8 * (uV % kSt), (uV / kSt) & 1)) failed = true;
     if (!failed) {
       float pb[kRows];
 #pragma unroll
@@ -604,7 +555,7 @@ decode_split_kernel(const DecodeArgs a, const LutTables lut) {
     // drain this CTA's outstanding copies (bounded), record the error, leave
     if (tid == 0) {
       atomicExch(a.status, 1);
-      for (int u = consumed; u < issued; ++u) mbar_wait_bounded(bar0 + 8 * (u % kSt), (u / kSt) & 1);
+      for (int u = consumed; u < issued; ++u) mbar_wait(bar0 + 8 * (u % kSt), (u / kSt) & 1);
     }
     return;
   }
