@@ -655,13 +655,21 @@ def run_comparators(torch, L, b, dev, reps=3):
     rows = {}
     # Lynx split stream (the step's encode output): full codes and the Anchor alone
     t_enc = timed(lambda: L.lynx_encode_pages(x, p, kA, kR, kM))
+    o_buf = torch.empty_like(o_ref)
+    l_buf = torch.empty(o_ref.shape[:-1], dtype=torch.float32, device=dev)
     full_o, _ = L.lynx_decode_attn(q, kA, kR, kM, vA, vR, vM, pt, ctx, HKV, p, workspace=ws)
+    t_full = timed(lambda: L.lynx_decode_attn(q, kA, kR, kM, vA, vR, vM, pt, ctx, HKV, p, out=o_buf, lse=l_buf,
+                                              workspace=ws))
     rows["lynx_full"] = {"bytes_per_value": 1.0 + 9216 / 32768, "encode_ms": round(t_enc, 4),
+                         "decode_ms": round(t_full, 4),
                          "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct(
                              kA[lo:hi], kR[lo:hi], kM[lo:hi], p, out=o, out_dtype=torch.float32)),
                          "attn_vnmse": attn_vnmse(full_o)}
     anc_o, _ = L.lynx_decode_attn(q, kA, None, kM, vA, None, vM, pt, ctx, HKV, p, workspace=ws)
+    t_anc = timed(lambda: L.lynx_decode_attn(q, kA, None, kM, vA, None, vM, pt, ctx, HKV, p, out=o_buf, lse=l_buf,
+                                             workspace=ws))
     rows["lynx_anchor"] = {"bytes_per_value": 0.5 + 9216 / 32768, "encode_ms": round(t_enc, 4),
+                           "decode_ms": round(t_anc, 4),
                            "kv_vnmse": kv_vnmse(lambda lo, hi, o: L.lynx_reconstruct(
                                kA[lo:hi], None, kM[lo:hi], p, out=o, out_dtype=torch.float32)),
                            "attn_vnmse": attn_vnmse(anc_o)}
@@ -677,6 +685,21 @@ def run_comparators(torch, L, b, dev, reps=3):
         if name == "lynx_int4":
             o4, _ = L.lynx_decode_attn_int4(q, codes, meta, codes[PER:], meta[PER:], pt, ctx, HKV, p, workspace=ws)
             ent["attn_vnmse"] = attn_vnmse(o4)
+            ent["decode_ms"] = round(timed(lambda: L.lynx_decode_attn_int4(
+                q, codes, meta, codes[PER:], meta[PER:], pt, ctx, HKV, p, out=o_buf, lse=l_buf, workspace=ws)), 4)
+        elif name.startswith("uniform"):
+            bits = 8 if name == "uniform_int8" else 4
+            if bits == 8:
+                c_lo, c_hi = L.lynx_split_nibbles(codes.view(n, 128, 256))
+                kh, vh = c_hi, c_hi[PER:]
+            else:
+                c_lo, kh, vh = codes.view(n, 128, 128), None, None
+            call = lambda out=None, lse=None: L.lynx_decode_attn_uniform(
+                q, bits, c_lo, kh, meta, c_lo[PER:], vh, meta[PER:], pt, ctx, HKV, out=out, lse=lse, workspace=ws)
+            ou, _ = call()
+            ent["attn_vnmse"] = attn_vnmse(ou)
+            ent["decode_ms"] = round(timed(lambda: call(o_buf, l_buf)), 4)
+            del c_lo, kh, vh
         else:
             rec = L.lynx_reconstruct_variant(codes, meta, name, p)
             o8, _ = L.lynx_decode_attn_bf16(q, rec, rec[PER:], pt, ctx, HKV, workspace=ws)
@@ -703,6 +726,8 @@ def run_comparators(torch, L, b, dev, reps=3):
         r["kv_vnmse"] = float(f"{r['kv_vnmse']:.4g}")
         r["attn_vnmse"] = float(f"{r['attn_vnmse']:.4g}")
     return {"rows": rows, "attention": "B=64, T=1 decode vs the same decode over the BF16 pages",
+            "decode": "decode_ms: the same B=64, T=1 decode through the fused kernel for that format "
+                      "(Lynx-INT8 values are Lynx's full codes)",
             "kv": "token vectors of the 64-layer cache, float32 reconstructions"}
 
 

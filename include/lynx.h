@@ -25,7 +25,8 @@
  *   lynx_encode_tokens    Algorithm 1 reading token-major (paged-attention) KV.
  *   lynx_encode_split, lynx_reconstruct_split
  *                         the split stream at other Anchor / Residual widths.
- *   lynx_encode_variant, lynx_reconstruct_variant, lynx_decode_attn_int4
+ *   lynx_encode_variant, lynx_reconstruct_variant, lynx_decode_attn_int4,
+ *   lynx_decode_attn_uniform, lynx_split_nibbles
  *                         the single-precision comparators of §6.1 (uniform
  *                         INT8 / INT4, Lynx-INT8, Lynx-INT4).
  *
@@ -323,6 +324,33 @@ int lynx_decode_attn_noalloc(const void* q_bf16, int B, int T, int Hq, int Hkv, 
                              int64_t n_pool_pages, const int32_t* page_table, int max_pages,
                              const int32_t* ctx_len, const lynx_params_t* params, float sm_scale,
                              int causal, float* out, float* lse, void* stream);
+
+/* Decode / verification attention over uniform INT-b pages (paper §6.1's
+ * uniform INT8 / INT4 baselines, LYNX_VARIANT_UNIFORM_INT8 / _INT4 codes and
+ * their meta: min[128], scale[128] per page), through the same kernels as
+ * lynx_decode_attn with x = min + scale * Q for every token of a channel row.
+ *   bits 4: k_lo / v_lo are the packed code pools [n][128][128] as
+ *     lynx_encode_variant writes them; k_hi, v_hi must be NULL.
+ *   bits 8: the one-byte codes split by lynx_split_nibbles: k_lo / v_lo the
+ *     low-nibble planes, k_hi / v_hi the high-nibble planes ([n][128][128]
+ *     each).
+ *   k_meta, v_meta: float32 [n][256].  Other arguments, workspace and errors as
+ *   lynx_decode_attn; INVALID_ARG for bits other than 4 and 8 or a missing /
+ *   superfluous high-nibble pool. */
+int lynx_decode_attn_uniform(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim, int bits,
+                             const uint8_t* k_lo, const uint8_t* k_hi, const float* k_meta, const uint8_t* v_lo,
+                             const uint8_t* v_hi, const float* v_meta, int64_t n_pool_pages,
+                             const int32_t* page_table, int max_pages, const int32_t* ctx_len, float sm_scale,
+                             int causal, float* out, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Rows of 256 one-byte codes (e.g. LYNX_VARIANT_UNIFORM_INT8 codes, n_rows =
+ * 128 per page) -> two planes of rows of 128 bytes: lo holds the low nibbles
+ * and hi the high nibbles, token 2j in the low half of byte j and token 2j + 1
+ * in the high half (the layout of the Anchor and Residual planes).  codes, lo,
+ * hi: device, 16-byte aligned, caller-allocated.  Asynchronous on `stream`.
+ * Errors: INVALID_ARG for n_rows < 0 or a NULL pointer; ALIGNMENT. */
+int lynx_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, void* stream);
 
 /* Decode / verification attention over Lynx-INT4 pages (LYNX_VARIANT_LYNX_INT4
  * codes and meta): the draft-decode kernels of lynx_decode_attn with the

@@ -16,6 +16,8 @@ from .lynx import (  # noqa: F401
     lynx_reconstruct_split,
     lynx_reconstruct_variant,
     lynx_decode_attn_int4,
+    lynx_decode_attn_uniform,
+    lynx_split_nibbles,
     lynx_decode_attn,
     lynx_decode_attn_bf16,
     lynx_decode_attn_workspace_size,

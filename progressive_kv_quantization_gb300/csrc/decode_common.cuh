@@ -129,10 +129,11 @@ __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_
     }
     const uint32_t dst = s_ring + st * G::kUnit;
     const uint32_t bar = bar_full + 8 * st;
-    mbar_expect_tx(bar, G::kUnit);
+    const uint32_t meta_bytes = 4u * (uint32_t)a.meta_floats;   // <= kMetaBytes, a multiple of 16
+    mbar_expect_tx(bar, G::kMetaOff + meta_bytes);
     tma_tile_g2s(dst, is_v ? tm_va : tm_ka, 0, (int)(id * kH), bar);
     if (FULL) tma_tile_g2s(dst + G::kResOff, is_v ? tm_vr : tm_kr, 0, (int)(id * kH), bar);
-    bulk_g2s(dst + G::kMetaOff, (is_v ? a.v_meta : a.k_meta) + id * kMetaFloats, kMetaBytes, bar);
+    bulk_g2s(dst + G::kMetaOff, (is_v ? a.v_meta : a.k_meta) + id * a.meta_floats, meta_bytes, bar);
     ++issued;
   }
   if (!ok) {

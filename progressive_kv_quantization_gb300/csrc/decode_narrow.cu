@@ -199,6 +199,7 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
     const bool odd_row = (g & 1) != 0;
     const float eps = a.eps;
     const float sc = a.scale_log2;
+    const bool uniform = a.uniform != 0;
     bool failed = false;
 
     // (A, B) of the unit's 128 channels, stored so that the two channels one
@@ -210,14 +211,19 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int d = L + 32 * k;
-        const float gmin = lds<float>(smem, mt + 4 * d);
-        const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
-        const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
-        const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
+        float2 ab;
+        if (uniform) {   // uniform codes: value = min + scale * code in every chunk
+          ab = make_float2(lds<float>(smem, mt + 4 * d), lds<float>(smem, mt + 4 * (kH + d)));
+        } else {
+          const float gmin = lds<float>(smem, mt + 4 * d);
+          const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
+          const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
+          const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
+          ab = make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+        }
         const int slot = key ? 8 * (d >> 3) + 2 * (d & 3) + ((d >> 2) & 1)
                              : 16 * (d >> 4) + 2 * (d & 7) + ((d >> 3) & 1);
-        *reinterpret_cast<float2*>(smem + s_ab + 8 * slot) =
-            make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+        *reinterpret_cast<float2*>(smem + s_ab + 8 * slot) = ab;
       }
     };
 

@@ -310,6 +310,8 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * t;
     const float eps = a.eps;
     const float sc = a.scale_log2;
+    const bool uniform = a.uniform != 0;
+    const float code_max = a.code_max;
     bool failed = false;
 
     if (kTmem) {   // O = 0 (TMEM contents are undefined after allocation)
@@ -321,7 +323,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     }
 
     // (A, B) of the unit's 128 channels; for a key unit scaled by 2^-ek so that
-    // the largest |A| + |B| (a bound on |k|) lies in [2^14, 2^15), ek returned
+    // the largest |A| + code_max |B| (a bound on |k|) lies in [2^14, 2^15), ek returned
     auto prep_ab = [&](uint32_t unit, bool key) -> int {
       const uint32_t mt = unit + G::kMetaOff;
       float2 ab[4];
@@ -329,12 +331,17 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int d = L + 32 * k;
-        const float gmin = lds<float>(smem, mt + 4 * d);
-        const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
-        const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
-        const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
-        ab[k] = make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
-        mx = fmaxf(mx, fabsf(ab[k].x) + fabsf(ab[k].y));
+        if (uniform) {   // uniform codes: value = min + scale * code in every chunk
+          ab[k] = make_float2(lds<float>(smem, mt + 4 * d), lds<float>(smem, mt + 4 * (kH + d)));
+        } else {
+          const float gmin = lds<float>(smem, mt + 4 * d);
+          const float dg = __fadd_rn(lds<float>(smem, mt + 4 * (kH + d)), eps);
+          const float mu = lds<float>(smem, mt + 4 * (kMetaMuOff + w * kH + d));
+          const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
+          ab[k] = make_float2(__fmaf_rn(dg, mu, gmin), __fmul_rn(dg, ds));
+        }
+        // |k| <= |A| + code_max |B| (code_max bounds the table values)
+        mx = fmaxf(mx, fabsf(ab[k].x) + code_max * fabsf(ab[k].y));
       }
       int ek = 0;
       if (key) {

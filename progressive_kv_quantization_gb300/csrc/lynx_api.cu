@@ -167,6 +167,26 @@ const LutTables* lut_tables4(float alpha, float eps) {
   return &lut;
 }
 
+const LutTables* uniform_tables(int bits) {
+  static LutTables t4, t8;
+  static bool built = false;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!built) {
+    for (int v = 0; v < 16; ++v) t4.anc16[v] = (float)v;
+    for (int byte = 0; byte < 256; ++byte) {
+      t4.anc_pair[byte] = make_float2((float)(byte & 15), (float)(byte >> 4));
+      t4.full[byte] = 0.0f;
+      t8.full[byte] = (float)byte;
+      t8.anc_pair[byte] = make_float2(0.0f, 0.0f);
+    }
+    for (int v = 0; v < 16; ++v) t8.anc16[v] = 0.0f;
+    t4.eps = t8.eps = 0.0f;
+    built = true;
+  }
+  return bits == 8 ? &t8 : &t4;
+}
+
 const LutTables* lut_tables8(float alpha, float eps) {
   thread_local LutTables lut;
   thread_local float cached_alpha = -1.0f, cached_eps = -1.0f;
@@ -380,7 +400,7 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
                   int head_dim, int64_t n_pool, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, float sm_scale, int causal, float* out, float* lse,
                   void* workspace, size_t ws_bytes, float alpha, float eps, void* stream,
-                  bool int4 = false) {
+                  bool int4 = false, const LutTables* uniform_lut = nullptr) {
   int st = check_decode_shape(B, T, Hq, Hkv, head_dim, max_pages);
   if (st != LYNX_OK) return st;
   if (!q || !page_table || !ctx_len || !out) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
@@ -417,7 +437,12 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.causal = causal;
   a.eps = eps;
-  const LutTables* lut = int4 ? lut_tables4(alpha, eps) : lut_tables(alpha, eps);
+  if (a.meta_floats == 0) {   // Lynx metadata unless the caller set the uniform form
+    a.uniform = 0;
+    a.meta_floats = kMetaFloats;
+    a.code_max = 1.0f;
+  }
+  const LutTables* lut = uniform_lut ? uniform_lut : int4 ? lut_tables4(alpha, eps) : lut_tables(alpha, eps);
   cudaError_t e = launch_decode(a, mode, lut, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_decode_attn launch");
   return LYNX_OK;
@@ -485,6 +510,49 @@ int lynx_decode_attn_int4(const void* q_bf16, int B, int T, int Hq, int Hkv, int
   return decode_common(a, kModeAnchor, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table, max_pages,
                        ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes, params->alpha,
                        params->eps, stream, true);
+}
+
+int lynx_decode_attn_uniform(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim, int bits,
+                             const uint8_t* k_lo, const uint8_t* k_hi, const float* k_meta, const uint8_t* v_lo,
+                             const uint8_t* v_hi, const float* v_meta, int64_t n_pool_pages,
+                             const int32_t* page_table, int max_pages, const int32_t* ctx_len, float sm_scale,
+                             int causal, float* out, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  g_last_error[0] = '\0';
+  if (bits != 4 && bits != 8) return fail(LYNX_ERR_INVALID_ARG, "bits=%d (need 4 or 8)", bits);
+  if (!k_lo || !k_meta || !v_lo || !v_meta) return fail(LYNX_ERR_INVALID_ARG, "NULL page pool");
+  if (bits == 8 && (!k_hi || !v_hi))
+    return fail(LYNX_ERR_INVALID_ARG, "bits=8 needs the high-nibble planes k_hi and v_hi");
+  if (bits == 4 && (k_hi || v_hi)) return fail(LYNX_ERR_INVALID_ARG, "bits=4 takes no high-nibble planes");
+  if (misaligned(k_lo) || misaligned(k_meta) || misaligned(v_lo) || misaligned(v_meta) ||
+      (k_hi && misaligned(k_hi)) || (v_hi && misaligned(v_hi)))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  DecodeArgs a{};
+  a.k_anc = k_lo;
+  a.k_res = k_hi;
+  a.k_meta = k_meta;
+  a.v_anc = v_lo;
+  a.v_res = v_hi;
+  a.v_meta = v_meta;
+  a.uniform = 1;
+  a.meta_floats = 2 * kH;
+  a.code_max = bits == 8 ? 255.0f : 15.0f;
+  return decode_common(a, bits == 8 ? kModeFull : kModeAnchor, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages,
+                       page_table, max_pages, ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes,
+                       100.0f, 1e-6f, stream, false, uniform_tables(bits));
+}
+
+int lynx_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, void* stream) {
+  g_last_error[0] = '\0';
+  if (n_rows < 0) return fail(LYNX_ERR_INVALID_ARG, "n_rows=%lld < 0", (long long)n_rows);
+  if (n_rows == 0) return LYNX_OK;
+  if (!codes || !lo || !hi) return fail(LYNX_ERR_INVALID_ARG, "NULL buffer pointer");
+  if (misaligned(codes) || misaligned(lo) || misaligned(hi))
+    return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (n_rows > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_rows too large");
+  cudaError_t e = launch_split_nibbles(codes, n_rows, lo, hi, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_split_nibbles launch");
+  return LYNX_OK;
 }
 
 int lynx_encode_variant(const void* x_bf16, int64_t n_pages, int variant, const lynx_params_t* params,

@@ -85,6 +85,9 @@ const LutTables* lut_tables(float alpha, float eps);
 const EncodeTables* encode_tables4(float alpha, float eps);
 const LutTables* lut_tables4(float alpha, float eps);
 const LutTables* lut_tables8(float alpha, float eps);
+// uniform INT-b codes as table values: anc_pair[byte] = (low nibble, high
+// nibble) and anc16[v] = v (bits 4), full[byte] = byte (bits 8)
+const LutTables* uniform_tables(int bits);
 
 // anchor-only values of an A-bit Anchor (S * l(V 2^R + 2^(R-1) - 1) for the
 // A-bit two's-complement code, 2 <= A <= 6), rounded to float32
@@ -106,6 +109,9 @@ cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8
                           float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s);
 cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, uint8_t* codes, float* meta,
                                   const EncodeTables* tab, cudaStream_t s);
+// rows of 256 one-byte codes -> rows of 128 bytes of low nibbles and of high
+// nibbles (token 2j in the low nibble of byte j, 2j + 1 in the high one)
+cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, cudaStream_t s);
 cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
                                        void* out, int out_dtype, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_encode_split(const void* x, int64_t n_pages, int anchor_bits, uint8_t* anchor,
@@ -148,6 +154,12 @@ struct DecodeArgs {
   float scale_log2;      // sm_scale * log2(e)
   int causal;
   float eps;
+  // page metadata: Lynx's (gamma_min, gamma_scale, mu, sigma; kMetaFloats per
+  // page) or, with `uniform`, a uniform code's (min[128], scale[128]): the value
+  // is min + scale * table value for every chunk
+  int uniform;
+  int meta_floats;
+  float code_max;        // the largest |table value| (1 for Lynx's l~)
 };
 
 struct DecodePlan {

@@ -191,6 +191,33 @@ uniform_reconstruct_kernel(const uint8_t* __restrict__ codes, const float* __res
   }
 }
 
+// One-byte codes -> two nibble planes: thread i takes 16 codes (tokens 16 m ..
+// 16 m + 15 of row r, i = 16 r + m) and writes their low nibbles and their
+// high nibbles as 8 bytes each, token 2j in the low half of byte j.
+__global__ void __launch_bounds__(256)
+split_nibbles_kernel(const uint4* __restrict__ codes, int64_t n_items, uint2* __restrict__ lo,
+                     uint2* __restrict__ hi) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_items;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 c = __ldg(codes + i);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t l[4], h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // bytes b0..b3 -> (b0 & 15) | (b1 & 15) << 4 in byte 0, (b2 & 15) | (b3 & 15) << 4 in byte 2
+      const uint32_t lw = w[k] & 0x0F0F0F0Fu, hw = (w[k] >> 4) & 0x0F0F0F0Fu;
+      l[k] = lw | (lw >> 4);
+      h[k] = hw | (hw >> 4);
+    }
+    auto pack = [](const uint32_t (&v)[4], int k0) {   // bytes 0 and 2 of v[k0], v[k0 + 1]
+      return (v[k0] & 0xFFu) | ((v[k0] >> 8) & 0xFF00u) | ((v[k0 + 1] & 0xFFu) << 16) |
+             ((v[k0 + 1] << 8) & 0xFF000000u);
+    };
+    lo[i] = make_uint2(pack(l, 0), pack(l, 2));
+    hi[i] = make_uint2(pack(h, 0), pack(h, 2));
+  }
+}
+
 // the `bits`-wide two's-complement code at bit position pos of a little-endian
 // bit string held in words w[], sign-extended
 template <int BITS>
@@ -316,6 +343,15 @@ cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* 
 }
 
 }  // namespace
+
+cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, cudaStream_t s) {
+  const int64_t n_items = n_rows * 16;
+  const int64_t need = (n_items + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  split_nibbles_kernel<<<(int)(need < cap ? need : cap), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(codes), n_items, reinterpret_cast<uint2*>(lo), reinterpret_cast<uint2*>(hi));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                                int64_t n_pages, void* out, int out_dtype, const LutTables* lut,

@@ -64,6 +64,9 @@ SIGNATURES = {
                                         _I64, _VP, _I32, _VP, _PP, _F32, _I32, _VP, _VP, _VP]),
     "lynx_attn_merge": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]),
     "lynx_encode_variant": (_I32, [_VP, _I64, _I32, _PP, _VP, _VP, _VP]),
+    "lynx_decode_attn_uniform": (_I32, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                        _I64, _VP, _I32, _VP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "lynx_split_nibbles": (_I32, [_VP, _I64, _VP, _VP, _VP]),
     "lynx_encode_split": (_I32, [_VP, _I64, _I32, _PP, _VP, _VP, _VP, _VP]),
     "lynx_reconstruct_split": (_I32, [_VP, _VP, _VP, _I64, _I32, _PP, _VP, _I32, _VP]),
     "lynx_reconstruct_variant": (_I32, [_VP, _VP, _I64, _I32, _PP, _VP, _I32, _VP]),
@@ -382,6 +385,49 @@ def lynx_decode_attn_int4(q, k_codes, k_meta, v_codes, v_meta, page_table, ctx_l
         _ptr(page_table), max_pages, _ptr(ctx_len), ctypes.byref(p), scale, int(bool(causal)), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "lynx_decode_attn_int4")
+    return out, lse
+
+
+def lynx_split_nibbles(codes, lo=None, hi=None, stream=None):
+    """One-byte codes [n, 128, 256] (e.g. uniform INT8) -> (lo, hi) nibble planes
+    [n, 128, 128]: token 2j in the low half of byte j, 2j + 1 in the high half."""
+    _need(codes, torch.uint8, "codes")
+    if codes.numel() % (H * P) != 0:
+        raise LynxError("codes must hold rows of 256 bytes, 128 rows per page")
+    n = codes.numel() // (H * P)
+    lo = lo if lo is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=codes.device)
+    hi = hi if hi is not None else torch.empty((n, H, P // 2), dtype=torch.uint8, device=codes.device)
+    for t, nm in ((lo, "lo"), (hi, "hi")):
+        _need(t, torch.uint8, nm)
+        if t.numel() < n * PLANE_BYTES:
+            raise LynxError(f"{nm} too small")
+    _check(load().lynx_split_nibbles(_ptr(codes), n * H, _ptr(lo), _ptr(hi), _stream(stream)), "lynx_split_nibbles")
+    return lo, hi
+
+
+def lynx_decode_attn_uniform(q, bits, k_lo, k_hi, k_meta, v_lo, v_hi, v_meta, page_table, ctx_len, n_kv_heads,
+                             sm_scale=None, causal=False, out=None, lse=None, workspace=None, stream=None):
+    """Attention of q over uniform INT-b page pools (lynx_encode_variant(...,
+    "uniform_int4" / "uniform_int8")): bits 4 takes the packed codes as k_lo /
+    v_lo (k_hi = v_hi = None); bits 8 the nibble planes of lynx_split_nibbles."""
+    B, T, Hq, D, max_pages, out, lse, workspace = _decode_prep(q, page_table, ctx_len, n_kv_heads,
+                                                               out, lse, workspace)
+    for t, nm in ((k_lo, "k_lo"), (v_lo, "v_lo")):
+        _need(t, torch.uint8, nm)
+    for t, nm in ((k_meta, "k_meta"), (v_meta, "v_meta")):
+        _need(t, torch.float32, nm)
+    n_pool = min(k_lo.numel(), v_lo.numel()) // PLANE_BYTES
+    n_pool = min(n_pool, k_meta.numel() // (2 * H), v_meta.numel() // (2 * H))
+    for t in (k_hi, v_hi):
+        if t is not None:
+            _need(t, torch.uint8, "high-nibble pool")
+            n_pool = min(n_pool, t.numel() // PLANE_BYTES)
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D)
+    _check(load().lynx_decode_attn_uniform(
+        _ptr(q), B, T, Hq, n_kv_heads, D, int(bits), _ptr(k_lo), _ptr(k_hi), _ptr(k_meta), _ptr(v_lo), _ptr(v_hi),
+        _ptr(v_meta), n_pool, _ptr(page_table), max_pages, _ptr(ctx_len), scale, int(bool(causal)), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "lynx_decode_attn_uniform")
     return out, lse
 
 

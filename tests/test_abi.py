@@ -155,3 +155,25 @@ def test_split_argument_checks(lynx_lib):
     assert lib.lynx_encode_split(a, 0, 3, ok, None, None, None, None) == 0
     assert lib.lynx_encode_split(ctypes.c_void_p(a.value + 2), 1, 3, ok, a, a, a, None) == -3
     assert lib.lynx_reconstruct_split(a, None, a, 1, 3, ok, a, 9, None) == -1
+
+
+def test_uniform_decode_and_nibble_split_argument_checks(lynx_lib):
+    lib = lynx_lib
+    buf = ctypes.create_string_buffer(64)
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 4)
+
+    def call(bits, k_hi=None, v_hi=None, k_lo=a, T=1):
+        return lib.lynx_decode_attn_uniform(a, 1, T, 32, 8, 128, bits, k_lo, k_hi, a, a, v_hi, a, 4, a, 4, a,
+                                            0.088, 0, a, a, a, 0, None)
+    assert call(6) == -1                     # bits other than 4 and 8
+    assert call(8) == -1                     # bits 8 without the high-nibble planes
+    assert call(4, k_hi=a, v_hi=a) == -1     # bits 4 with them
+    assert call(4, k_lo=None) == -1
+    assert call(4, k_lo=odd) == -3
+    assert call(4, T=33) == -2               # shape checks as lynx_decode_attn
+    assert call(4) == -4                     # no workspace
+    assert lib.lynx_split_nibbles(a, -1, a, a, None) == -1
+    assert lib.lynx_split_nibbles(a, 0, None, None, None) == 0
+    assert lib.lynx_split_nibbles(None, 1, a, a, None) == -1
+    assert lib.lynx_split_nibbles(odd, 1, a, a, None) == -3

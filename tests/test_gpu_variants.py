@@ -1,6 +1,7 @@
 """GPU parity of the single-precision comparators (lynx_encode_variant,
-lynx_reconstruct_variant, lynx_decode_attn_int4) against oracle/baselines.py,
-and their consistency with the split-stream entry points."""
+lynx_reconstruct_variant, lynx_decode_attn_int4, lynx_decode_attn_uniform,
+lynx_split_nibbles) against oracle/baselines.py, and their consistency with the
+split-stream entry points."""
 import math
 
 import numpy as np
@@ -120,24 +121,28 @@ def test_uniform_codes_and_reconstruction(cuda_device, bits):
     assert np.all(err <= 2.0 ** -24 * np.abs(ref) + 1e-30)
 
 
+def _table(B, Hkv, npph):
+    return np.stack([np.stack([(h * npph + np.arange(npph) + b) % (Hkv * npph) for h in range(Hkv)])
+                     for b in range(B)]).astype(np.int32)
+
+
 @pytest.mark.parametrize("T", [1, 8])
 def test_lynx_int4_decode_attention(cuda_device, T):
     """Attention over Lynx-INT4 K and V pools (2 KV heads x 2048 tokens, 8
-    query heads) through the draft kernels (T = 1: 8-row narrow tiles; T = 8
-    causal: 16-row tensor-core tiles) against the float64 oracle over the
-    oracle's dequantisation of the same codes."""
+    query heads) encoded by the oracle, through the draft kernels (T = 1: 8-row
+    narrow tiles; T = 8 causal: 16-row tensor-core tiles), against the float64
+    oracle over the oracle's dequantisation of the same codes."""
     Hkv, Hq, n_tok = 2, 8, 2048
     outl = inputs.outlier_pairs(Hkv, 71)
     pools = {}
     for name, seed in (("k", 711), ("v", 712)):
         bits = inputs.kv_pages_np(Hkv, n_tok, seed, outl)
-        codes, meta = L.lynx_encode_variant(to_dev(bits), "lynx_int4")
-        c_np, m_np = codes.cpu().numpy().reshape(-1, 128, 128), meta.cpu().numpy()
-        pools[name] = (codes, meta, bl.lynx_int4_decode(c_np, m_np, 100.0, EPS))
+        opk, ometa = bl.lynx_int4_encode(bits, 100.0, EPS)
+        pools[name] = (torch.from_numpy(opk).cuda(), torch.from_numpy(ometa).cuda(),
+                       bl.lynx_int4_decode(opk, ometa, 100.0, EPS))
     npph = n_tok // 256
     B = 2
-    table = np.stack([np.stack([(h * npph + np.arange(npph) + b) % (Hkv * npph) for h in range(Hkv)])
-                      for b in range(B)]).astype(np.int32)
+    table = _table(B, Hkv, npph)
     ctx = np.array([2048, 1300], dtype=np.int32)
     q_bits = inputs.queries_np((B, T, Hq, 128), 720 + T)
     q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
@@ -147,6 +152,55 @@ def test_lynx_int4_decode_attention(cuda_device, T):
     torch.cuda.synchronize()
     L.lynx_device_status()
     fetch = lambda ids: (pools["k"][2][ids], pools["v"][2][ids])
+    ro, rl = at.decode_attention(lo.bf16_to_f32(q_bits).astype(np.float64), fetch, table, ctx, Hkv,
+                                 1.0 / math.sqrt(128), T > 1)
+    check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
+
+
+def test_split_nibbles_matches_the_byte_plane(cuda_device):
+    """lynx_split_nibbles on random byte planes: the low- and high-nibble planes
+    hold the bytes' nibbles, token 2j in the low half of byte j."""
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 256, (3, 128, 256), dtype=np.uint8)
+    lo_d, hi_d = L.lynx_split_nibbles(torch.from_numpy(codes).cuda())
+    torch.cuda.synchronize()
+    exp_lo = (codes[..., 0::2] & 15) | ((codes[..., 1::2] & 15) << 4)
+    exp_hi = (codes[..., 0::2] >> 4) | ((codes[..., 1::2] >> 4) << 4)
+    assert np.array_equal(lo_d.cpu().numpy(), exp_lo) and np.array_equal(hi_d.cpu().numpy(), exp_hi)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("T", [1, 8])
+def test_uniform_decode_attention(cuda_device, bits, T):
+    """Attention over uniform INT-b K and V pools encoded by the oracle (2 KV
+    heads x 2048 tokens, 8 query heads; INT8 codes split into nibble planes on
+    the GPU): the draft kernels (T = 1) and the tensor-core tiles (T = 8,
+    causal) against the float64 oracle over min + Q * scale."""
+    Hkv, Hq, n_tok = 2, 8, 2048
+    outl = inputs.outlier_pairs(Hkv, 81)
+    pools = {}
+    for name, seed in (("k", 811), ("v", 812)):
+        xb = inputs.kv_pages_np(Hkv, n_tok, seed + bits, outl)
+        qc, mn, sc = bl.uniform_encode(xb, bits)
+        meta = torch.from_numpy(np.stack([mn, sc], axis=1).reshape(-1, 256).astype(np.float32)).cuda()
+        if bits == 4:
+            lo_p, hi_p = torch.from_numpy(bl.pack_codes4(qc)).cuda(), None
+        else:
+            lo_p, hi_p = L.lynx_split_nibbles(torch.from_numpy(qc).cuda())
+        pools[name] = (lo_p, hi_p, meta, bl.uniform_decode(qc, mn, sc))
+    npph = n_tok // 256
+    B = 2
+    table = _table(B, Hkv, npph)
+    ctx = np.array([2048, 1500], dtype=np.int32)
+    q_bits = inputs.queries_np((B, T, Hq, 128), 830 + T + bits)
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    k, v = pools["k"], pools["v"]
+    o, lse = L.lynx_decode_attn_uniform(q, bits, k[0], k[1], k[2], v[0], v[1], v[2],
+                                        torch.from_numpy(table).cuda(), torch.from_numpy(ctx).cuda(), Hkv,
+                                        causal=T > 1)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    fetch = lambda ids: (k[3][ids], v[3][ids])
     ro, rl = at.decode_attention(lo.bf16_to_f32(q_bits).astype(np.float64), fetch, table, ctx, Hkv,
                                  1.0 / math.sqrt(128), T > 1)
     check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
