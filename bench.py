@@ -467,7 +467,7 @@ def run_e2e(torch, L, b, ks, args, dev):
     ev_cmp = [torch.cuda.Event() for _ in range(n_chunks)]
     ev_free = torch.cuda.Event()
     ev_free.record(comp)
-    steps = max(3, min(args.steps, 5))
+    steps = max(5, min(args.steps, 9))
 
     def one():
         with torch.cuda.stream(s_in):

@@ -71,7 +71,8 @@ struct NLayout {
 static_assert(NLayout<false>::kAlloc <= 232448, "shared memory (anchor, narrow)");
 static_assert(NLayout<true>::kAlloc <= 232448, "shared memory (full, narrow)");
 
-template <bool FULL>
+// UNI: uniform-code metadata (min, scale per channel row) instead of Lynx's
+template <bool FULL, bool UNI>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
                      const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_va,
@@ -199,7 +200,6 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
     const bool odd_row = (g & 1) != 0;
     const float eps = a.eps;
     const float sc = a.scale_log2;
-    const bool uniform = a.uniform != 0;
     bool failed = false;
 
     // (A, B) of the unit's 128 channels, stored so that the two channels one
@@ -212,7 +212,7 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       for (int k = 0; k < 4; ++k) {
         const int d = L + 32 * k;
         float2 ab;
-        if (uniform) {   // uniform codes: value = min + scale * code in every chunk
+        if (UNI) {   // uniform codes: value = min + scale * code in every chunk
           ab = make_float2(lds<float>(smem, mt + 4 * d), lds<float>(smem, mt + 4 * (kH + d)));
         } else {
           const float gmin = lds<float>(smem, mt + 4 * d);
@@ -453,14 +453,14 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   }
 }
 
-template <bool FULL>
+template <bool FULL, bool UNI>
 cudaError_t launch_narrow(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
   constexpr int kSmem = NLayout<FULL>::kAlloc;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_narrow_kernel<FULL>,
+    const cudaError_t e = cudaFuncSetAttribute(decode_narrow_kernel<FULL, UNI>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -477,14 +477,15 @@ cudaError_t launch_narrow(const DecodeArgs& a, const LutTables* lut, cudaStream_
     tvr = tva;
   }
   dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + kNr - 1) / kNr), a.B);
-  return launch_programmatic(decode_narrow_kernel<FULL>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
+  return launch_programmatic(decode_narrow_kernel<FULL, UNI>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
                              tvr);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_narrow(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
-  return full ? launch_narrow<true>(a, lut, s) : launch_narrow<false>(a, lut, s);
+  if (a.uniform) return full ? launch_narrow<true, true>(a, lut, s) : launch_narrow<false, true>(a, lut, s);
+  return full ? launch_narrow<true, false>(a, lut, s) : launch_narrow<false, false>(a, lut, s);
 }
 
 }  // namespace lynx

@@ -142,7 +142,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <bool FULL, int R>
+// UNI: uniform-code metadata (min, scale per channel row) instead of Lynx's
+template <bool FULL, int R, bool UNI>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 decode_tc_kernel(const DecodeArgs a, const LutTables lut,
                  const __grid_constant__ CUtensorMap tm_ka, const __grid_constant__ CUtensorMap tm_va,
@@ -310,8 +311,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * t;
     const float eps = a.eps;
     const float sc = a.scale_log2;
-    const bool uniform = a.uniform != 0;
-    const float code_max = a.code_max;
+    const float code_max = UNI ? a.code_max : 1.0f;
     bool failed = false;
 
     if (kTmem) {   // O = 0 (TMEM contents are undefined after allocation)
@@ -331,7 +331,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int d = L + 32 * k;
-        if (uniform) {   // uniform codes: value = min + scale * code in every chunk
+        if (UNI) {   // uniform codes: value = min + scale * code in every chunk
           ab[k] = make_float2(lds<float>(smem, mt + 4 * d), lds<float>(smem, mt + 4 * (kH + d)));
         } else {
           const float gmin = lds<float>(smem, mt + 4 * d);
@@ -682,14 +682,14 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 // dequantised once for 32 rows), else 16
 constexpr bool tc_wide(int rows, bool) { return rows > 16; }
 
-template <bool FULL, int R>
+template <bool FULL, int R, bool UNI>
 cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s) {
   constexpr int kSmem = TLayout<FULL, R>::kAlloc;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FULL, R>,
+    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FULL, R, UNI>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -706,7 +706,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const LutTables* lut, cudaStream_t s)
     tvr = tva;
   }
   dim3 grid(a.n_splits, a.Hkv * ((a.T * a.G + R - 1) / R), a.B);
-  return launch_programmatic(decode_tc_kernel<FULL, R>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
+  return launch_programmatic(decode_tc_kernel<FULL, R, UNI>, grid, dim3(kThreadsQ), kSmem, s, a, *lut, tka, tva, tkr,
                              tvr);
 }
 
@@ -717,8 +717,12 @@ int tc_rows_per_cta(int rows, bool full) { return tc_wide(rows, full) ? 32 : 16;
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
   const bool wide = tc_wide(a.T * a.G, full);
-  if (!full) return wide ? launch_tc<false, 32>(a, lut, s) : launch_tc<false, 16>(a, lut, s);
-  return wide ? launch_tc<true, 32>(a, lut, s) : launch_tc<true, 16>(a, lut, s);
+  if (a.uniform) {
+    if (!full) return wide ? launch_tc<false, 32, true>(a, lut, s) : launch_tc<false, 16, true>(a, lut, s);
+    return wide ? launch_tc<true, 32, true>(a, lut, s) : launch_tc<true, 16, true>(a, lut, s);
+  }
+  if (!full) return wide ? launch_tc<false, 32, false>(a, lut, s) : launch_tc<false, 16, false>(a, lut, s);
+  return wide ? launch_tc<true, 32, false>(a, lut, s) : launch_tc<true, 16, false>(a, lut, s);
 }
 
 }  // namespace lynx
