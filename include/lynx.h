@@ -44,6 +44,12 @@
  *                mu[8][128], sigma[8][128] (Algorithm 1's metadata; mu and
  *                sigma chunk-major: element [b][c] is chunk b of channel c).
  *                9216 B.
+ *   Streams     The paper's §5 serialises each stream as one contiguous block:
+ *                the Anchor planes of the pages followed immediately by their
+ *                metadata.  Here that block is one caller buffer of
+ *                n * (16384 + 9216) bytes: pass its first n * 16384 bytes as
+ *                `anchor` and the rest as `meta` (16-byte aligned, as every
+ *                offset in it is); the Residual stream is the residual planes.
  *
  * Code definition (per channel c of a page, per token t, chunk b = t / 32):
  *   x_n = (x - gamma_min) / (gamma_scale + eps)              (Stage 1)

@@ -222,3 +222,34 @@ def test_partial_last_page_then_decode(cuda_device):
                                      table.cpu().numpy(), np.array([ctx]), Hkv, 1 / math.sqrt(128), False)
         from lynx_testutil import check_attention
         check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
+
+
+def test_anchor_stream_as_one_contiguous_block(cuda_device):
+    """The Anchor stream as the paper serialises it -- the Anchor planes of all
+    pages followed immediately by their metadata, one buffer -- written by
+    lynx_encode_pages through two views of that buffer, and read back by the
+    reconstruction and the draft decode: results equal those of separate
+    buffers."""
+    n_heads, n_tok = 2, 2048
+    outl = inputs.outlier_pairs(n_heads, 41)
+    x = torch.cat([inputs.kv_pages_torch(n_heads, n_tok, 410 + t, outl, "cuda") for t in range(2)])
+    n = x.shape[0]
+    block = torch.empty(n * (16384 + 9216), dtype=torch.uint8, device="cuda")
+    anc = block[:n * 16384].view(n, 128, 128)
+    meta = block[n * 16384:].view(torch.float32).view(n, 2304)
+    res = torch.empty_like(anc)
+    L.lynx_encode_pages(x, L.Params(), anc, res, meta)
+    a2, r2, m2 = L.lynx_encode_pages(x)
+    torch.cuda.synchronize()
+    assert torch.equal(anc, a2) and torch.equal(res, r2) and torch.equal(meta, m2)
+    assert torch.equal(L.lynx_reconstruct(anc, None, meta), L.lynx_reconstruct(a2, None, m2))
+    npph = n_tok // 256
+    pt = torch.arange(n_heads * npph, dtype=torch.int32, device="cuda").view(1, n_heads, npph)
+    ctx = torch.full((1,), n_tok, dtype=torch.int32, device="cuda")
+    q = inputs.queries_torch((1, 1, 4 * n_heads, 128), 42, "cuda")
+    vo = n_heads * npph
+    o1, l1 = L.lynx_decode_attn(q, anc, None, meta, anc[vo:], None, meta[vo:], pt, ctx, n_heads)
+    o2, l2 = L.lynx_decode_attn(q, a2, None, m2, a2[vo:], None, m2[vo:], pt, ctx, n_heads)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
