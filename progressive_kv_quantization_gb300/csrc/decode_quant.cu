@@ -36,15 +36,35 @@ EncodeTiledFn encode_tiled_fn() {
 }  // namespace
 
 bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool) {
+  // a decode loop passes the same pools call after call: the last few maps of
+  // this host thread are kept (a map depends only on the address and size)
+  struct Entry {
+    const uint8_t* pool;
+    int64_t n_pool;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i)
+    if (cache[i].pool == pool && cache[i].n_pool == n_pool && pool != nullptr) {
+      *m = cache[i].map;
+      return true;
+    }
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)n_pool * kH};
   const cuuint64_t strides[1] = {128};
   const cuuint32_t box[2] = {128, 128};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const bool ok = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (ok) {
+    cache[next] = Entry{pool, n_pool, *m};
+    next = (next + 1) % kEntries;
+  }
+  return ok;
 }
 
 bool token_map(CUtensorMap* m, const void* x, int64_t n_tokens, int64_t row_elems, int64_t stride) {

@@ -9,6 +9,7 @@ There is no fallback: if the library is missing or a call fails, a
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 from dataclasses import dataclass
@@ -42,7 +43,13 @@ class Params:
     C: int = C
 
     def c(self) -> lynx_params_t:
-        return lynx_params_t(self.H, self.P, self.C, self.alpha, self.eps)
+        return _params_struct(self.H, self.P, self.C, self.alpha, self.eps)
+
+
+@functools.lru_cache(maxsize=64)
+def _params_struct(H_, P_, C_, alpha, eps) -> lynx_params_t:
+    """One C struct per parameter set (the library only reads it)."""
+    return lynx_params_t(H_, P_, C_, alpha, eps)
 
 
 _lib = None
@@ -105,12 +112,21 @@ def _check(status: int, what: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # the argtypes are c_void_p, which takes the integer address directly
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device=None):
+    """cudaStream_t of `stream`, or of torch's current stream on `device` (the
+    tensor's device; the current device when None)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device() if device is None else device.index)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _need(t, dtype, name, device=None):
