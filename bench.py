@@ -76,6 +76,9 @@ def peaks():
     return 6800.0, "fallback"
 
 
+NOMINAL_HBM_GBS = 8000.0   # GB300's nominal HBM3e bandwidth (context for frac_of_hbm, which uses the measured copy)
+
+
 def tensor_peak():
     """Dense bf16 tensor-core TFLOP/s for a kernel timed alone (the measured
     burst figure), and where it came from."""
@@ -352,7 +355,8 @@ def run_gpu(args, rank, world):
         ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[name])
         kern[name] = {"ms": round(ms, 4), "GBps_headline": round(head / ms / 1e6, 1),
                       "GBps_moved": round(moved / ms / 1e6, 1),
-                      "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3), "launches": launches,
+                      "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3),
+                      "frac_of_nominal_hbm": round(moved / ms / 1e6 / NOMINAL_HBM_GBS, 3), "launches": launches,
                       "headline_bytes": head, "moved_bytes": moved}
         if name in attn_shape:
             B, T = attn_shape[name]
