@@ -777,6 +777,30 @@ def _graph_ms(torch, fn, reps):
     return statistics.median(ts)
 
 
+def _graph_loop_ms(torch, fn, n_calls=100, reps=3):
+    """Per-call GPU time of ``n_calls`` back-to-back calls captured in one CUDA
+    graph (median of ``reps`` replays / n_calls): a decode loop without the
+    per-replay launch of the graph itself."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n_calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / n_calls)
+    del g
+    return statistics.median(ts)
+
+
 def run_decode_sweep(torch, L, inputs, dev, reps=5):
     """The decode-attention sweep workload: 8 KV heads x 128, 32 query heads,
     contexts 4K / 16K / 128K tokens x batch 1 / 16 x T = 1 / 8 / 32 (causal for
@@ -785,7 +809,9 @@ def run_decode_sweep(torch, L, inputs, dev, reps=5):
     GB/s = KV bytes read (packed planes + metadata, or BF16) / time; median of
     ``reps`` CUDA-event timings of a CUDA-graph replay of the call ("ms") and of
     the eager Python call ("eager_ms", which adds the binding's host-side time
-    wherever the GPU finishes before the host has issued the launches)."""
+    wherever the GPU finishes before the host has issued the launches); calls
+    under 0.1 ms also as a graph of 100 back-to-back calls ("loop_ms" per call,
+    the working set staying in L2 from call to call)."""
     Hkv, Hq, n_max, B_max = 8, 32, 131072, 16
     npph = n_max // 256
     outl = inputs.outlier_pairs(Hkv, 5)
@@ -827,10 +853,13 @@ def run_decode_sweep(torch, L, inputs, dev, reps=5):
                     ms = _graph_ms(torch, fn, reps)
                     moved = 2 * B * Hkv * mp * page_bytes
                     tf = attn_flops(B, T, Hq // Hkv, Hkv, ctx_len) / ms / 1e9
-                    rows.append({"ctx": ctx_len, "B": B, "T": T, "kv": mode, "ms": round(ms, 4),
-                                 "eager_ms": round(eager, 4), "GBps": round(moved / ms / 1e6, 1),
-                                 "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3),
-                                 "attn_tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / tflops_peak, 4)})
+                    row = {"ctx": ctx_len, "B": B, "T": T, "kv": mode, "ms": round(ms, 4),
+                           "eager_ms": round(eager, 4), "GBps": round(moved / ms / 1e6, 1),
+                           "frac_of_hbm": round(moved / ms / 1e6 / gbps_peak, 3),
+                           "attn_tflops": round(tf, 1), "frac_of_bf16_tensor": round(tf / tflops_peak, 4)}
+                    if ms < 0.1:   # small calls: also as a loop of 100 captured calls
+                        row["loop_ms"] = round(_graph_loop_ms(torch, fn), 4)
+                    rows.append(row)
     del x, a, r, m
     return {"rows": rows, "statistic": f"median of {reps}; ms = CUDA-graph replay, eager_ms = Python call",
             "tensor_roof": "attn_tflops = 4 * 128 * T * G FLOPs per key per KV head per sequence / ms, against the "
