@@ -117,21 +117,33 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   // wait on the kernel ahead in the stream: with a programmatic launch this
   // overlaps that kernel's tail
   if (warp < kConsumers) {
-    for (int i = tid; i < 256 * 32; i += kConsumerThreads) {
-      const int e = i >> 5, ln = i & 31;
+    // thread e makes row e of the tables and stores its 32 copies, the copy
+    // index rotated by the lane so that a warp's stores hit different banks
+    {
+      const int e = tid;
       if (!FULL) {
         const float2 v = lut.anc_pair[e];
         const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
         const __half lx = __float2half_rn(v.x - __half2float(hx));
         const __half ly = __float2half_rn(v.y - __half2float(hy));
-        *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
-        *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = make_uint2(h2(hx, hy), h2(lx, ly));
+        const uint2 pv = make_uint2(h2(hx, hy), h2(lx, ly));
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const int ln = (L + k) & 31;
+          *reinterpret_cast<float2*>(smem + S::kLutK + e * 256 + 8 * ln) = v;
+          *reinterpret_cast<uint2*>(smem + S::kLutV + e * 256 + 8 * ln) = pv;
+        }
       } else {
         const float v = lut.full[e];
         const __half hv = __float2half_rn(v);
         const __half lv = __float2half_rn(v - __half2float(hv));
-        *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
-        *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = h2(hv, lv);
+        const uint32_t pv = h2(hv, lv);
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const int ln = (L + k) & 31;
+          *reinterpret_cast<float*>(smem + S::kLutK + e * 256 + 4 * ln) = v;
+          *reinterpret_cast<uint32_t*>(smem + S::kLutK + e * 256 + 128 + 4 * ln) = pv;
+        }
       }
     }
   }
