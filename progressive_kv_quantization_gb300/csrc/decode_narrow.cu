@@ -57,8 +57,8 @@ struct NLayout {
   static constexpr int kLutK = kRing + G::kStages * G::kUnit;
   static constexpr int kLutV = FULL ? kLutK : kLutK + 256 * 256;
   static constexpr int kWarps = kLutV + 256 * 256;
-  static constexpr int kQ = kWarps + kConsumers * kNrWarpBytes;   // uint2 [16 k-steps][32 lanes]
-  static constexpr int kFlag = kQ + 16 * 32 * 8;
+  static constexpr int kQ = kWarps + kConsumers * kNrWarpBytes;   // BF16 pairs [16 k-steps][32 lanes]
+  static constexpr int kFlag = kQ + 16 * 32 * 4;
   static constexpr int kBar = kFlag + 16;
   static constexpr int kTotal = kBar + 2 * G::kStages * 8;
   static constexpr int kAlloc = kTotal + 1024;
@@ -187,14 +187,18 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   } else {
     // the Q^T fragments; the consumer warps meet at named barrier 1 (the
     // producer warp never takes part in it)
-    // entry (ks, lane, e): query row g' (= lane >> 2), channel 8 ks + t' + 4e; BF16 is exact in TF32
-    for (int i = tid; i < 16 * 32 * 2; i += kConsumerThreads) {
-      const int e = i & 1, ln = (i >> 1) & 31, ks = i >> 6;
+    // entry (ks, lane): query row g' (= lane >> 2), BF16 of channel 8 ks + t' in
+    // the low half and of channel 8 ks + t' + 4 in the high half; a BF16 value
+    // shifted into the top half of a word is its exact TF32 operand
+    for (int i = tid; i < 16 * 32; i += kConsumerThreads) {
+      const int ln = i & 31, ks = i >> 5;
       const int row = row0 + (ln >> 2);
-      const int d = 8 * ks + (ln & 3) + 4 * e;
+      const int d = 8 * ks + (ln & 3);
       uint32_t v = 0u;
-      if (row < TG)
-        v = (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + d] << 16;
+      if (row < TG) {
+        const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+        v = (uint32_t)qr[d] | ((uint32_t)qr[d + 4] << 16);
+      }
       reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
@@ -259,7 +263,8 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
         for (int e = 0; e < 4; ++e) sacc[mi][e] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
-        const uint2 qf = lds<uint2>(smem, S::kQ + (ks * 32 + L) * 8);
+        const uint32_t qw = lds<uint32_t>(smem, S::kQ + (ks * 32 + L) * 4);
+        const uint2 qf = make_uint2(qw << 16, qw & 0xFFFF0000u);
         const int c0 = 8 * ks + t, c1 = c0 + 4;
         const float4 ab = lds<float4>(smem, s_ab + 16 * (4 * ks + t));   // (A, B) of c0, c1
         const uint32_t r0 = unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword;
