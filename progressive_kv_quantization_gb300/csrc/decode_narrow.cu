@@ -261,6 +261,17 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[mi][e] = 0.0f;
+      // the plane words of all 16 k-steps first, so that no table lookup
+      // waits on its word's load
+      uint32_t kw[16][2];
+      if (!FULL) {
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const int c0 = 8 * ks + t, c1 = c0 + 4;
+          kw[ks][0] = lds<uint32_t>(smem, unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword);
+          kw[ks][1] = lds<uint32_t>(smem, unitK + c1 * 128 + ((w ^ (c1 & 7)) << 4) + kword);
+        }
+      }
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
         const uint32_t qw = lds<uint32_t>(smem, S::kQ + (ks * 32 + L) * 4);
@@ -269,7 +280,8 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
         const float4 ab = lds<float4>(smem, s_ab + 16 * (4 * ks + t));   // (A, B) of c0, c1
         const uint32_t r0 = unitK + c0 * 128 + ((w ^ (c0 & 7)) << 4) + kword;
         const uint32_t r1 = unitK + c1 * 128 + ((w ^ (c1 & 7)) << 4) + kword;
-        const uint32_t wa0 = lds<uint32_t>(smem, r0), wa1 = lds<uint32_t>(smem, r1);
+        const uint32_t wa0 = FULL ? lds<uint32_t>(smem, r0) : kw[ks][0];
+        const uint32_t wa1 = FULL ? lds<uint32_t>(smem, r1) : kw[ks][1];
         // l~ pairs (even, odd token) of m-tiles 0 and 1 for channels c0, c1
         float2 l00, l01, l10, l11;
         if (!FULL) {
