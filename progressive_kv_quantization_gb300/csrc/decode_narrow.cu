@@ -35,6 +35,13 @@
 // own.  The P^T fragments of the V side (row g, tokens 8t + 4kv + 0..3) come
 // from lane 4 (2t + kv) + (g >> 1) by shuffles.
 //
+// Softmax.  A row's running maximum moves only when one of the chunk's scores
+// exceeds it by more than 2^5 (a warp vote; then the rows take their maxima by
+// shuffles), so most pages skip the max reduction and the rescale, and the
+// probabilities (x 2^10) stay below 2^15, inside fp16.  The chunk's row sums
+// of the fp16 probabilities come from one more MMA pair, ones x P^T, instead
+// of a shuffle reduction.
+//
 // Rounding: P is rounded to fp16 (relative 2^-11); everything else keeps at
 // least ~21 bits, sums are float32.
 
@@ -44,6 +51,8 @@ namespace lynx {
 namespace {
 
 constexpr int kNr = 8;                 // query rows per CTA
+constexpr float kLazyLog2 = 5.0f;      // largest log2 lead of a score over the running maximum
+constexpr uint32_t kOnes2 = 0x3C003C00u;   // fp16 pair (1, 1)
 constexpr int kNrWarpBytes = kH * 8;   // per warp: float2 (A, B) per channel of the current unit
 
 template <bool FULL>
@@ -323,21 +332,32 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       const int pos0 = p * kP + 32 * w + 4 * g;
       const bool all_visible = (p + 1) * kP <= min_vis;
       float pr[2][4];   // [e][j], probabilities x 2^10
-      float corr[2], psum[2];
+      float corr[2], mloc[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mloc = -CUDART_INF_F;
+        mloc[e] = -CUDART_INF_F;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float sv = sacc[j >> 1][2 * (j & 1) + e] * sc;
           if (!all_visible && pos0 + j >= nv[e]) sv = -CUDART_INF_F;
           pr[e][j] = sv;
-          mloc = fmaxf(mloc, sv);
+          mloc[e] = fmaxf(mloc[e], sv);
         }
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-        const float mnew = fmaxf(m_run[e], mloc);
+      }
+      // the running maximum moves only when a score of the chunk exceeds it by
+      // more than kLazyLog2 (then every row of the warp takes its row maximum);
+      // otherwise the probabilities stay below 2^(10 + kLazyLog2), inside fp16
+      const bool grow = __any_sync(0xffffffffu, mloc[0] > m_run[0] + kLazyLog2 || mloc[1] > m_run[1] + kLazyLog2);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mnew = m_run[e];
+        if (grow) {
+          float mr = mloc[e];
+          mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 4));
+          mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 8));
+          mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 16));
+          mnew = fmaxf(m_run[e], mr);
+        }
         corr[e] = (mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[e] - mnew);
         float ps = 0.0f;
 #pragma unroll
@@ -348,10 +368,6 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
           ps += pv;
         }
         l_run[e] = l_run[e] * corr[e] + ps;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        psum[e] = ps;
         m_run[e] = mnew;
       }
       // P^T fragments: b0 / b1 of k-step kv = row g, tokens 8t + 4kv + {0,1} / {2,3},
@@ -367,8 +383,14 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
         pb[kv][0] = odd_row ? y10 : y00;
         pb[kv][1] = odd_row ? y11 : y01;
       }
+      // the chunk's row sums of the fp16 probabilities the V side multiplies,
+      // from a 16 x 32 matrix of ones times P^T (every accumulator row holds
+      // them; the lane's entries 0 and 1 are its rows 2t and 2t + 1)
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(ps4, kOnes2, kOnes2, kOnes2, kOnes2, pb[0][0], pb[0][1]);
+      mma_f16(ps4, kOnes2, kOnes2, kOnes2, kOnes2, pb[1][0], pb[1][1]);
       const float2 cr = make_float2(corr[0], corr[1]);
-      const float2 pss = make_float2(psum[0], psum[1]);
+      const float2 pss = make_float2(ps4[0], ps4[1]);
       const bool rescale = __any_sync(0xffffffffu, corr[0] != 1.0f || corr[1] != 1.0f);
 
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
