@@ -502,3 +502,36 @@ def test_more_than_128_splits(cuda_device, llama_pools, mode):
     o, lse = run(llama_pools, mode, q, table, ctx, 1, False)
     ro, rl = reference(llama_pools, mode, q, table, ctx, 1, False)
     check_attention(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("mode", ["anchor", "full"])
+@pytest.mark.parametrize("T", [1, 2])
+def test_rising_scores_across_pages(cuda_device, mode, T):
+    """Pages ordered so that each one's largest logit exceeds every earlier
+    page's: the running maxima of an online softmax move on nearly every page,
+    by leads from below to well above 2^5 depending on the softmax scale (the
+    draft kernel moves a maximum only when a score leads it by more than 2^5,
+    and otherwise keeps probabilities up to 2^5 times its reference).  Also the
+    reverse order, where the maximum is found on the first page and never
+    moves."""
+    pools = Pools(2, 4096, 21, lazy=True)
+    B, Hq, Hkv, npp = 1, 8, 2, 16
+    G = Hq // Hkv
+    q_bits = inputs.queries_np((B, T, Hq, 128), 960 + T)
+    q = lo.bf16_to_f32(q_bits).astype(np.float64)
+    ctx = np.array([npp * 256])
+    s0 = 1.0 / math.sqrt(128)
+    for mult in (1.0, 8.0, 40.0):
+        scale = s0 * mult
+        for rev in (False, True):
+            table = np.zeros((B, Hkv, npp), dtype=np.int32)
+            for h in range(Hkv):
+                ids = h * npp + np.arange(npp)
+                k = pools.pages("k", mode, ids)                  # [npp][128 channels][256 tokens]
+                qh = q[0, :, h * G:(h + 1) * G].reshape(-1, 128)  # the rows sharing KV head h
+                top = np.einsum("rc,pct->prt", qh, k).max(axis=(1, 2)) * scale
+                order = np.argsort(top)
+                table[0, h] = ids[order[::-1] if rev else order]
+            o, lse = run(pools, mode, q_bits, table, ctx, Hkv, True, scale=scale)
+            ro, rl = at.decode_attention(q, pools.fetch(mode), table, ctx, Hkv, scale, True)
+            check_attention(o, lse, ro, rl)
