@@ -358,12 +358,14 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
           mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 16));
           mnew = fmaxf(m_run[e], mr);
         }
-        corr[e] = (mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[e] - mnew);
+        corr[e] = (!grow || mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[e] - mnew);
+        // p x 2^10 = 2^(s - (m - 10)); a masked score (-inf) gives 0, and a row
+        // with no visible score yet (m = -inf) takes reference 0 instead
+        const float mref = (mnew == -CUDART_INF_F) ? 0.0f : mnew - 10.0f;
         float ps = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float sv = pr[e][j];
-          const float pv = (sv == -CUDART_INF_F) ? 0.0f : exp2f(sv - mnew) * 1024.0f;
+          const float pv = exp2f(pr[e][j] - mref);
           pr[e][j] = pv;
           ps += pv;
         }
