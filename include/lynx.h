@@ -287,7 +287,8 @@ int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float
  *               initialisation and are clobbered.
  * All values of every page a sequence touches must be finite, including the
  * positions past ctx_len in its last page.
- * Limits: 1 <= T <= 32, Hq % Hkv == 0, T * (Hq/Hkv) <= 256, max_pages >= 1,
+ * Limits: 1 <= T <= 64 (the paper's cap of 64 draft tokens, §6.1), Hq % Hkv == 0,
+ *         T * (Hq/Hkv) <= 256, max_pages >= 1,
  * B <= 65535, Hkv * ceil(T*(Hq/Hkv)/4) <= 65535. */
 int lynx_decode_attn(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
                      const uint8_t* k_anc, const uint8_t* k_res, const float* k_meta,
@@ -323,7 +324,11 @@ int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int
  *   Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents (the kernels overwrite all of it that they read, so it
  *   needs no clearing); calls whose kernels overlap on the GPU (different
- *   streams, no ordering between them) race on it and give wrong results. */
+ *   streams, no ordering between them) race on it and give wrong results.
+ *   Device reset: the resolved address is kept for the life of the process;
+ *   after cudaDeviceReset (or any reset of the device's primary context) the
+ *   library reloads its module and the kept address is stale, so do not use
+ *   this entry point on a device after resetting it. */
 int lynx_decode_attn_noalloc(const void* q_bf16, int B, int T, int Hq, int Hkv, int head_dim,
                              const uint8_t* k_anc, const uint8_t* k_res, const float* k_meta,
                              const uint8_t* v_anc, const uint8_t* v_res, const float* v_meta,
@@ -389,6 +394,18 @@ int lynx_attn_merge(const float* o_a, const float* lse_a, const float* o_b, cons
 /* Workspace bytes needed by lynx_decode_attn / lynx_decode_attn_bf16 for the
  * given shape on the current device (0 for invalid shapes). */
 size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages);
+
+/* Test hook (not for production use; off by default): the next n_calls calls
+ * of lynx_decode_attn, lynx_decode_attn_int4 or lynx_decode_attn_uniform made
+ * from this host thread run with a fault planted on the host side of the
+ * launch: the producer of every CTA never issues the copy of its first V page,
+ * and every bounded wait of those kernels gives up after 1 ms instead of 2 s.
+ * The consumers' waits for that page then run out, the kernel records device
+ * error word 1, drains the copies it did issue, frees its tensor memory and
+ * returns; the call's outputs are unspecified.  Used to check that a wait that
+ * runs out leaves the context usable.  n_calls = 0 disarms it.  The paper has
+ * no counterpart.  Errors: INVALID_ARG (n_calls < 0). */
+int lynx_test_inject_wait_timeout(int n_calls);
 
 /* Reads and clears the current device's error word, which kernels set when a
  * bounded wait on a TMA transfer gives up.  Synchronises the device.

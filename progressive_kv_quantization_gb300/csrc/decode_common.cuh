@@ -103,8 +103,10 @@ __device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& e
 // Unit u (K of page u/2 for even u, V for odd u) goes to slot u % kStages once
 // the consumers released that slot's previous unit.  An out-of-range page id
 // is reported (status 2) and page 0 read instead.  A wait that gives up sets
-// status 1 and the CTA's abort flag, then waits (bounded) for the copies
-// already in flight to land before returning.
+// status 1 and the CTA's abort flag.  Before returning, the lane waits
+// (bounded) until every copy it issued has landed: a unit older than the last
+// kStages was consumed before its slot was reused, so only those last units
+// can still be in flight, whether the consumers finished or gave up early.
 template <bool FULL, int STAGES = 3>
 __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np,
                               uint32_t s_ring, uint32_t bar_full, uint32_t bar_empty,
@@ -112,14 +114,17 @@ __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_
                               const CUtensorMap* tm_kr, const CUtensorMap* tm_vr, int* s_flag) {
   using G = QGeo<FULL, STAGES>;
   constexpr int kSt = G::kStages;
-  int issued = 0;
+  const int skip = a.inject_skip - 1;   // -1: no unit is skipped
+  int u_end = 0;                        // units attempted
   bool ok = true;
   for (int u = 0; u < 2 * np; ++u) {
     const int st = u % kSt;
-    if (u >= kSt && !mbar_wait(bar_empty + 8 * st, ((u / kSt) - 1) & 1)) {
+    if (u >= kSt && !mbar_wait(bar_empty + 8 * st, ((u / kSt) - 1) & 1, a.wait_ns)) {
       ok = false;
       break;
     }
+    u_end = u + 1;
+    if (u == skip) continue;   // test hook: this unit's copy is never issued
     const int p = p_begin + (u >> 1);
     const bool is_v = (u & 1) != 0;
     int64_t id = pt_row[p];
@@ -134,15 +139,13 @@ __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_
     tma_tile_g2s(dst, is_v ? tm_va : tm_ka, 0, (int)(id * kH), bar);
     if (FULL) tma_tile_g2s(dst + G::kResOff, is_v ? tm_vr : tm_kr, 0, (int)(id * kH), bar);
     bulk_g2s(dst + G::kMetaOff, (is_v ? a.v_meta : a.k_meta) + id * a.meta_floats, meta_bytes, bar);
-    ++issued;
   }
   if (!ok) {
     atomicExch(a.status, 1);
     *s_flag = 1;
-    // the newest issue of every slot must land before the CTA leaves
-    for (int u = issued - 1; u >= 0 && u >= issued - kSt; --u)
-      mbar_wait(bar_full + 8 * (u % kSt), (u / kSt) & 1);
   }
+  for (int u = u_end - 1; u >= 0 && u >= u_end - kSt; --u)
+    if (u != skip) mbar_wait(bar_full + 8 * (u % kSt), (u / kSt) & 1, a.wait_ns);
 }
 
 }  // namespace

@@ -36,11 +36,12 @@
 // from lane 4 (2t + kv) + (g >> 1) by shuffles.
 //
 // Softmax.  A row's running maximum moves only when one of the chunk's scores
-// exceeds it by more than 2^5 (a warp vote; then the rows take their maxima by
-// shuffles), so most pages skip the max reduction and the rescale, and the
-// probabilities (x 2^10) stay below 2^15, inside fp16.  The chunk's row sums
-// of the fp16 probabilities come from one more MMA pair, ones x P^T, instead
-// of a shuffle reduction.
+// exceeds it by more than 5 in log2 units (a probability factor of 2^5; a warp
+// vote, then the rows take their maxima by shuffles), so most pages skip the
+// max reduction and the rescale, and the probabilities (x 2^10) stay below
+// 2^15, inside fp16.  The chunk's row sums of the fp16 probabilities come from
+// one more MMA pair, ones x P^T, instead of a shuffle reduction; they feed
+// both the output and the normaliser, so the two see the same probabilities.
 //
 // Rounding: P is rounded to fp16 (relative 2^-11); everything else keeps at
 // least ~21 bits, sums are float32.
@@ -259,7 +260,7 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       const uint32_t unitK = S::kRing + sK * G::kUnit;
       const uint32_t unitV = S::kRing + sV * G::kUnit;
 
-      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1));
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1, a.wait_ns));
       if (failed) break;
       prep_ab(unitK, true);
       __syncwarp();
@@ -362,14 +363,8 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
         // p x 2^10 = 2^(s - (m - 10)); a masked score (-inf) gives 0, and a row
         // with no visible score yet (m = -inf) takes reference 0 instead
         const float mref = (mnew == -CUDART_INF_F) ? 0.0f : mnew - 10.0f;
-        float ps = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float pv = exp2f(pr[e][j] - mref);
-          pr[e][j] = pv;
-          ps += pv;
-        }
-        l_run[e] = l_run[e] * corr[e] + ps;
+        for (int j = 0; j < 4; ++j) pr[e][j] = exp2f(pr[e][j] - mref);
         m_run[e] = mnew;
       }
       // P^T fragments: b0 / b1 of k-step kv = row g, tokens 8t + 4kv + {0,1} / {2,3},
@@ -393,10 +388,12 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
       mma_f16(ps4, kOnes2, kOnes2, kOnes2, kOnes2, pb[1][0], pb[1][1]);
       const float2 cr = make_float2(corr[0], corr[1]);
       const float2 pss = make_float2(ps4[0], ps4[1]);
+      l_run[0] = l_run[0] * corr[0] + pss.x;
+      l_run[1] = l_run[1] * corr[1] + pss.y;
       const bool rescale = __any_sync(0xffffffffu, corr[0] != 1.0f || corr[1] != 1.0f);
 
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
-      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1));
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1, a.wait_ns));
       if (failed) break;
       prep_ab(unitV, false);
       __syncwarp();
@@ -456,13 +453,9 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   if (warp < kConsumers) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float lw = l_run[e];
-      lw += __shfl_xor_sync(0xffffffffu, lw, 4);
-      lw += __shfl_xor_sync(0xffffffffu, lw, 8);
-      lw += __shfl_xor_sync(0xffffffffu, lw, 16);
-      if (g == 0) {
+      if (g == 0) {   // every lane of equal t holds the rows' whole-chunk sums
         mm[warp * kNr + 2 * t + e] = m_run[e];
-        ml[warp * kNr + 2 * t + e] = lw;
+        ml[warp * kNr + 2 * t + e] = l_run[e];
       }
     }
 #pragma unroll

@@ -3,8 +3,10 @@
 // Residual phases of §4.2-4.3 deliver) to its two tensor-core kernels, and the
 // TMA tensor maps both use to stream the 4-bit planes.
 //
-//   fewer than 12 query rows per KV head  decode_narrow_kernel, 8 rows per CTA
-//                                          (the draft decode at T = 1)
+//   fewer than 12 query rows per KV head  decode_draft_kernel over Anchor planes
+//                                          with Lynx metadata (the draft decode at
+//                                          T = 1), else decode_narrow_kernel;
+//                                          8 rows per CTA
 //   12 or more                             decode_tc_kernel, 16 or 32 rows per CTA
 //                                          (the T-token verification)
 
@@ -87,6 +89,7 @@ bool n_pool_too_large(int64_t n_pool) { return n_pool <= 0 || n_pool * kH > ((in
 
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s) {
   if (use_tc_rows(a.T * a.G)) return launch_decode_tc(a, full, lut, s);
+  if (!full && !a.uniform) return launch_decode_draft(a, lut, s);
   return launch_decode_narrow(a, full, lut, s);
 }
 

@@ -374,7 +374,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       const uint32_t unitK = S::kRing + sK * G::kUnit;
       const uint32_t unitV = S::kRing + sV * G::kUnit;
 
-      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1));
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1, a.wait_ns));
       if (failed) break;
       const int ek = prep_ab(unitK, true);
       __syncwarp();
@@ -505,7 +505,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       const bool rescale = __any_sync(0xffffffffu, any_corr);
 
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
-      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1));
+      failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1, a.wait_ns));
       if (failed) break;
       prep_ab(unitV, false);
       __syncwarp();

@@ -379,12 +379,17 @@ int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float
 
 namespace {
 
+// quantised decode calls of this host thread still to run with the wait
+// time-out injected (lynx_test_inject_wait_timeout)
+thread_local int g_inject_calls = 0;
+
 int check_decode_shape(int B, int T, int Hq, int Hkv, int head_dim, int max_pages) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || max_pages < 1)
     return fail(LYNX_ERR_INVALID_ARG, "B=%d T=%d Hq=%d Hkv=%d max_pages=%d must be >= 1", B, T, Hq,
                 Hkv, max_pages);
   if (head_dim != kH) return fail(LYNX_ERR_UNSUPPORTED, "head_dim=%d (need 128)", head_dim);
-  if (T > 32) return fail(LYNX_ERR_UNSUPPORTED, "T=%d > 32", T);
+  // the Lynx paper (§6.1) drafts at most 64 tokens, all verified in one pass
+  if (T > 64) return fail(LYNX_ERR_UNSUPPORTED, "T=%d > 64", T);
   if (Hq % Hkv != 0) return fail(LYNX_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
   const int G = Hq / Hkv;
   if (T * G > 256) return fail(LYNX_ERR_UNSUPPORTED, "T*Hq/Hkv=%d > 256", T * G);
@@ -441,6 +446,12 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
     a.uniform = 0;
     a.meta_floats = kMetaFloats;
     a.code_max = 1.0f;
+  }
+  a.wait_ns = kDefaultWaitNs;
+  if (mode != kModeBf16 && g_inject_calls > 0) {   // test hook, off unless armed
+    --g_inject_calls;
+    a.inject_skip = 2;       // the first V unit of every split is never copied
+    a.wait_ns = 1000000ull;  // and every wait gives up after 1 ms
   }
   const LutTables* lut = uniform_lut ? uniform_lut : int4 ? lut_tables4(alpha, eps) : lut_tables(alpha, eps);
   cudaError_t e = launch_decode(a, mode, lut, static_cast<cudaStream_t>(stream));
@@ -679,6 +690,13 @@ int lynx_decode_attn_bf16(const void* q_bf16, int B, int T, int Hq, int Hkv, int
   return decode_common(a, kModeBf16, q_bf16, B, T, Hq, Hkv, head_dim, n_pool_pages, page_table,
                        max_pages, ctx_len, sm_scale, causal, out, lse, workspace, workspace_bytes,
                        100.0f, 1e-6f, stream);
+}
+
+int lynx_test_inject_wait_timeout(int n_calls) {
+  g_last_error[0] = '\0';
+  if (n_calls < 0) return fail(LYNX_ERR_INVALID_ARG, "n_calls=%d < 0", n_calls);
+  g_inject_calls = n_calls;
+  return LYNX_OK;
 }
 
 int lynx_device_status(void) {

@@ -44,6 +44,10 @@ cudaError_t launch_programmatic(void (*k)(KArgs...), dim3 grid, dim3 block, size
 }
 
 
+// A kernel's bounded wait on a copy or a peer gives up after this long (ns)
+// and records an error instead of hanging.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
 // Page geometry (H channels x P tokens, C-token chunks).
 constexpr int kH = 128;
 constexpr int kP = 256;
@@ -160,6 +164,12 @@ struct DecodeArgs {
   int uniform;
   int meta_floats;
   float code_max;        // the largest |table value| (1 for Lynx's l~)
+  // every bounded wait of the quantised decode kernels gives up after wait_ns
+  // nanoseconds (two seconds unless the test hook lynx_test_inject_wait_timeout
+  // armed this call); with inject_skip > 0 (test hook only) the producer never
+  // issues the copy of unit inject_skip - 1 of its split, so that wait runs out
+  unsigned long long wait_ns;
+  int inject_skip;
 };
 
 struct DecodePlan {
@@ -179,6 +189,9 @@ bool use_tc_rows(int rows);
 int tc_rows_per_cta(int rows, bool full);
 constexpr int kNarrowRows = 8;
 cudaError_t launch_decode_narrow(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
+// the draft decode kernel: Anchor planes with Lynx metadata and a table of
+// values |l~| < 1, fewer than 12 query rows per KV head (8 per CTA)
+cudaError_t launch_decode_draft(const DecodeArgs& a, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);

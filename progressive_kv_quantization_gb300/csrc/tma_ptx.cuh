@@ -22,7 +22,7 @@ bool token_map(CUtensorMap* m, const void* x, int64_t n_tokens, int64_t row_elem
 
 namespace {
 
-constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr unsigned long long kWaitNs = kDefaultWaitNs;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,13 +53,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// gives up after kWaitNs (clock checked every 256 polls) or 2^26 polls
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// gives up after limit_ns (clock checked every 256 polls) or 2^26 polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 26); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - t0 > kWaitNs) return false;
+    if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

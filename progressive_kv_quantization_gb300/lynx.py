@@ -81,6 +81,7 @@ SIGNATURES = {
                                      _VP, _PP, _F32, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "lynx_decode_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lynx_device_status": (_I32, []),
+    "lynx_test_inject_wait_timeout": (_I32, [_I32]),
     "lynx_status_string": (ctypes.c_char_p, [_I32]),
     "lynx_last_error": (ctypes.c_char_p, []),
     "lynx_version": (_I32, []),

@@ -30,3 +30,16 @@ def cuda_device(lynx_lib):
         pytest.fail("a CUDA device is required for tests marked gpu")
     torch.cuda.init()
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The rounding-edge code fraction over every GPU code comparison of the run
+    (codes may differ from the oracle's by +-1 only within 1e-5 of an edge, and
+    that fraction must stay below 1e-4)."""
+    import lynx_testutil
+    if lynx_testutil.CODE_TALLY:
+        n = sum(d for d, _ in lynx_testutil.CODE_TALLY)
+        tot = sum(c for _, c in lynx_testutil.CODE_TALLY)
+        worst = max(d / c for d, c in lynx_testutil.CODE_TALLY)
+        terminalreporter.write_line(f"rounding-edge +-1 codes: {n} of {tot} compared ({n / tot:.3g}); "
+                                    f"largest fraction in one check {worst:.3g} (bar 1e-4)")

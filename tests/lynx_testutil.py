@@ -22,6 +22,11 @@ def full_codes(anchor: np.ndarray, residual: np.ndarray) -> np.ndarray:
     return np.where(S > 0, I, -I - 1)
 
 
+# (differing codes, codes compared) of every check_codes call of the session,
+# reported at the end of the run (conftest's terminal summary)
+CODE_TALLY = []
+
+
 def check_codes(gpu_anchor, gpu_res, ora_anchor, ora_res, Y):
     """Codes must be bit-exact except +-1 where the oracle's float64 Y is within
     CODE_EDGE of a rounding edge; returns the fraction of differing codes."""
@@ -38,6 +43,7 @@ def check_codes(gpu_anchor, gpu_res, ora_anchor, ora_res, Y):
         assert np.all(near), f"{n} codes differ, {int((~near).sum())} of them away from a rounding edge"
         assert np.all(step <= 1)
     frac = n / g.size
+    CODE_TALLY.append((n, g.size))
     assert frac < CODE_FRACTION, f"differing-code fraction {frac}"
     return frac
 

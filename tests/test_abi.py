@@ -63,7 +63,7 @@ def test_reconstruct_and_decode_argument_checks(lynx_lib):
     ok = ctypes.byref(_p())
     assert lib.lynx_reconstruct(a, None, a, 1, ok, a, 7, None) == -1
     assert lib.lynx_reconstruct(a, None, a, 0, ok, a, 0, None) == 0
-    # decode: T > 32, Hq not a multiple of Hkv, head_dim != 128, mixed residual pools
+    # decode: T > 64, Hq not a multiple of Hkv, head_dim != 128, mixed residual pools
     args = lambda **kw: dict(dict(q=a, B=1, T=1, Hq=32, Hkv=8, D=128, kr=None, vr=None,
                                   ws=a, wsb=0), **kw)
 
@@ -71,13 +71,15 @@ def test_reconstruct_and_decode_argument_checks(lynx_lib):
         x = args(**kw)
         return lib.lynx_decode_attn(x["q"], x["B"], x["T"], x["Hq"], x["Hkv"], x["D"], a, x["kr"], a,
                                     a, x["vr"], a, 4, a, 4, a, ok, 0.088, 0, a, a, x["ws"], x["wsb"], None)
-    assert call(T=33) == -2
+    assert call(T=65) == -2
+    assert call(T=64, Hq=64) == -2           # T * Hq/Hkv = 512 > 256
     assert call(Hq=30) == -1
     assert call(D=64) == -2
     assert call(kr=a) == -1
     assert call(ws=None) == -4
     assert lib.lynx_decode_attn_workspace_size(1, 1, 32, 8, 128, 64) > 0
-    assert lib.lynx_decode_attn_workspace_size(1, 40, 32, 8, 128, 64) == 0
+    assert lib.lynx_decode_attn_workspace_size(1, 64, 32, 8, 128, 64) > 0
+    assert lib.lynx_decode_attn_workspace_size(1, 65, 32, 8, 128, 64) == 0
 
 
 def test_status_strings(lynx_lib):
@@ -171,7 +173,7 @@ def test_uniform_decode_and_nibble_split_argument_checks(lynx_lib):
     assert call(4, k_hi=a, v_hi=a) == -1     # bits 4 with them
     assert call(4, k_lo=None) == -1
     assert call(4, k_lo=odd) == -3
-    assert call(4, T=33) == -2               # shape checks as lynx_decode_attn
+    assert call(4, T=65) == -2               # shape checks as lynx_decode_attn
     assert call(4) == -4                     # no workspace
     assert lib.lynx_split_nibbles(a, -1, a, a, None) == -1
     assert lib.lynx_split_nibbles(a, 0, None, None, None) == 0

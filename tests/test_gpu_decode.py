@@ -110,9 +110,10 @@ def test_llama8b_layer_draft_decode(cuda_device, llama_pools, mode):
 
 
 @pytest.mark.parametrize("mode", ["anchor", "full", "bf16"])
-@pytest.mark.parametrize("T", [4, 8, 32])
+@pytest.mark.parametrize("T", [4, 8, 32, 33, 48, 64])
 def test_verification_causal_ragged_batch(cuda_device, llama_pools, mode, T):
-    """T-token causal verification over sequences of different, ragged lengths."""
+    """T-token causal verification over sequences of different, ragged lengths,
+    up to the paper's 64 draft tokens (256 query rows per KV head at G = 4)."""
     B, Hq, Hkv = 3, 32, 8
     ctx = np.array([16384, 5000, 300])
     table = np.stack([contiguous_table(1, Hkv, 64, 64, offset=17 * b)[0] for b in range(B)])

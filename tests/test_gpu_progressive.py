@@ -47,3 +47,73 @@ def test_anchor_first_transfer_and_draft_on_the_anchor(cuda_device):
         assert torch.equal(a, b)
     t_anchor, t_full = tr.times_ms()
     assert 0 < t_anchor <= tr.start.elapsed_time(tr.full_ready[0]) <= t_full
+
+
+def test_encode_overlapped_transfer_chains_draft_and_verification(cuda_device):
+    """encode_and_send: each layer is encoded and sent while the next one is
+    encoded (Anchor + metadata on a high-priority stream, the Residual on a
+    low-priority one).  On the receiving side the draft decode of layer l waits
+    only for anchor_ready[l] and the T-token verification of layer l only for
+    full_ready[l].  The received bytes equal a direct encode; the drafts equal
+    the same decode over the sender's planes; the verifications match the
+    float64 oracle over the oracle's own encoding of the same BF16 pages."""
+    import math
+
+    from oracle import attention as at
+    from oracle import lynx_oracle as lo
+
+    from lynx_testutil import EPS, check_attention
+
+    n_layers, Hkv, npph, T = 3, 2, 4, 4
+    per = Hkv * npph
+    out = inputs.outlier_pairs(Hkv, 95)
+    bits = [inputs.kv_pages_np(Hkv, 256 * npph, inputs.layer_seed(95, l, t), out)
+            for l in range(n_layers) for t in range(2)]
+    x_np = np.concatenate(bits)
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).cuda()
+    n = x.shape[0]
+    src = (torch.empty((n, 128, 128), dtype=torch.uint8, device="cuda"),
+           torch.empty((n, 128, 128), dtype=torch.uint8, device="cuda"),
+           torch.empty((n, L.META_FLOATS), dtype=torch.float32, device="cuda"))
+    dst = tuple(torch.zeros_like(t) for t in src)
+    layers = [(2 * l * per, 2 * (l + 1) * per) for l in range(n_layers)]
+    tr = ProgressiveTransfer(layers)
+    Hq = 4 * Hkv
+    q1 = torch.from_numpy(inputs.queries_np((1, 1, Hq, 128), 96).view(np.int16)).view(torch.bfloat16).cuda()
+    qv_np = inputs.queries_np((1, T, Hq, 128), 97)
+    qv = torch.from_numpy(qv_np.view(np.int16)).view(torch.bfloat16).cuda()
+    ctx = torch.tensor([256 * npph], dtype=torch.int32, device="cuda")
+    table = torch.arange(per, dtype=torch.int32, device="cuda").view(1, Hkv, npph)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    tr.encode_and_send(x, src, dst, stream=producer)
+    drafts, verifs = [], []
+    for l, (a, _) in enumerate(layers):
+        kv = lambda t: (t[a:], t[a + per:])
+        with torch.cuda.stream(consumer):
+            consumer.wait_event(tr.anchor_ready[l])
+            (ka, va), (km, vm) = kv(dst[0]), kv(dst[2])
+            drafts.append(L.lynx_decode_attn(q1, ka, None, km, va, None, vm, table, ctx, Hkv)[0])
+            consumer.wait_event(tr.full_ready[l])
+            (kr, vr) = kv(dst[1])
+            verifs.append(L.lynx_decode_attn(qv, ka, kr, km, va, vr, vm, table, ctx, Hkv, causal=True))
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    direct = L.lynx_encode_pages(x)
+    for a_, b_ in zip(direct, dst):
+        assert torch.equal(a_, b_)
+    t_anchor, t_full = tr.times_ms()
+    # every Anchor lands before any Residual; layer l's encode ends before its Anchor lands
+    assert 0 < t_anchor <= min(tr.start.elapsed_time(e) for e in tr.full_ready) <= t_full
+    for l in range(n_layers):
+        assert tr.start.elapsed_time(tr.encoded[l]) <= tr.start.elapsed_time(tr.anchor_ready[l])
+    for l, (a, _) in enumerate(layers):
+        ref = L.lynx_decode_attn(q1, src[0][a:], None, src[2][a:], src[0][a + per:], None, src[2][a + per:],
+                                 table, ctx, Hkv)[0]
+        assert torch.equal(drafts[l], ref)
+        oa, orr, om = lo.encode_pages(x_np[a:a + 2 * per], 100.0, EPS)
+        kf = lo.reconstruct(oa[:per], orr[:per], om[:per], 100.0, EPS)
+        vf = lo.reconstruct(oa[per:], orr[per:], om[per:], 100.0, EPS)
+        ro, rl = at.decode_attention(lo.bf16_to_f32(qv_np).astype(np.float64), lambda ids: (kf[ids], vf[ids]),
+                                     table.cpu().numpy(), np.array([256 * npph]), Hkv, 1 / math.sqrt(128), True)
+        o, lse = verifs[l]
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)

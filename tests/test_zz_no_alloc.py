@@ -55,8 +55,14 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device):
         cl = torch.tensor(ctx, dtype=torch.int32, device="cuda")
         args = (q, ka, kr if full else None, km, va, vr if full else None, vm, table, cl, Hkv)
         o_ref, l_ref = L.lynx_decode_attn(*args, causal=causal)
-        o, l = L.lynx_decode_attn_noalloc(*args, causal=causal)
+        o, l = torch.empty_like(o_ref), torch.empty_like(l_ref)
+        L.lynx_decode_attn_noalloc(*args, causal=causal, out=o, lse=l)   # warm-up: resolves the scratch
         torch.cuda.synchronize()
+        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        L.lynx_decode_attn_noalloc(*args, causal=causal, out=o, lse=l)
+        torch.cuda.synchronize()
+        # the call allocated nothing: neither the device's free memory nor torch's allocator moved
+        assert torch.cuda.mem_get_info()[0] == free0 and torch.cuda.memory_allocated() == alloc0
         L.lynx_device_status()
         _close(o, o_ref)
         _close(l, l_ref)
