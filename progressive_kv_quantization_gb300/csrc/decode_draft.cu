@@ -4,13 +4,9 @@
 // (T x Hq/Hkv <= 8 per CTA, the n = 8 dimension of the mma.sync tiles).
 //
 // CTA: one producer lane streams the split's K and V page units through a
-// 5-slot shared-memory ring (2-D TMA tile for the plane, bulk copy for the
-// metadata).  The 32-token chunk c of every page has two warps: K warp c
-// forms the chunk's scores and probabilities, V warp c (warp 8 + c) folds the
-// probabilities into its output.  They hand the probabilities over through a
-// two-slot shared-memory buffer per chunk guarded by mbarriers, so the two
-// sides of consecutive pages run on different warps at the same time (17
-// warps per SM instead of 9 for one warp per chunk).
+// 6-slot shared-memory ring (2-D TMA tile for the plane, bulk copy for the
+// metadata); 8 consumer warps, warp w owning the 32-token chunk w of every
+// page with its own online softmax, one merge of the 8 chunk states at the end.
 //
 // Dequantisation table.  Each of the 256 plane bytes maps to one 32-bit entry
 // holding the Anchor values l~ of its two nibbles as 15-bit fixed point,
@@ -38,18 +34,19 @@
 //           hold 8t + 4kv + {2, 3}, so an A fragment register is one plane
 //           byte's entry.
 //
-// Lane (g = L >> 2, t = L & 3) of K warp c holds S of query rows 2t, 2t+1 for
-// tokens 4g .. 4g+3 of chunk c; lane L of V warp c holds O of channels
-// 16 mt + g (+ 8) for the same two rows, and receives from lane L of K warp c
-// its P^T fragments and the rows' rescale factors.
+// Lane (g = L >> 2, t = L & 3) holds S of query rows 2t, 2t+1 for tokens
+// 4g .. 4g+3 of its chunk, and O of channels 16 mt + g (+ 8) for the same two
+// rows, so the per-row softmax statistics a lane needs for its output are its
+// own.  The P^T fragments of the V side (row g, tokens 8t + 4kv + 0..3) come
+// from lane 4 (2t + kv) + (g >> 1) by shuffles.
 //
-// Softmax (K warp).  A row's running maximum moves only when one of the
+// Softmax.  A row's running maximum moves only when one of the
 // chunk's scores exceeds it by more than 5 in log2 units (a probability factor
 // of 2^5; a warp vote, then the rows take their maxima by shuffles), so most
 // pages skip the max reduction and the rescale, and the probabilities (x 2^10)
-// stay below 2^15, inside fp16.  The V warp takes the row sums of the fp16
-// probabilities it multiplies from one more MMA pair (ones x P^T), so the
-// normaliser sums exactly the probabilities the output used.
+// stay below 2^15, inside fp16.  The row sums of the fp16 probabilities the V
+// side multiplies come from one more MMA pair (ones x P^T), so the normaliser
+// sums exactly the probabilities the output used.
 //
 // Rounding: P is rounded to fp16 (relative 2^-11) and l~ to 1 / (2 F) absolute;
 // products keep ~21 bits, sums are float32.
@@ -60,11 +57,9 @@ namespace lynx {
 namespace {
 
 constexpr int kDRows = 8;                                 // query rows per CTA
-constexpr int kDChunks = 8;                               // one K warp and one V warp per chunk
-constexpr int kDThreads = (2 * kDChunks + 1) * 32;        // + the producer warp: 544
-constexpr int kDStages = 5;                               // ring slots
-constexpr int kDPSlots = 2;                               // probability hand-over slots per chunk
-constexpr int kDXBytes = 32 * 16 + 32 * 8;                // one hand-over slot: uint4 P^T + float2 corr per lane
+constexpr int kDChunks = 8;                               // consumer warps: one per 32-token chunk
+constexpr int kDThreads = (kDChunks + 1) * 32;            // + the producer warp: 288
+constexpr int kDStages = 6;                               // ring slots
 constexpr float kDLazyLog2 = 5.0f;                        // largest log2 lead of a score over the running maximum
 constexpr uint32_t kDOnes2 = 0x3C003C00u;                 // fp16 pair (1, 1)
 constexpr uint32_t kDP8 = 0x1C001C00u;                    // fp16 pair (2^-8, 2^-8)
@@ -85,15 +80,14 @@ struct DLayout {
   using G = QGeo<false, kDStages>;
   static constexpr int kRing = 0;
   static constexpr int kLut = kRing + kDStages * G::kUnit;           // [byte][256 B]: lane L's copy at 4L
-  static constexpr int kKab = kLut + 256 * 256;                       // K warp c: float2 (A', B') x 128
-  static constexpr int kVab = kKab + kDChunks * kH * 8;               // V warp c: float2 (A - B 2^14/F, B 2^32/F)
-  static constexpr int kX = kVab + kDChunks * kH * 8;                 // hand-over [chunk][slot]
-  static constexpr int kQ = kX + kDChunks * kDPSlots * kDXBytes;      // Q BF16 pairs [64 channel pairs][8 rows]
+  // per warp: float2 per channel of the current unit, (A', B') for a key unit,
+  // (A - B 2^14/F, B 2^32/F) for a value unit
+  static constexpr int kAb = kLut + 256 * 256;
+  static constexpr int kQ = kAb + kDChunks * kH * 8;                  // Q BF16 pairs [64 channel pairs][8 rows]
   static constexpr int kQmax = kQ + 64 * kDRows * 4;                  // u32: largest |q| (BF16 bits)
   static constexpr int kFlag = kQmax + 16;
-  static constexpr int kBar = kFlag + 16;
-  // ring full[kDStages], ring empty[kDStages], hand-over full[8][kDPSlots], hand-over empty[8][kDPSlots]
-  static constexpr int kTotal = kBar + (2 * kDStages + 2 * kDChunks * kDPSlots) * 8;
+  static constexpr int kBar = kFlag + 16;                             // ring full[kDStages], empty[kDStages]
+  static constexpr int kTotal = kBar + 2 * kDStages * 8;
   static constexpr int kAlloc = kTotal + 1024;
   // end-of-kernel merge area (reuses the ring): m[8][8], l[8][8], o[8][8][128]
   static constexpr int kMergeM = 0;
@@ -137,23 +131,19 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   const uint32_t s_ring = base + S::kRing;
   const uint32_t bar_full = base + S::kBar;
   const uint32_t bar_empty = bar_full + 8 * kSt;
-  const uint32_t bar_pfull = bar_empty + 8 * kSt;
-  const uint32_t bar_pempty = bar_pfull + 8 * kDChunks * kDPSlots;
   int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
+  uint32_t* s_q = reinterpret_cast<uint32_t*>(smem + S::kQ);
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
 
   // ---- prologue: barriers first; the producer lane starts streaming pages
-  // while the K warps fill the value table and the Q^T fragments
+  // while the consumer warps fill the value table and the queries
   if (tid == 0) {
     for (int st = 0; st < kSt; ++st) {
       mbar_init(bar_full + 8 * st, 1);
       mbar_init(bar_empty + 8 * st, kDChunks);
     }
-    for (int i = 0; i < kDChunks * kDPSlots; ++i) {
-      mbar_init(bar_pfull + 8 * i, 1);
-      mbar_init(bar_pempty + 8 * i, 1);
-    }
     *s_flag = 0;
-    *reinterpret_cast<uint32_t*>(smem + S::kQmax) = 0u;
+    *s_qmax = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -196,26 +186,23 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   const int32_t* pt_row = a.page_table + ((int64_t)b * a.Hkv + h) * a.max_pages;
   const float eps = a.eps;
 
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};   // K warps: query rows 2t, 2t + 1
-  float l_run[2] = {0.0f, 0.0f};                     // V warps
-  // V warps: O[mt] = (channel 16 mt + g, rows 2t, 2t+1), (channel 16 mt + g + 8, rows 2t, 2t+1)
+  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};   // query rows 2t, 2t + 1
+  float l_run[2] = {0.0f, 0.0f};
+  // O[mt] = (channel 16 mt + g, rows 2t, 2t+1), (channel 16 mt + g + 8, rows 2t, 2t+1)
   float2 O[8][2];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = make_float2(0.f, 0.f);
   bool failed = false;
 
-  if (warp == 2 * kDChunks) {
+  if (warp == kDChunks) {
     if (L == 0)
       produce_units<false, kDStages>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_ka,
                                      &tm_va, s_flag);
-  } else if (warp < kDChunks) {
-    // ================= K warp of chunk w
+  } else {
     const int w = warp;
-    // the query rows as BF16 pairs (K warps only; they meet at named barrier 1):
-    // word (pair p, row r) = channels 2p, 2p + 1 of query row r of this CTA
-    // (0 for padding rows); the CTA's largest |q| sets the fp16 scaling of Q'
-    uint32_t* s_q = reinterpret_cast<uint32_t*>(smem + S::kQ);
-    uint32_t* s_qmax = reinterpret_cast<uint32_t*>(smem + S::kQmax);
+    // the query rows as BF16 pairs (the consumer warps meet at named barrier 1):
+    // word (pair p, row r) = channels 2p, 2p + 1 of query row r of this CTA (0
+    // for padding rows); the CTA's largest |q| sets the fp16 scaling of Q'
     {
       uint32_t qm = 0u;
       for (int i = tid; i < 64 * kDRows; i += kDChunks * 32) {
@@ -232,14 +219,16 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
       atomicMax(s_qmax, qm);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDChunks * 32) : "memory");
-    // exponent of the largest |q| (BF16 bits -> power of two at or above it)
+    // exponent of the largest |q| (BF16 bits -> power of two above it)
     const int eq = (int)((*s_qmax >> 7) & 0xFFu) - 127 + 1;
 
-    const uint32_t s_ab = S::kKab + w * kH * 8;
+    const uint32_t s_ab = S::kAb + w * kH * 8;
     const uint32_t lane4 = 4u * L;
-    // bytes 2 (g & 1) (m-tile 0) and 2 (g & 1) + 1 (m-tile 1) of word g >> 1 of a channel row
+    // K side: bytes 2 (g & 1) (m-tile 0) and 2 (g & 1) + 1 (m-tile 1) of word g >> 1 of a channel row
     const uint32_t ksel0 = byte_sel(2 * (g & 1)), ksel1 = byte_sel(2 * (g & 1) + 1);
     const uint32_t kword = 4 * (g >> 1);
+    // V side: bytes 4t..4t+3 of channel 16 mt + g, word t of its chunk unit
+    const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * t;
     // source lanes of the P^T fragments of V k-steps 0 and 1
     const int src0 = 4 * (2 * t) + (g >> 1), src1 = src0 + 4;
     const bool odd_row = (g & 1) != 0;
@@ -248,9 +237,10 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
 
     for (int i = 0; i < np && !failed; ++i) {
       const int p = p_begin + i;
-      const int uK = 2 * i;
-      const int sK = uK % kSt;
+      const int uK = 2 * i, uV = 2 * i + 1;
+      const int sK = uK % kSt, sV = uV % kSt;
       const uint32_t unitK = S::kRing + sK * G::kUnit;
+      const uint32_t unitV = S::kRing + sV * G::kUnit;
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sK, (uK / kSt) & 1, a.wait_ns));
       if (failed) break;
       // (A', B') of the 128 channels in channel order: A' = A - B 2^14 / F and
@@ -317,10 +307,11 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
         alpha2 = __ffma2_rn(q1, make_float2(ab1.x, ab1.z), alpha2);
         const float2 qp0 = __fmul2_rn(q0, make_float2(ab0.y, ab0.w));
         const float2 qp1 = __fmul2_rn(q1, make_float2(ab1.y, ab1.w));
-        const __half2 h0 = __floats2half2_rn(qp0.x, qp0.y), h1 = __floats2half2_rn(qp1.x, qp1.y);
-        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-        const float2 r0 = __ffma2_rn(f0, make_float2(-1.0f, -1.0f), qp0), r1 = __ffma2_rn(f1, make_float2(-1.0f, -1.0f), qp1);
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(&h0), bh1 = *reinterpret_cast<const uint32_t*>(&h1);
+        const __half2 hh0 = __floats2half2_rn(qp0.x, qp0.y), hh1 = __floats2half2_rn(qp1.x, qp1.y);
+        const float2 f0 = __half22float2(hh0), f1 = __half22float2(hh1);
+        const float2 r0 = __ffma2_rn(f0, make_float2(-1.0f, -1.0f), qp0);
+        const float2 r1 = __ffma2_rn(f1, make_float2(-1.0f, -1.0f), qp1);
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(&hh0), bh1 = *reinterpret_cast<const uint32_t*>(&hh1);
         const uint32_t bl0 = h2(r0.x, r0.y), bl1 = h2(r1.x, r1.y);
         const uint32_t bs0 = hmul2_bits(bh0, kDP8), bs1 = hmul2_bits(bh1, kDP8);
 #pragma unroll
@@ -330,12 +321,13 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
 #pragma unroll
           for (int c = 0; c < 4; ++c) e[c] = lds<uint32_t>(smem, S::kLut + lut_off(kw[ks][c], lane4, sel));
           // a0 / a1: the even / odd token of channels (c0, c0 + 1); a2 / a3: of (c0 + 8, c0 + 9)
-          mma_f16(sacc[mi], prmt(e[0], e[1], kDSelKEvenHi), prmt(e[0], e[1], kDSelKOddHi),
-                  prmt(e[2], e[3], kDSelKEvenHi), prmt(e[2], e[3], kDSelKOddHi), bh0, bh1);
-          mma_f16(sacc[mi], prmt(e[0], e[1], kDSelKEvenHi), prmt(e[0], e[1], kDSelKOddHi),
-                  prmt(e[2], e[3], kDSelKEvenHi), prmt(e[2], e[3], kDSelKOddHi), bl0, bl1);
-          mma_f16(sacc[mi], prmt(e[0], e[1], kDSelKEvenLo), prmt(e[0], e[1], kDSelKOddLo),
-                  prmt(e[2], e[3], kDSelKEvenLo), prmt(e[2], e[3], kDSelKOddLo), bs0, bs1);
+          const uint32_t h0 = prmt(e[0], e[1], kDSelKEvenHi), h1 = prmt(e[0], e[1], kDSelKOddHi);
+          const uint32_t h2_ = prmt(e[2], e[3], kDSelKEvenHi), h3 = prmt(e[2], e[3], kDSelKOddHi);
+          const uint32_t l0 = prmt(e[0], e[1], kDSelKEvenLo), l1 = prmt(e[0], e[1], kDSelKOddLo);
+          const uint32_t l2 = prmt(e[2], e[3], kDSelKEvenLo), l3 = prmt(e[2], e[3], kDSelKOddLo);
+          mma_f16(sacc[mi], h0, h1, h2_, h3, bh0, bh1);
+          mma_f16(sacc[mi], h0, h1, h2_, h3, bl0, bl1);
+          mma_f16(sacc[mi], l0, l1, l2, l3, bs0, bs1);
         }
       }
       __syncwarp();
@@ -394,7 +386,7 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
       // held by lane 4 (2t + kv) + (g >> 1) as its pairs of row 2 (g >> 1) + (g & 1)
       const uint32_t x00 = h2(pr[0][0], pr[0][1]), x01 = h2(pr[0][2], pr[0][3]);
       const uint32_t x10 = h2(pr[1][0], pr[1][1]), x11 = h2(pr[1][2], pr[1][3]);
-      uint32_t pb[2][2];
+      uint32_t pb[2][2], pl[2][2];   // P, and P 2^-8 (the multiplier of the low bytes)
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
         const int src = kv ? src1 : src0;
@@ -402,34 +394,26 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
         const uint32_t y10 = __shfl_sync(0xffffffffu, x10, src), y11 = __shfl_sync(0xffffffffu, x11, src);
         pb[kv][0] = odd_row ? y10 : y00;
         pb[kv][1] = odd_row ? y11 : y01;
+        pl[kv][0] = hmul2_bits(pb[kv][0], kDP8);
+        pl[kv][1] = hmul2_bits(pb[kv][1], kDP8);
       }
-      // ---- hand the fragments and the rows' rescale factors to V warp w
-      const int ps = i % kDPSlots;
-      if (i >= kDPSlots) {
-        failed = __any_sync(0xffffffffu, !mbar_wait(bar_pempty + 8 * (w * kDPSlots + ps), ((i / kDPSlots) - 1) & 1, a.wait_ns));
-        if (failed) break;
-      }
-      const uint32_t xb = S::kX + (w * kDPSlots + ps) * kDXBytes;
-      *reinterpret_cast<uint4*>(smem + xb + 16 * L) = make_uint4(pb[0][0], pb[0][1], pb[1][0], pb[1][1]);
-      *reinterpret_cast<float2*>(smem + xb + 512 + 8 * L) = make_float2(corr[0], corr[1]);
-      __syncwarp();
-      if (L == 0) mbar_arrive(bar_pfull + 8 * (w * kDPSlots + ps));
-    }
-  } else {
-    // ================= V warp of chunk w
-    const int w = warp - kDChunks;
-    const uint32_t s_ab = S::kVab + w * kH * 8;
-    const uint32_t lane4 = 4u * L;
-    // bytes 4t..4t+3 of channel 16 mt + g, word t of its chunk unit
-    const uint32_t vofs = g * 128 + ((w ^ g) << 4) + 4 * t;
-    for (int i = 0; i < np && !failed; ++i) {
-      const int uV = 2 * i + 1;
-      const int sV = uV % kSt;
-      const uint32_t unitV = S::kRing + sV * G::kUnit;
+      // the chunk's row sums of the fp16 probabilities, from a 16 x 32 matrix of
+      // ones times P^T (every accumulator row holds them; the lane's entries 0
+      // and 1 are its rows 2t and 2t + 1)
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(ps4, kDOnes2, kDOnes2, kDOnes2, kDOnes2, pb[0][0], pb[0][1]);
+      mma_f16(ps4, kDOnes2, kDOnes2, kDOnes2, kDOnes2, pb[1][0], pb[1][1]);
+      const float2 pss = make_float2(ps4[0], ps4[1]);
+      const float2 cr = make_float2(corr[0], corr[1]);
+      l_run[0] = l_run[0] * cr.x + pss.x;
+      l_run[1] = l_run[1] * cr.y + pss.y;
+      const bool rescale = __any_sync(0xffffffffu, cr.x != 1.0f || cr.y != 1.0f);
+
+      // ---- V unit: T = u 2^-32 P^T per 16-channel m-tile, folded into O
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1, a.wait_ns));
       if (failed) break;
-      // (A - B 2^14/F, B 2^32/F) of the 128 channels, channels c and c + 8 (c & 8 == 0)
-      // side by side: slot 16 (c >> 4) + 2 (c & 7) + ((c >> 3) & 1)
+      // (A - B 2^14/F, B 2^32/F) of the 128 channels, channels c and c + 8
+      // (c & 8 == 0) side by side: slot 16 (c >> 4) + 2 (c & 7) + ((c >> 3) & 1)
       {
         const uint32_t mt = unitV + G::kMetaOff;
 #pragma unroll
@@ -441,38 +425,10 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
           const float ds = __fadd_rn(lds<float>(smem, mt + 4 * (kMetaSigmaOff + w * kH + d)), eps);
           const float A = __fmaf_rn(dg, mu, gmin), B = __fmul_rn(dg, ds);
           const int slot = 16 * (d >> 4) + 2 * (d & 7) + ((d >> 3) & 1);
-          *reinterpret_cast<float2*>(smem + s_ab + 8 * slot) =
-              make_float2(__fmaf_rn(-B, kDVsum, A), __fmul_rn(B, kDVt));
+          *reinterpret_cast<float2*>(smem + s_ab + 8 * slot) = make_float2(__fmaf_rn(-B, kDVsum, A), __fmul_rn(B, kDVt));
         }
       }
-      // ---- the probabilities of this page's chunk from K warp w
-      const int ps = i % kDPSlots;
-      failed = __any_sync(0xffffffffu, !mbar_wait(bar_pfull + 8 * (w * kDPSlots + ps), (i / kDPSlots) & 1, a.wait_ns));
-      if (failed) break;
-      const uint32_t xb = S::kX + (w * kDPSlots + ps) * kDXBytes;
-      const uint4 pv = lds<uint4>(smem, xb + 16 * L);
-      const float2 cr = lds<float2>(smem, xb + 512 + 8 * L);
       __syncwarp();
-      if (L == 0) mbar_arrive(bar_pempty + 8 * (w * kDPSlots + ps));
-      const uint32_t pb[2][2] = {{pv.x, pv.y}, {pv.z, pv.w}};
-      uint32_t pl[2][2];   // P 2^-8, the multiplier of the low bytes
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) pl[kv][j] = hmul2_bits(pb[kv][j], kDP8);
-      // the chunk's row sums of the fp16 probabilities, from a 16 x 32 matrix of
-      // ones times P^T (every accumulator row holds them; the lane's entries 0
-      // and 1 are its rows 2t and 2t + 1)
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16(ps4, kDOnes2, kDOnes2, kDOnes2, kDOnes2, pb[0][0], pb[0][1]);
-      mma_f16(ps4, kDOnes2, kDOnes2, kDOnes2, kDOnes2, pb[1][0], pb[1][1]);
-      const float2 pss = make_float2(ps4[0], ps4[1]);
-      l_run[0] = l_run[0] * cr.x + pss.x;
-      l_run[1] = l_run[1] * cr.y + pss.y;
-      const bool rescale = __any_sync(0xffffffffu, cr.x != 1.0f || cr.y != 1.0f);
-      __syncwarp();   // every lane's (A - B 2^14/F, B 2^32/F) is in place
-
-      // ---- V unit: T = u 2^-32 P^T per 16-channel m-tile, folded into O
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float4 ab = lds<float4>(smem, s_ab + 16 * (8 * mt + g));   // of 16 mt + g and + 8
@@ -486,10 +442,12 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
           const uint32_t e10 = lds<uint32_t>(smem, S::kLut + lut_off(wa1, lane4, byte_sel(2 * kv)));
           const uint32_t e01 = lds<uint32_t>(smem, S::kLut + lut_off(wa0, lane4, byte_sel(2 * kv + 1)));
           const uint32_t e11 = lds<uint32_t>(smem, S::kLut + lut_off(wa1, lane4, byte_sel(2 * kv + 1)));
-          mma_f16(u, prmt(e00, e00, kDSelHi), prmt(e10, e10, kDSelHi), prmt(e01, e01, kDSelHi),
-                  prmt(e11, e11, kDSelHi), pb[kv][0], pb[kv][1]);
-          mma_f16(u, prmt(e00, e00, kDSelLo), prmt(e10, e10, kDSelLo), prmt(e01, e01, kDSelLo),
-                  prmt(e11, e11, kDSelLo), pl[kv][0], pl[kv][1]);
+          const uint32_t h0 = prmt(e00, e00, kDSelHi), h1 = prmt(e10, e10, kDSelHi);
+          const uint32_t h2_ = prmt(e01, e01, kDSelHi), h3 = prmt(e11, e11, kDSelHi);
+          const uint32_t l0 = prmt(e00, e00, kDSelLo), l1 = prmt(e10, e10, kDSelLo);
+          const uint32_t l2 = prmt(e01, e01, kDSelLo), l3 = prmt(e11, e11, kDSelLo);
+          mma_f16(u, h0, h1, h2_, h3, pb[kv][0], pb[kv][1]);
+          mma_f16(u, l0, l1, l2, l3, pl[kv][0], pl[kv][1]);
         }
         float2 q0 = O[mt][0], q1 = O[mt][1];
         if (rescale) {
@@ -504,10 +462,10 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
       __syncwarp();
       if (L == 0) mbar_arrive(bar_empty + 8 * sV);
     }
-  }
-  if (failed && L == 0) {
-    atomicExch(a.status, 1);
-    *s_flag = 1;
+    if (failed && L == 0) {
+      atomicExch(a.status, 1);
+      *s_flag = 1;
+    }
   }
 
   // ================= merge the 8 chunk states (the ring is idle now)
@@ -518,19 +476,15 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
   float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
   if (warp < kDChunks) {
-    if (g == 0) {
+    if (g == 0) {   // every lane of equal t holds the rows' maxima and whole-chunk sums
       mm[warp * kDRows + 2 * t] = m_run[0];
       mm[warp * kDRows + 2 * t + 1] = m_run[1];
-    }
-  } else if (warp < 2 * kDChunks) {
-    const int w = warp - kDChunks;
-    if (g == 0) {   // every lane of equal t holds the rows' sums
-      ml[w * kDRows + 2 * t] = l_run[0];
-      ml[w * kDRows + 2 * t + 1] = l_run[1];
+      ml[warp * kDRows + 2 * t] = l_run[0];
+      ml[warp * kDRows + 2 * t + 1] = l_run[1];
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const int r = w * kDRows + 2 * t;
+      const int r = warp * kDRows + 2 * t;
       const int c0 = 16 * mt + g;
       mo[r * kH + c0] = O[mt][0].x;
       mo[(r + 1) * kH + c0] = O[mt][0].y;

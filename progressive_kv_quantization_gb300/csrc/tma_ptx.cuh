@@ -53,14 +53,28 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// gives up after limit_ns (clock checked every 256 polls) or 2^26 polls
+// one poll that may suspend the thread for up to hint_ns; a suspended thread
+// resumes as soon as the phase completes, and issues nothing meanwhile
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kPollHintNs = 100000u;   // a waiting thread sleeps in polls of up to 100 us
+// gives up after limit_ns (clock checked after every poll) or 2^26 polls
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 26); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_hint(bar, parity, kPollHintNs)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
