@@ -302,6 +302,11 @@ encode_kernel(const uint4* __restrict__ x, int64_t n_groups, uint4* __restrict__
   __shared__ float s_thr[129];
   for (int i = threadIdx.x; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
   __syncthreads();
+  // launched as a programmatic dependent: every global-memory access follows
+  // the wait for the kernel ahead in the stream, and the next kernel may be
+  // scheduled at once (its CTAs take the SMs as this grid's CTAs leave them)
+  wait_prerequisite_grids();
+  allow_dependent_launch();
 
   const int lane = threadIdx.x & 31;
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -789,16 +794,17 @@ cudaError_t launch_encode_t(const void* x, int64_t n_pages, uint8_t* anchor, uin
                             float* meta, const EncodeTables* tab, const int32_t* valid, cudaStream_t s) {
   const int64_t n_groups = n_pages * 32;
   const int threads = 256;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<PARTIAL>, threads, 0);
-  if (per_sm < 1) per_sm = 1;
+  static int per_sm = 0;   // resident CTAs per SM (a property of the kernel)
+  if (per_sm == 0) {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<PARTIAL>, threads, 0);
+    if (per_sm < 1) per_sm = 1;
+  }
   const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
   const int64_t need = (n_groups + 7) / 8;
   const int blocks = (int)(need < max_blocks ? need : max_blocks);
-  encode_kernel<PARTIAL><<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), n_groups,
-                                                   reinterpret_cast<uint4*>(anchor),
-                                                   reinterpret_cast<uint4*>(residual), meta, *tab, valid);
-  return cudaGetLastError();
+  return launch_programmatic(encode_kernel<PARTIAL>, dim3(blocks), dim3(threads), 0, s,
+                             static_cast<const uint4*>(x), n_groups, reinterpret_cast<uint4*>(anchor),
+                             reinterpret_cast<uint4*>(residual), meta, *tab, valid);
 }
 
 cudaError_t launch_encode(const void* x, int64_t n_pages, uint8_t* anchor, uint8_t* residual,

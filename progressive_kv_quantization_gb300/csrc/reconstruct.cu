@@ -37,6 +37,12 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
   for (int i = threadIdx.x; i < kEntries * 32; i += blockDim.x)
     s_lut[i] = kFull ? lut.full[i >> 5] : lut.anc16[i >> 5];
 
+  // launched as a programmatic dependent: every global-memory access follows
+  // the wait for the kernel ahead in the stream, and the next kernel may be
+  // scheduled at once (its CTAs take the SMs as this grid's CTAs leave them)
+  wait_prerequisite_grids();
+  allow_dependent_launch();
+
   const int tid = threadIdx.x;
   const int w = tid >> 5;
   const int lane = tid & 31;
@@ -331,15 +337,16 @@ cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* 
                    int64_t n_pages, void* out, const LutTables* lut, cudaStream_t s) {
   const int64_t n_groups = n_pages * (kH / 16);
   const int threads = 256;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_kernel<kMode, kF32>, threads, 0);
-  if (per_sm < 1) per_sm = 1;
+  static int per_sm = 0;   // resident CTAs per SM (a property of the kernel)
+  if (per_sm == 0) {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reconstruct_kernel<kMode, kF32>, threads, 0);
+    if (per_sm < 1) per_sm = 1;
+  }
   const int64_t max_blocks = (int64_t)device_sm_count() * per_sm;
   const int blocks = (int)(n_groups < max_blocks ? n_groups : max_blocks);
-  reconstruct_kernel<kMode, kF32><<<blocks, threads, 0, s>>>(
-      reinterpret_cast<const uint32_t*>(anchor), reinterpret_cast<const uint32_t*>(residual), meta,
-      n_groups, out, *lut);
-  return cudaGetLastError();
+  return launch_programmatic(reconstruct_kernel<kMode, kF32>, dim3(blocks), dim3(threads), 0, s,
+                             reinterpret_cast<const uint32_t*>(anchor), reinterpret_cast<const uint32_t*>(residual),
+                             meta, n_groups, out, *lut);
 }
 
 }  // namespace
