@@ -89,11 +89,17 @@ struct DLayout {
   static constexpr int kBar = kFlag + 16;                             // ring full[kDStages], empty[kDStages]
   static constexpr int kTotal = kBar + 2 * kDStages * 8;
   static constexpr int kAlloc = kTotal + 1024;
-  // end-of-kernel merge area (reuses the ring): m[8][8], l[8][8], o[8][8][128]
-  static constexpr int kMergeM = 0;
+  // end-of-kernel merge area (reuses the ring): o[8][8][kMergeStride] (each
+  // chunk's output rows, already scaled by the chunk's factor 2^(m_w - m*); the
+  // padded row stride keeps a warp's stores on 32 banks), then m[8][8],
+  // l[8][8], the factors f[8][8] and the rows' (m*, l*) pairs
+  static constexpr int kMergeStride = kH + 4;
+  static constexpr int kMergeO = 0;
+  static constexpr int kMergeM = kMergeO + kDChunks * kDRows * kMergeStride * 4;
   static constexpr int kMergeL = kMergeM + kDChunks * kDRows * 4;
-  static constexpr int kMergeO = kMergeL + kDChunks * kDRows * 4;
-  static_assert(kMergeO + kDChunks * kDRows * kH * 4 <= kDStages * G::kUnit, "merge area");
+  static constexpr int kMergeF = kMergeL + kDChunks * kDRows * 4;
+  static constexpr int kMergeS = kMergeF + kDChunks * kDRows * 4;
+  static_assert(kMergeS + kDRows * 8 <= kDStages * G::kUnit, "merge area");
   static_assert(kLut % 1024 == 0, "ring slots keep the 1024-byte alignment of swizzled tiles");
 };
 static_assert(DLayout::kAlloc <= 232448, "shared memory (draft decode)");
@@ -202,21 +208,28 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
     const int w = warp;
     // the query rows as BF16 pairs (the consumer warps meet at named barrier 1):
     // word (pair p, row r) = channels 2p, 2p + 1 of query row r of this CTA (0
-    // for padding rows); the CTA's largest |q| sets the fp16 scaling of Q'
+    // for padding rows), from 16-byte loads (thread i < 128: row i >> 4,
+    // channels 8 (i & 15) .. + 7); the CTA's largest |q| sets the fp16 scaling of Q'
     {
       uint32_t qm = 0u;
-      for (int i = tid; i < 64 * kDRows; i += kDChunks * 32) {
-        const int pr = i >> 3, r = i & 7;
+      if (tid < kDRows * 16) {
+        const int r = tid >> 4, v = tid & 15;
         const int row = row0 + r;
-        uint32_t v = 0u;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (row < TG) {
           const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
-          v = (uint32_t)qr[2 * pr] | ((uint32_t)qr[2 * pr + 1] << 16);
+          x = __ldg(reinterpret_cast<const uint4*>(qr) + v);
         }
-        s_q[i] = v;
-        qm = max(qm, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s_q[(4 * v + j) * kDRows + r] = w4[j];
+          qm = max(qm, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
+        }
       }
-      atomicMax(s_qmax, qm);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qm = max(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+      if (L == 0) atomicMax(s_qmax, qm);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDChunks * 32) : "memory");
     // exponent of the largest |q| (BF16 bits -> power of two above it)
@@ -472,24 +485,50 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   __syncthreads();
   allow_dependent_launch();   // the split combine may be scheduled once every CTA is here
   if (*reinterpret_cast<volatile int*>(s_flag) != 0) return;
+  float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
   float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
-  float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
-  if (warp < kDChunks) {
-    if (g == 0) {   // every lane of equal t holds the rows' maxima and whole-chunk sums
-      mm[warp * kDRows + 2 * t] = m_run[0];
-      mm[warp * kDRows + 2 * t + 1] = m_run[1];
-      ml[warp * kDRows + 2 * t] = l_run[0];
-      ml[warp * kDRows + 2 * t + 1] = l_run[1];
+  float* mf = reinterpret_cast<float*>(smem + S::kMergeF);
+  float2* mrow = reinterpret_cast<float2*>(smem + S::kMergeS);
+  constexpr int MS = S::kMergeStride;
+  if (warp < kDChunks && g == 0) {   // every lane of equal t holds the rows' maxima and whole-chunk sums
+    mm[warp * kDRows + 2 * t] = m_run[0];
+    mm[warp * kDRows + 2 * t + 1] = m_run[1];
+    ml[warp * kDRows + 2 * t] = l_run[0];
+    ml[warp * kDRows + 2 * t + 1] = l_run[1];
+  }
+  __syncthreads();
+  // chunk w's factor of row r, 2^(m_w - m*) (0 where the chunk saw no key of the row)
+  if (tid < kDChunks * kDRows) {
+    const int r = tid % kDRows;
+    float mstar = -CUDART_INF_F;
+#pragma unroll
+    for (int ww = 0; ww < kDChunks; ++ww) mstar = fmaxf(mstar, mm[ww * kDRows + r]);
+    const float mw = mm[tid];
+    mf[tid] = (mw == -CUDART_INF_F) ? 0.0f : exp2f(mw - mstar);
+  }
+  __syncthreads();
+  // each row's (m*, l*); each lane's O values, scaled by its chunk's factors,
+  // into the chunk's rows of the merge area
+  if (tid < kDRows) {
+    float mstar = -CUDART_INF_F, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kDChunks; ++ww) {
+      mstar = fmaxf(mstar, mm[ww * kDRows + tid]);
+      l += ml[ww * kDRows + tid] * mf[ww * kDRows + tid];
     }
+    mrow[tid] = make_float2(mstar, l);
+  }
+  if (warp < kDChunks) {
+    const float f0 = mf[warp * kDRows + 2 * t], f1 = mf[warp * kDRows + 2 * t + 1];
+    float* dst = mo + (warp * kDRows + 2 * t) * MS;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const int r = warp * kDRows + 2 * t;
       const int c0 = 16 * mt + g;
-      mo[r * kH + c0] = O[mt][0].x;
-      mo[(r + 1) * kH + c0] = O[mt][0].y;
-      mo[r * kH + c0 + 8] = O[mt][1].x;
-      mo[(r + 1) * kH + c0 + 8] = O[mt][1].y;
+      dst[c0] = O[mt][0].x * f0;
+      dst[MS + c0] = O[mt][0].y * f1;
+      dst[c0 + 8] = O[mt][1].x * f0;
+      dst[MS + c0 + 8] = O[mt][1].y * f1;
     }
   }
   __syncthreads();
@@ -498,27 +537,17 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
     const int row = row0 + r;
     const int rg4 = row >> 2;
     if (rg4 >= a.n_rg) continue;
-    float mstar = -CUDART_INF_F;
+    float o = 0.0f;
 #pragma unroll
-    for (int ww = 0; ww < kDChunks; ++ww) mstar = fmaxf(mstar, mm[ww * kDRows + r]);
-    float o = 0.0f, l = 0.0f;
-    if (mstar != -CUDART_INF_F) {
-#pragma unroll
-      for (int ww = 0; ww < kDChunks; ++ww) {
-        const float mw = mm[ww * kDRows + r];
-        if (mw == -CUDART_INF_F) continue;
-        const float f = exp2f(mw - mstar);
-        o += mo[(ww * kDRows + r) * kH + d] * f;
-        l += ml[ww * kDRows + r] * f;
-      }
-    }
+    for (int ww = 0; ww < kDChunks; ++ww) o += mo[(ww * kDRows + r) * MS + d];
+    const float2 st = mrow[r];
     // the 2^10 scale of the probabilities cancels in o / l; remove it from both
     const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
     float* ws = a.ws + cta * kWsPerCta;
     ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
     if (d == 0) {
-      ws[kRows * kH + (row & 3)] = mstar;
-      ws[kRows * kH + kRows + (row & 3)] = l * (1.0f / 1024.0f);
+      ws[kRows * kH + (row & 3)] = st.x;
+      ws[kRows * kH + kRows + (row & 3)] = st.y * (1.0f / 1024.0f);
     }
   }
 }

@@ -82,12 +82,18 @@ struct TLayout {
   static constexpr int kBar = kFlag + 16;
   static constexpr int kTotal = kBar + 2 * G::kStages * 8;
   static constexpr int kAlloc = kTotal + 1024;
-  // end-of-kernel merge area (reuses the ring): m[8][R], l[8][R], o[8][16][128]
-  // (the output rows are merged 16 at a time)
-  static constexpr int kMergeM = 0;
+  // end-of-kernel merge area (reuses the ring and the tables, idle by then):
+  // o[8][R][kMergeStride] (each chunk's output rows, already scaled by the
+  // chunk's factor 2^(m_w - m*); the padded row stride keeps a warp's stores
+  // on 32 banks), then m[8][R], l[8][R], the factors f[8][R] and the rows'
+  // (m*, l*) pairs
+  static constexpr int kMergeStride = kH + 4;
+  static constexpr int kMergeO = 0;
+  static constexpr int kMergeM = kMergeO + kConsumers * R * kMergeStride * 4;
   static constexpr int kMergeL = kMergeM + kConsumers * R * 4;
-  static constexpr int kMergeO = kMergeL + kConsumers * R * 4;
-  static_assert(kMergeO + kConsumers * 16 * kH * 4 <= G::kStages * G::kUnit, "merge area");
+  static constexpr int kMergeF = kMergeL + kConsumers * R * 4;
+  static constexpr int kMergeS = kMergeF + kConsumers * R * 4;
+  static_assert(kMergeS + R * 8 <= kWarps, "merge area");
 };
 static_assert(TLayout<false, 16>::kAlloc <= 232448, "shared memory (anchor, tensor core)");
 static_assert(TLayout<true, 16>::kAlloc <= 232448, "shared memory (full, tensor core)");
@@ -281,34 +287,49 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
                           &tm_vr, s_flag);
   } else {
     // the Q fragments, by the 8 consumer warps only; they meet at named
-    // barrier 1 (the producer warp never takes part in it)
-    // Q fragments in fp16, scaled by 2^-eq so that the largest |q| of the CTA's rows
-    // lies in [2^14, 2^15) (the other values keep their 8 significant bits unless
-    // they are 2^-28 times smaller than it)
+    // barrier 1 (the producer warp never takes part in it).  The CTA's R query
+    // rows arrive as 16-byte loads (vector (r, v): channels 8v .. 8v + 7 of row
+    // r; zeros for padding rows); the largest |q| sets the fp16 scaling: 2^-eq
+    // puts it in [2^14, 2^15) (the other values keep their 8 significant bits
+    // unless they are 2^-28 times smaller than it)
+    constexpr int kQPer = R * 16 / kConsumerThreads;   // vectors per consumer thread
+    uint4 qv[kQPer];
     {
       uint32_t qm = 0u;
-      for (int i = tid; i < R * kH; i += kConsumerThreads) {
-        const int row = row0 + (i >> 7);
-        if (row < TG)
-          qm = max(qm, (uint32_t)a.q[(((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH + (i & 127)] &
-                           0x7FFFu);
+#pragma unroll
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = tid + k * kConsumerThreads;
+        const int row = row0 + (i >> 4);
+        qv[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < TG) {
+          const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+          qv[k] = __ldg(reinterpret_cast<const uint4*>(qr) + (i & 15));
+        }
+        const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qm = max(qm, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
       }
-      atomicMax(s_qmax, qm);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qm = max(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+      if (L == 0) atomicMax(s_qmax, qm);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
     const int eq = min(max((int)((*s_qmax >> 7) & 0xFFu) - 127 - 14, -100), 113);
     const float qscale = __uint_as_float((uint32_t)(127 - eq) << 23);   // 2^-eq
-    // entry (mi, ks, lane, e): row 16 mi + g' + 8 (e & 1), channels 16 ks + 2t' + 8 (e >> 1) + {0, 1}
-    for (int i = tid; i < MT * 8 * 32 * 4; i += kConsumerThreads) {
-      const int e = i & 3, ln = (i >> 2) & 31, ks = (i >> 7) & 7, mi = i >> 10;
-      const int row = row0 + 16 * mi + (ln >> 2) + 8 * (e & 1);
-      const int d = 16 * ks + 2 * (ln & 3) + 8 * (e >> 1);
-      uint32_t v = 0u;
-      if (row < TG) {
-        const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
-        v = h2(__uint_as_float((uint32_t)qr[d] << 16) * qscale, __uint_as_float((uint32_t)qr[d + 1] << 16) * qscale);
-      }
-      reinterpret_cast<uint32_t*>(smem + S::kQ)[i] = v;
+    // fragment entry (mi, ks, lane, e) holds row 16 mi + g' + 8 (e & 1), channels
+    // 16 ks + 2t' + 8 (e >> 1) + {0, 1} (lane = 4 g' + t'): word j of vector
+    // (r, v) goes to mi = r >> 4, g' = r & 7, e = 2 (v & 1) + ((r >> 3) & 1),
+    // ks = v >> 1, t' = j
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * kConsumerThreads;
+      const int r = i >> 4, v = i & 15;
+      const int e = 2 * (v & 1) + ((r >> 3) & 1);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(smem + S::kQ) + (((r >> 4) * 8 + (v >> 1)) * 32 + 4 * (r & 7)) * 4 + e;
+      const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[4 * j] = h2(__uint_as_float(w4[j] << 16) * qscale, __uint_as_float(w4[j] & 0xFFFF0000u) * qscale);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 
@@ -589,15 +610,18 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     }
   }
 
-  // ================= merge the 8 chunk states (the ring is idle now), 16 rows at a time
+  // ================= merge the 8 chunk states (the ring and the tables are idle now)
   if (kTmem) tmem_fence_before_sync();
   __syncthreads();
   if (kTmem) tmem_fence_after_sync();
   allow_dependent_launch();   // the split combine may be scheduled once every CTA is here
   const bool ok = *reinterpret_cast<volatile int*>(s_flag) == 0;
+  float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
   float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
   float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
-  float* mo = reinterpret_cast<float*>(smem + S::kMergeO);
+  float* mf = reinterpret_cast<float*>(smem + S::kMergeF);
+  float2* mrow = reinterpret_cast<float2*>(smem + S::kMergeS);
+  constexpr int MS = S::kMergeStride;
   if (ok && warp < kConsumers) {
 #pragma unroll
     for (int rh = 0; rh < NR; ++rh) {
@@ -610,73 +634,82 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       }
     }
   }
+  __syncthreads();
+  // chunk w's factor of row r, 2^(m_w - m*) (0 where the chunk saw no key of the row)
+  if (ok && tid < kConsumers * R) {
+    const int r = tid % R;
+    float mstar = -CUDART_INF_F;
 #pragma unroll
-  for (int hf = 0; hf < MT; ++hf) {
+    for (int ww = 0; ww < kConsumers; ++ww) mstar = fmaxf(mstar, mm[ww * R + r]);
+    const float mw = mm[tid];
+    mf[tid] = (mw == -CUDART_INF_F) ? 0.0f : exp2f(mw - mstar);
+  }
+  __syncthreads();
+  // each row's (m*, l*); each lane's O values, scaled by its chunk's factors,
+  // into the chunk's rows of the merge area
+  if (ok && tid < R) {
+    float mstar = -CUDART_INF_F, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kConsumers; ++ww) {
+      mstar = fmaxf(mstar, mm[ww * R + tid]);
+      l += ml[ww * R + tid] * mf[ww * R + tid];
+    }
+    mrow[tid] = make_float2(mstar, l);
+  }
+  if (ok && warp < kConsumers) {
+    float2 fr[NR];   // factors of the lane's rows 8 nt + 2t and 8 nt + 2t + 1
+#pragma unroll
+    for (int nt = 0; nt < NR; ++nt) fr[nt] = make_float2(mf[warp * R + 8 * nt + 2 * t], mf[warp * R + 8 * nt + 2 * t + 1]);
+    float* dst = mo + warp * R * MS;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      float2 q[NR][2];   // [nt][c]: channel 16 mt + g + 8c, rows 8 nt + 2t, + 1
+      if (kTmem) {
+        uint32_t ov[16];
+        tmem_ld16(t_warp + 16u * mt, ov);
+        tmem_wait_ld(ov);
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt) {
+          q[nt][0] = make_float2(__uint_as_float(ov[4 * nt]), __uint_as_float(ov[4 * nt + 1]));
+          q[nt][1] = make_float2(__uint_as_float(ov[4 * nt + 2]), __uint_as_float(ov[4 * nt + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt) {
+          q[nt][0] = O[kTmem ? 0 : mt][nt & 1][0];
+          q[nt][1] = O[kTmem ? 0 : mt][nt & 1][1];
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NR; ++nt) {
+        const int r = 8 * nt + 2 * t;
+        const int c0 = 16 * mt + g;
+        dst[r * MS + c0] = q[nt][0].x * fr[nt].x;
+        dst[(r + 1) * MS + c0] = q[nt][0].y * fr[nt].y;
+        dst[r * MS + c0 + 8] = q[nt][1].x * fr[nt].x;
+        dst[(r + 1) * MS + c0 + 8] = q[nt][1].y * fr[nt].y;
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < R * kH; i += kThreadsQ) {
     if (!ok) break;
-    // the 16 rows 16 hf .. 16 hf + 15: n-tiles 2 hf and 2 hf + 1
-    if (warp < kConsumers) {
+    const int r = i >> 7, d = i & 127;
+    const int row = row0 + r;
+    const int rg4 = row >> 2;
+    if (rg4 >= a.n_rg) continue;
+    float o = 0.0f;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        float2 q[2][2];
-        if (kTmem) {
-          uint32_t ov[16];
-          tmem_ld16(t_warp + 16u * mt, ov);
-          tmem_wait_ld(ov);
-#pragma unroll
-          for (int n2 = 0; n2 < 2; ++n2) {
-            const int nt = 2 * hf + n2;
-            q[n2][0] = make_float2(__uint_as_float(ov[4 * nt]), __uint_as_float(ov[4 * nt + 1]));
-            q[n2][1] = make_float2(__uint_as_float(ov[4 * nt + 2]), __uint_as_float(ov[4 * nt + 3]));
-          }
-        } else {
-#pragma unroll
-          for (int n2 = 0; n2 < 2; ++n2) {
-            q[n2][0] = O[kTmem ? 0 : mt][n2][0];
-            q[n2][1] = O[kTmem ? 0 : mt][n2][1];
-          }
-        }
-#pragma unroll
-        for (int n2 = 0; n2 < 2; ++n2) {
-          const int r = warp * 16 + 8 * n2 + 2 * t;
-          const int c0 = 16 * mt + g;
-          mo[r * kH + c0] = q[n2][0].x;
-          mo[(r + 1) * kH + c0] = q[n2][0].y;
-          mo[r * kH + c0 + 8] = q[n2][1].x;
-          mo[(r + 1) * kH + c0 + 8] = q[n2][1].y;
-        }
-      }
+    for (int ww = 0; ww < kConsumers; ++ww) o += mo[(ww * R + r) * MS + d];
+    const float2 st = mrow[r];
+    // the 2^10 scale of the probabilities cancels in o / l; remove it from both
+    const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
+    float* ws = a.ws + cta * kWsPerCta;
+    ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
+    if (d == 0) {
+      ws[kRows * kH + (row & 3)] = st.x;
+      ws[kRows * kH + kRows + (row & 3)] = st.y * (1.0f / 1024.0f);
     }
-    __syncthreads();
-    for (int i = tid; i < 16 * kH; i += kThreadsQ) {
-      const int rr = i >> 7, d = i & 127;
-      const int r = 16 * hf + rr;
-      const int row = row0 + r;
-      const int rg4 = row >> 2;
-      if (rg4 >= a.n_rg) continue;
-      float mstar = -CUDART_INF_F;
-#pragma unroll
-      for (int ww = 0; ww < kConsumers; ++ww) mstar = fmaxf(mstar, mm[ww * R + r]);
-      float o = 0.0f, l = 0.0f;
-      if (mstar != -CUDART_INF_F) {
-#pragma unroll
-        for (int ww = 0; ww < kConsumers; ++ww) {
-          const float mw = mm[ww * R + r];
-          if (mw == -CUDART_INF_F) continue;
-          const float f = exp2f(mw - mstar);
-          o += mo[(ww * 16 + rr) * kH + d] * f;
-          l += ml[ww * R + r] * f;
-        }
-      }
-      // the 2^10 scale of the probabilities cancels in o / l; remove it from both
-      const int64_t cta = (((int64_t)b * a.Hkv + h) * a.n_rg + rg4) * a.n_splits + split;
-      float* ws = a.ws + cta * kWsPerCta;
-      ws[(row & 3) * kH + d] = o * (1.0f / 1024.0f);
-      if (d == 0) {
-        ws[kRows * kH + (row & 3)] = mstar;
-        ws[kRows * kH + kRows + (row & 3)] = l * (1.0f / 1024.0f);
-      }
-    }
-    __syncthreads();
   }
   // every TMEM access of every warp has completed (each waited for its own
   // loads and stores) before the columns are freed
