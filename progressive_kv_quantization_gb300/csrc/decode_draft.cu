@@ -181,11 +181,10 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
     const int n = a.causal ? ctx - a.T + row / a.G + 1 : ctx;
     return n < 0 ? 0 : n;
   };
-  int max_vis = 0, min_vis = max_keys;
-  for (int r = 0; r < kDRows && row0 + r < TG; ++r) {
-    max_vis = max(max_vis, n_visible(r));
-    min_vis = min(min_vis, n_visible(r));
-  }
+  // n_visible does not decrease with the row: the extremes are the CTA's
+  // first and last real rows (the grid's row tiles start below TG)
+  const int max_vis = n_visible(min(kDRows, TG - row0) - 1);
+  const int min_vis = n_visible(0);
   const int n_pages = (max_vis + kP - 1) / kP;
   const int p_begin = split * a.pages_per_split;
   const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
@@ -292,11 +291,14 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
       // alpha = sum_c q_c A'_c.  k-slots 2t, 2t+1 / 2t+8, 2t+9 are channels
       // 16 ks + 2t, + 1 / + 8, + 9; row g of m-tile mi is token 4g + 2mi, row
       // g + 8 token 4g + 2mi + 1.
-      float sacc[2][4];   // [m-tile][(token even, row 2t), (even, 2t+1), (odd, 2t), (odd, 2t+1)]
+      // [m-tile][(token even, row 2t), (even, 2t+1), (odd, 2t), (odd, 2t+1)]; the
+      // three products of a k-step go to three accumulators (shorter MMA
+      // dependency chains), summed after the last k-step
+      float sacc[2][4], sacc2[2][4], sacc3[2][4];
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mi][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) sacc[mi][e] = sacc2[mi][e] = sacc3[mi][e] = 0.0f;
       float2 alpha2 = make_float2(0.0f, 0.0f);
       // the plane words of all 8 k-steps first: channels 16 ks + 2t + {0, 1, 8, 9}
       uint32_t kw[8][4];
@@ -339,10 +341,14 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
           const uint32_t l0 = prmt(e[0], e[1], kDSelKEvenLo), l1 = prmt(e[0], e[1], kDSelKOddLo);
           const uint32_t l2 = prmt(e[2], e[3], kDSelKEvenLo), l3 = prmt(e[2], e[3], kDSelKOddLo);
           mma_f16(sacc[mi], h0, h1, h2_, h3, bh0, bh1);
-          mma_f16(sacc[mi], h0, h1, h2_, h3, bl0, bl1);
-          mma_f16(sacc[mi], l0, l1, l2, l3, bs0, bs1);
+          mma_f16(sacc2[mi], h0, h1, h2_, h3, bl0, bl1);
+          mma_f16(sacc3[mi], l0, l1, l2, l3, bs0, bs1);
         }
       }
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mi][e] += sacc2[mi][e] + sacc3[mi][e];
       __syncwarp();
       if (L == 0) mbar_arrive(bar_empty + 8 * sK);
       // alpha of query row g: the four lanes of equal g hold its channels; the

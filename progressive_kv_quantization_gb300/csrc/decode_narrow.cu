@@ -172,11 +172,10 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
     const int n = a.causal ? ctx - a.T + row / a.G + 1 : ctx;
     return n < 0 ? 0 : n;
   };
-  int max_vis = 0, min_vis = max_keys;
-  for (int r = 0; r < kNr && row0 + r < TG; ++r) {
-    max_vis = max(max_vis, n_visible(r));
-    min_vis = min(min_vis, n_visible(r));
-  }
+  // n_visible does not decrease with the row: the extremes are the CTA's
+  // first and last real rows (the grid's row tiles start below TG)
+  const int max_vis = n_visible(min(kNr, TG - row0) - 1);
+  const int min_vis = n_visible(0);
   const int nv[2] = {n_visible(2 * t), n_visible(2 * t + 1)};   // the lane's query rows
   const int n_pages = (max_vis + kP - 1) / kP;
   const int p_begin = split * a.pages_per_split;

@@ -242,6 +242,20 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   }
   // every global-memory access of this kernel follows this wait
   wait_prerequisite_grids();
+  // the consumer threads' query vectors, issued before the context length is
+  // read: vector i = (row i >> 4, channels 8 (i & 15) .. + 7), zeros for padding rows
+  constexpr int kQPer = R * 16 / kConsumerThreads;   // vectors per consumer thread
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kConsumerThreads;
+    const int row = row0 + (i >> 4);
+    qv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (warp < kConsumers && row < TG) {
+      const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+      qv[k] = __ldg(reinterpret_cast<const uint4*>(qr) + (i & 15));
+    }
+  }
 
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
@@ -255,11 +269,10 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
     const int n = a.causal ? ctx - a.T + row / a.G + 1 : ctx;
     return n < 0 ? 0 : n;
   };
-  int max_vis = 0, min_vis = max_keys;
-  for (int r = 0; r < R && row0 + r < TG; ++r) {
-    max_vis = max(max_vis, n_visible(r));
-    min_vis = min(min_vis, n_visible(r));
-  }
+  // n_visible does not decrease with the row: the extremes are the CTA's
+  // first and last real rows (the grid's row tiles start below TG)
+  const int max_vis = n_visible(min(R, TG - row0) - 1);
+  const int min_vis = n_visible(0);
   int nv[NR];   // visible keys of the lane's rows 8 rh + g
 #pragma unroll
   for (int rh = 0; rh < NR; ++rh) nv[rh] = n_visible(8 * rh + g);
@@ -288,23 +301,13 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   } else {
     // the Q fragments, by the 8 consumer warps only; they meet at named
     // barrier 1 (the producer warp never takes part in it).  The CTA's R query
-    // rows arrive as 16-byte loads (vector (r, v): channels 8v .. 8v + 7 of row
-    // r; zeros for padding rows); the largest |q| sets the fp16 scaling: 2^-eq
+    // rows are the vectors qv loaded above; the largest |q| sets the fp16 scaling: 2^-eq
     // puts it in [2^14, 2^15) (the other values keep their 8 significant bits
     // unless they are 2^-28 times smaller than it)
-    constexpr int kQPer = R * 16 / kConsumerThreads;   // vectors per consumer thread
-    uint4 qv[kQPer];
     {
       uint32_t qm = 0u;
 #pragma unroll
       for (int k = 0; k < kQPer; ++k) {
-        const int i = tid + k * kConsumerThreads;
-        const int row = row0 + (i >> 4);
-        qv[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (row < TG) {
-          const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
-          qv[k] = __ldg(reinterpret_cast<const uint4*>(qr) + (i & 15));
-        }
         const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) qm = max(qm, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
