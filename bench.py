@@ -429,8 +429,8 @@ KERNEL_SOURCES = {
     "encode": ["encode.cu", "lynx_internal.cuh"],
     "reconstruct_anchor": ["reconstruct.cu", "lynx_internal.cuh"],
     "reconstruct_full": ["reconstruct.cu", "lynx_internal.cuh"],
-    "decode_anchor_b1": ["decode_narrow.cu", "decode_common.cuh", "lynx_internal.cuh"],
-    "decode_anchor_b8": ["decode_narrow.cu", "decode_common.cuh", "lynx_internal.cuh"],
+    "decode_anchor_b1": ["decode_draft.cu", "decode_common.cuh", "lynx_internal.cuh"],
+    "decode_anchor_b8": ["decode_draft.cu", "decode_common.cuh", "lynx_internal.cuh"],
     "verify_full_t8": ["decode_tc.cu", "decode_common.cuh", "lynx_internal.cuh"],
     "decode_bf16_b1": ["decode_attn.cu", "lynx_internal.cuh"],
 }
