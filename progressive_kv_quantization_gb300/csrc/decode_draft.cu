@@ -158,7 +158,11 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   // Thread e makes entry e and stores its 32 copies, the copy index rotated by
   // the lane so that a warp's stores hit different banks.
   if (tid < 256) {
-    const float2 v = lut.anc_pair[tid];
+    // entry e = (value of nibble e & 15, value of nibble e >> 4): lane L reads
+    // nibble L & 15's value once (16 parameter addresses per warp instead of 32)
+    // and the two values come by shuffles
+    const float n16 = lut.anc16[L & 15];
+    const float2 v = make_float2(__shfl_sync(0xffffffffu, n16, tid & 15), __shfl_sync(0xffffffffu, n16, (tid >> 4) & 15));
     const int v0 = min(max(__float2int_rn(v.x * kDFix), -16383), 16383);
     const int v1 = min(max(__float2int_rn(v.y * kDFix), -16383), 16383);
     const uint32_t ent = (uint32_t)(v0 + 16384) | ((uint32_t)(v1 + 16384) << 16);
@@ -168,6 +172,16 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   }
   // every global-memory access of this kernel follows this wait
   wait_prerequisite_grids();
+  // the query vector of thread i < 128 (row i >> 4, channels 8 (i & 15) .. + 7;
+  // zeros for padding rows), requested before the context length is read
+  uint4 qx = make_uint4(0u, 0u, 0u, 0u);
+  if (tid < kDRows * 16) {
+    const int row = row0 + (tid >> 4);
+    if (row < TG) {
+      const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
+      qx = __ldg(reinterpret_cast<const uint4*>(qr) + (tid & 15));
+    }
+  }
 
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
@@ -207,19 +221,13 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
     const int w = warp;
     // the query rows as BF16 pairs (the consumer warps meet at named barrier 1):
     // word (pair p, row r) = channels 2p, 2p + 1 of query row r of this CTA (0
-    // for padding rows), from 16-byte loads (thread i < 128: row i >> 4,
-    // channels 8 (i & 15) .. + 7); the CTA's largest |q| sets the fp16 scaling of Q'
+    // for padding rows), from the vectors qx loaded above; the CTA's largest |q|
+    // sets the fp16 scaling of Q'
     {
       uint32_t qm = 0u;
       if (tid < kDRows * 16) {
         const int r = tid >> 4, v = tid & 15;
-        const int row = row0 + r;
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (row < TG) {
-          const uint16_t* qr = a.q + (((int64_t)b * a.T + row / a.G) * a.Hq + h * a.G + row % a.G) * kH;
-          x = __ldg(reinterpret_cast<const uint4*>(qr) + v);
-        }
-        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t w4[4] = {qx.x, qx.y, qx.z, qx.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           s_q[(4 * v + j) * kDRows + r] = w4[j];
