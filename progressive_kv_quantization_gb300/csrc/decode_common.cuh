@@ -107,8 +107,12 @@ __device__ __forceinline__ void full_codes(uint32_t wa, uint32_t wr, uint32_t& e
 // (bounded) until every copy it issued has landed: a unit older than the last
 // kStages was consumed before its slot was reused, so only those last units
 // can still be in flight, whether the consumers finished or gave up early.
+// first_id is the page id pt_row[p_begin], read by the caller ahead of time
+// (e.g. together with the context length) so that the first copy waits on one
+// global load less; the table entry of every later page is read once, for its
+// K unit.
 template <bool FULL, int STAGES = 3>
-__device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np,
+__device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np, int first_id,
                               uint32_t s_ring, uint32_t bar_full, uint32_t bar_empty,
                               const CUtensorMap* tm_ka, const CUtensorMap* tm_va,
                               const CUtensorMap* tm_kr, const CUtensorMap* tm_vr, int* s_flag) {
@@ -117,6 +121,7 @@ __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_
   const int skip = a.inject_skip - 1;   // -1: no unit is skipped
   int u_end = 0;                        // units attempted
   bool ok = true;
+  int64_t id = first_id;
   for (int u = 0; u < 2 * np; ++u) {
     const int st = u % kSt;
     if (u >= kSt && !mbar_wait(bar_empty + 8 * st, ((u / kSt) - 1) & 1, a.wait_ns)) {
@@ -124,10 +129,10 @@ __device__ void produce_units(const DecodeArgs& a, const int32_t* pt_row, int p_
       break;
     }
     u_end = u + 1;
-    if (u == skip) continue;   // test hook: this unit's copy is never issued
     const int p = p_begin + (u >> 1);
     const bool is_v = (u & 1) != 0;
-    int64_t id = pt_row[p];
+    if (u >= 2 && !is_v) id = pt_row[p];
+    if (u == skip) continue;   // test hook: this unit's copy is never issued
     if (id < 0 || id >= a.n_pool) {
       atomicExch(a.status, 2);
       id = 0;

@@ -172,6 +172,12 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
   }
   // every global-memory access of this kernel follows this wait
   wait_prerequisite_grids();
+  // the producer lane reads its first page id together with the context length
+  int first_id = 0;
+  if (tid == kDChunks * 32) {
+    const int pb = split * a.pages_per_split;
+    if (pb < a.max_pages) first_id = a.page_table[((int64_t)b * a.Hkv + h) * a.max_pages + pb];
+  }
   // the query vector of thread i < 128 (row i >> 4, channels 8 (i & 15) .. + 7;
   // zeros for padding rows), requested before the context length is read
   uint4 qx = make_uint4(0u, 0u, 0u, 0u);
@@ -215,7 +221,7 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
 
   if (warp == kDChunks) {
     if (L == 0)
-      produce_units<false, kDStages>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_ka,
+      produce_units<false, kDStages>(a, pt_row, p_begin, np, first_id, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_ka,
                                      &tm_va, s_flag);
   } else {
     const int w = warp;

@@ -159,6 +159,12 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
   }
   // every global-memory access of this kernel follows this wait
   wait_prerequisite_grids();
+  // the producer lane reads its first page id together with the context length
+  int first_id = 0;
+  if (tid == kConsumers * 32) {
+    const int pb = split * a.pages_per_split;
+    if (pb < a.max_pages) first_id = a.page_table[((int64_t)b * a.Hkv + h) * a.max_pages + pb];
+  }
 
   int ctx = a.ctx_len[b];
   if (ctx < 0 || ctx > max_keys) {
@@ -191,7 +197,7 @@ decode_narrow_kernel(const DecodeArgs a, const LutTables lut,
 
   if (warp == kConsumers) {
     if (L == 0)
-      produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
+      produce_units<FULL>(a, pt_row, p_begin, np, first_id, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
     // the Q^T fragments; the consumer warps meet at named barrier 1 (the

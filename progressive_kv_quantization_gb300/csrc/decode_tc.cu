@@ -242,6 +242,12 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   }
   // every global-memory access of this kernel follows this wait
   wait_prerequisite_grids();
+  // the producer lane reads its first page id together with the context length
+  int first_id = 0;
+  if (tid == kConsumers * 32) {
+    const int pb = split * a.pages_per_split;
+    if (pb < a.max_pages) first_id = a.page_table[((int64_t)b * a.Hkv + h) * a.max_pages + pb];
+  }
   // the consumer threads' query vectors, issued before the context length is
   // read: vector i = (row i >> 4, channels 8 (i & 15) .. + 7), zeros for padding rows
   constexpr int kQPer = R * 16 / kConsumerThreads;   // vectors per consumer thread
@@ -296,7 +302,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
 
   if (warp == kConsumers) {
     if (L == 0)
-      produce_units<FULL>(a, pt_row, p_begin, np, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
+      produce_units<FULL>(a, pt_row, p_begin, np, first_id, s_ring, bar_full, bar_empty, &tm_ka, &tm_va, &tm_kr,
                           &tm_vr, s_flag);
   } else {
     // the Q fragments, by the 8 consumer warps only; they meet at named
