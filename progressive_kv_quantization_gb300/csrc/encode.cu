@@ -17,8 +17,10 @@
 // then q = RN(x r) corrected by one FMA residual step, q' = RN(q + r (x - q d))
 // (Markstein's FMA division correction), which returns the correctly rounded
 // quotient.  The Stage 2 quotient |x_c| / (sigma + eps) feeds only the code
-// decision: its estimate uses q = RN(x r) (within 1.5 ulp), and the corrected
-// quotient is formed where the code is decided from the threshold table.  sigma = max_t |x_n,t - mu| is taken as
+// decision: the estimate takes alpha |x_f| as |x_c| RN(alpha r), inside the fused
+// multiply-add that forms 1 + alpha |x_f| (relative error below 2^-23; one
+// product per chunk), and the correctly rounded quotient is formed where the
+// code is decided from the threshold table.  sigma = max_t |x_n,t - mu| is taken as
 // max(RN(x_n(max x) - mu), RN(mu - x_n(min x))): every step from x to
 // x_n - mu is a monotone rounding, so the extreme deviations sit at the
 // chunk's extreme inputs and the value is the same.  The Stage 3 code
@@ -227,7 +229,10 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
   if (PARTIAL && nc == 0) sigma = 0.0f;
   const float ds = __fadd_rn(sigma, eps);
   const float rs = __frcp_rn(ds);
-  const float2 nmu2 = f2(-mu), rs2 = f2(rs);
+  const float2 nmu2 = f2(-mu);
+  // Stage 3's magnitude enters the estimate as |x_c| (alpha / (sigma + eps)): one
+  // product per chunk instead of one per element
+  const QuantConsts qcs{f2(__fmul_rn(qc.alpha2.x, rs)), qc.c2, qc.edge};
 
   // ---- Stages 3-4, eight tokens at a time: codes in the low byte of the
   // rounded floats, sign masks, then split and pack
@@ -250,10 +255,10 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
       }
       xs[2 * u] = xc.x;
       xs[2 * u + 1] = xc.y;
-      a[u] = __fmul2_rn(make_float2(fabsf(xc.x), fabsf(xc.y)), rs2);   // |x_f| within 1.5 ulp
+      a[u] = make_float2(fabsf(xc.x), fabsf(xc.y));
     }
     // the exact |x_f| = RN(|x_c| / (sigma + eps)) only where the code is decided from the table
-    quantise8<OUT == kOutInt4 ? 7 : 127>(a, ib, s_thr, qc, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
+    quantise8<OUT == kOutInt4 ? 7 : 127>(a, ib, s_thr, qcs, [&](int e) { return div1(fabsf(xs[e]), ds, rs); });
     if constexpr (OUT >= kOutSplitBits) {
       constexpr int A = OUT - kOutSplitBits, R = 8 - A;
 #pragma unroll
