@@ -49,6 +49,16 @@ constexpr uint32_t kMagicBits = 0x4B400000u;
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
+// (x_lo + c, x_hi + c) for the two BF16 values of w, each one float32
+// addition of the exactly converted BF16 value (mixed-precision add)
+__device__ __forceinline__ float2 sub_min_bf16x2(uint32_t w, float c) {
+  float2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %3;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(c));
+  return r;
+}
+
 // correctly rounded x / d for a pair, given r = RN(1/d) and nd = -d
 __device__ __forceinline__ float2 div2(float2 x, float2 nd, float2 r) {
   const float2 q = __fmul2_rn(x, r);
@@ -204,12 +214,15 @@ __device__ __forceinline__ void encode_chunk(const uint32_t (&w)[16], int nc, fl
   float2 xn[16];
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
-    float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
-    if (PARTIAL) {   // padding enters no operation: it becomes gamma_min, so x_n = 0 exactly
+    if (PARTIAL) {
+      float2 v = make_float2(__uint_as_float(w[t] << 16), __uint_as_float(w[t] & 0xFFFF0000u));
+      // padding enters no operation: it becomes gamma_min, so x_n = 0 exactly
       v.x = 2 * t < nc ? v.x : mn;
       v.y = 2 * t + 1 < nc ? v.y : mn;
+      xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
+    } else {
+      xn[t] = div2(sub_min_bf16x2(w[t], -mn), ndg2, rg2);
     }
-    xn[t] = div2(__fadd2_rn(v, nmn2), ndg2, rg2);
   }
 
   // ---- Stage 2: mu (left-to-right sum), sigma, x_f
