@@ -371,7 +371,9 @@ int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float
     return fail(LYNX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
   if (n_pages > ((int64_t)1 << 40)) return fail(LYNX_ERR_INVALID_ARG, "n_pages too large");
   const LutTables* lut = lut_tables(params->alpha, params->eps);
-  cudaError_t e = launch_reconstruct(anchor, residual, meta, n_pages, out, out_dtype, lut,
+  int* status = device_status_ptr();
+  if (!status) return fail(LYNX_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = launch_reconstruct(anchor, residual, meta, n_pages, out, out_dtype, lut, status,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct launch");
   return LYNX_OK;

@@ -15,6 +15,7 @@
 //   x = fmaf(fmaf(S*l(I_hat), sigma+eps, mu), gamma_scale+eps, gamma_min).
 
 #include "lynx_internal.cuh"
+#include "tma_ptx.cuh"
 
 #include <cuda_bf16.h>
 
@@ -149,6 +150,157 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
     }
     if (on < n_groups) store_meta(buf ^ 1, m0, m1);
     __syncthreads();
+  }
+}
+
+// The same reconstruction with whole pages staged by bulk copies: one producer
+// lane streams each page's Anchor plane (and Residual plane) and its metadata
+// record into a kRStages-slot shared-memory ring (full / empty mbarriers, every
+// wait bounded); 16 consumer warps turn each staged page into BF16 (or float32)
+// rows.  Consumer warp w takes the rows r = w + 16k (k = 0..7) of the page, and
+// its lane group c = L >> 2 (lanes 4c .. 4c+3, tokens 32c .. 32c+31 = chunk c)
+// works on row (r + c) mod 128: over the 128 values of r every (row, chunk)
+// pair is taken once, and the eight lane groups of a warp read eight different
+// rows' metadata, so the per-chunk mu / sigma reads hit eight different banks
+// (and the plane words, word (row, L), one bank per lane).
+constexpr int kRConsumers = 16;
+constexpr int kRThreads = (kRConsumers + 1) * 32;
+constexpr int kRStages = 4;
+
+template <bool kFull>
+struct RLayout {
+  static constexpr int kUnit = (kFull ? 2 * kPlaneBytes : kPlaneBytes) + kMetaBytes;
+  static constexpr int kMetaOff = kFull ? 2 * kPlaneBytes : kPlaneBytes;
+  static constexpr int kRing = 0;
+  static constexpr int kLut = kRing + kRStages * kUnit;              // float [entries][32 lanes]
+  static constexpr int kBar = kLut + (kFull ? 256 : 16) * 32 * 4;    // full[kRStages], empty[kRStages]
+  static constexpr int kFlag = kBar + 2 * kRStages * 8;
+  static constexpr int kTotal = kFlag + 16;
+};
+static_assert(RLayout<true>::kTotal <= 232448, "shared memory (staged reconstruction)");
+static_assert(RLayout<false>::kUnit % 16 == 0 && RLayout<true>::kUnit % 16 == 0, "bulk-copy alignment");
+
+template <bool kFull, bool kF32>
+__global__ void __launch_bounds__(kRThreads, 1)
+reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
+                          const float* __restrict__ meta, int64_t n_pages, void* __restrict__ out,
+                          const LutTables lut, int* __restrict__ status) {
+  using S = RLayout<kFull>;
+  constexpr int kEntries = kFull ? 256 : 16;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bar_full = base + S::kBar;
+  const uint32_t bar_empty = bar_full + 8 * kRStages;
+  int* s_flag = reinterpret_cast<int*>(smem + S::kFlag);
+  float* s_lut = reinterpret_cast<float*>(smem + S::kLut);
+  if (tid == 0) {
+    for (int st = 0; st < kRStages; ++st) {
+      mbar_init(bar_full + 8 * st, 1);
+      mbar_init(bar_empty + 8 * st, kRConsumers);
+    }
+    *s_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // the value table (kernel parameters only), entry e of lane L at word e * 32 + L
+  for (int i = tid; i < kEntries * 32; i += kRThreads) s_lut[i] = kFull ? lut.full[i >> 5] : lut.anc16[i >> 5];
+  __syncthreads();
+  // launched as a programmatic dependent: every global-memory access follows
+  // the wait for the kernel ahead in the stream
+  wait_prerequisite_grids();
+  allow_dependent_launch();
+
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int n_mine = first < n_pages ? (int)((n_pages - 1 - first) / stride + 1) : 0;
+  if (warp == kRConsumers) {   // ---- producer lane
+    if (lane != 0) return;
+    int u_end = 0;
+    bool ok = true;
+    for (int u = 0; u < n_mine; ++u) {
+      const int st = u % kRStages;
+      if (u >= kRStages && !mbar_wait(bar_empty + 8 * st, ((u / kRStages) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      u_end = u + 1;
+      const int64_t page = first + (int64_t)u * stride;
+      const uint32_t dst = base + S::kRing + st * S::kUnit;
+      const uint32_t bar = bar_full + 8 * st;
+      mbar_expect_tx(bar, S::kUnit);
+      bulk_g2s(dst, anchor + page * kPlaneBytes, kPlaneBytes, bar);
+      if (kFull) bulk_g2s(dst + kPlaneBytes, residual + page * kPlaneBytes, kPlaneBytes, bar);
+      bulk_g2s(dst + S::kMetaOff, meta + page * kMetaFloats, kMetaBytes, bar);
+    }
+    if (!ok) {
+      atomicExch(status, 1);
+      *reinterpret_cast<volatile int*>(s_flag) = 1;
+    }
+    // every copy this lane issued has landed before the CTA may exit
+    for (int u = u_end - 1; u >= 0 && u >= u_end - kRStages; --u)
+      mbar_wait(bar_full + 8 * (u % kRStages), (u / kRStages) & 1);
+    return;
+  }
+
+  // ---- consumer warps
+  const float eps = lut.eps;
+  const float* lut_lane = s_lut + lane;
+  const int c = lane >> 2;   // the lane group's chunk
+  for (int u = 0; u < n_mine; ++u) {
+    const int st = u % kRStages;
+    const bool got = mbar_wait(bar_full + 8 * st, (u / kRStages) & 1);
+    if (__any_sync(0xffffffffu, !got) || *reinterpret_cast<volatile int*>(s_flag) != 0) {
+      if (lane == 0) {
+        atomicExch(status, 1);
+        *reinterpret_cast<volatile int*>(s_flag) = 1;
+      }
+      break;
+    }
+    const int64_t page = first + (int64_t)u * stride;
+    const uint8_t* unit = smem + S::kRing + st * S::kUnit;
+    const uint32_t* pa = reinterpret_cast<const uint32_t*>(unit);
+    const uint32_t* pr = reinterpret_cast<const uint32_t*>(unit + kPlaneBytes);
+    const float* mt = reinterpret_cast<const float*>(unit + S::kMetaOff);
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+      const int row = (warp + 16 * k + c) & 127;
+      const uint32_t wa = pa[row * 32 + lane];
+      const uint32_t wr = kFull ? pr[row * 32 + lane] : 0u;
+      const float gmin = mt[row];
+      const float dgv = __fadd_rn(mt[kH + row], eps);
+      const float muv = mt[kMetaMuOff + c * kH + row];
+      const float dsv = __fadd_rn(mt[kMetaSigmaOff + c * kH + row], eps);
+      const float2 ds2 = make_float2(dsv, dsv), mu2 = make_float2(muv, muv);
+      const float2 dg2 = make_float2(dgv, dgv), gm2 = make_float2(gmin, gmin);
+      float2 xv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t c0 = (wa >> (8 * j)) & 0xFu, c1 = (wa >> (8 * j + 4)) & 0xFu;
+        if (kFull) {
+          c0 |= ((wr >> (8 * j)) & 0xFu) << 4;
+          c1 |= ((wr >> (8 * j + 4)) & 0xFu) << 4;
+        }
+        const float2 l = make_float2(lut_lane[c0 * 32], lut_lane[c1 * 32]);
+        xv[j] = __ffma2_rn(__ffma2_rn(l, ds2, mu2), dg2, gm2);
+      }
+      const int64_t orow = page * kH + row;
+      if (kF32) {
+        float4* op = reinterpret_cast<float4*>(out) + orow * 64 + lane * 2;
+        op[0] = make_float4(xv[0].x, xv[0].y, xv[1].x, xv[1].y);
+        op[1] = make_float4(xv[2].x, xv[2].y, xv[3].x, xv[3].y);
+      } else {
+        uint32_t pk[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(xv[j].x, xv[j].y);
+          pk[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        reinterpret_cast<uint4*>(out)[orow * 32 + lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * st);
   }
 }
 
@@ -349,6 +501,26 @@ cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* 
                              meta, n_groups, out, *lut);
 }
 
+// one CTA per SM (each holds kRStages pages), pages taken round robin
+template <bool kFull, bool kF32>
+cudaError_t launch_staged(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
+                          void* out, const LutTables* lut, int* status, cudaStream_t s) {
+  constexpr int kSmem = RLayout<kFull>::kTotal;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(reconstruct_staged_kernel<kFull, kF32>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int64_t sms = device_sm_count();
+  const int blocks = (int)(n_pages < sms ? n_pages : sms);
+  return launch_programmatic(reconstruct_staged_kernel<kFull, kF32>, dim3(blocks), dim3(kRThreads), kSmem, s,
+                             anchor, residual, meta, n_pages, out, *lut, status);
+}
+
 }  // namespace
 
 cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, cudaStream_t s) {
@@ -361,16 +533,16 @@ cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* 
 }
 
 cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
-                               int64_t n_pages, void* out, int out_dtype, const LutTables* lut,
+                               int64_t n_pages, void* out, int out_dtype, const LutTables* lut, int* status,
                                cudaStream_t s) {
   const bool full = residual != nullptr;
   const bool f32 = out_dtype == LYNX_OUT_F32;
   if (full) {
-    return f32 ? launch<1, true>(anchor, residual, meta, n_pages, out, lut, s)
-               : launch<1, false>(anchor, residual, meta, n_pages, out, lut, s);
+    return f32 ? launch_staged<true, true>(anchor, residual, meta, n_pages, out, lut, status, s)
+               : launch_staged<true, false>(anchor, residual, meta, n_pages, out, lut, status, s);
   }
-  return f32 ? launch<0, true>(anchor, residual, meta, n_pages, out, lut, s)
-             : launch<0, false>(anchor, residual, meta, n_pages, out, lut, s);
+  return f32 ? launch_staged<false, true>(anchor, residual, meta, n_pages, out, lut, status, s)
+             : launch_staged<false, false>(anchor, residual, meta, n_pages, out, lut, status, s);
 }
 
 cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,
