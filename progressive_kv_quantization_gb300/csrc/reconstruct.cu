@@ -155,9 +155,10 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
 
 // The same reconstruction with whole pages staged by bulk copies: one producer
 // lane streams each page's Anchor plane (and Residual plane) and its metadata
-// record into a kRStages-slot shared-memory ring (full / empty mbarriers, every
-// wait bounded); 16 consumer warps turn each staged page into BF16 (or float32)
-// rows.  Consumer warp w takes the rows r = w + 16k (k = 0..7) of the page, and
+// record into a shared-memory ring of 6 slots (Anchor only) or 5 (full codes)
+// with full / empty mbarriers, every wait bounded; 16 consumer warps turn each
+// staged page into BF16 (or float32) rows.  The full-code table keeps 16 copies
+// (lane L reads copy L & 15) so that the fifth slot fits.  Consumer warp w takes the rows r = w + 16k (k = 0..7) of the page, and
 // its lane group c = L >> 2 (lanes 4c .. 4c+3, tokens 32c .. 32c+31 = chunk c)
 // works on row (r + c) mod 128: over the 128 values of r every (row, chunk)
 // pair is taken once, and the eight lane groups of a warp read eight different
@@ -165,15 +166,16 @@ reconstruct_kernel(const uint32_t* __restrict__ anchor, const uint32_t* __restri
 // (and the plane words, word (row, L), one bank per lane).
 constexpr int kRConsumers = 16;
 constexpr int kRThreads = (kRConsumers + 1) * 32;
-constexpr int kRStages = 4;
+template <bool kFull> constexpr int kRStagesOf = kFull ? 5 : 6;   // ring slots
 
 template <bool kFull>
 struct RLayout {
+  static constexpr int kRStages = kRStagesOf<kFull>;
   static constexpr int kUnit = (kFull ? 2 * kPlaneBytes : kPlaneBytes) + kMetaBytes;
   static constexpr int kMetaOff = kFull ? 2 * kPlaneBytes : kPlaneBytes;
   static constexpr int kRing = 0;
   static constexpr int kLut = kRing + kRStages * kUnit;              // float [entries][32 lanes]
-  static constexpr int kBar = kLut + (kFull ? 256 : 16) * 32 * 4;    // full[kRStages], empty[kRStages]
+  static constexpr int kBar = kLut + (kFull ? 256 * 16 : 16 * 32) * 4;    // full[kRStages], empty[kRStages]
   static constexpr int kFlag = kBar + 2 * kRStages * 8;
   static constexpr int kTotal = kFlag + 16;
 };
@@ -186,6 +188,7 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
                           const float* __restrict__ meta, int64_t n_pages, void* __restrict__ out,
                           const LutTables lut, int* __restrict__ status) {
   using S = RLayout<kFull>;
+  constexpr int kRStages = S::kRStages;
   constexpr int kEntries = kFull ? 256 : 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -205,7 +208,8 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // the value table (kernel parameters only), entry e of lane L at word e * 32 + L
-  for (int i = tid; i < kEntries * 32; i += kRThreads) s_lut[i] = kFull ? lut.full[i >> 5] : lut.anc16[i >> 5];
+  constexpr int kCopies = kFull ? 16 : 32;
+  for (int i = tid; i < kEntries * kCopies; i += kRThreads) s_lut[i] = kFull ? lut.full[i >> 4] : lut.anc16[i >> 5];
   __syncthreads();
   // launched as a programmatic dependent: every global-memory access follows
   // the wait for the kernel ahead in the stream
@@ -245,7 +249,7 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
 
   // ---- consumer warps
   const float eps = lut.eps;
-  const float* lut_lane = s_lut + lane;
+  const float* lut_lane = s_lut + (kFull ? (lane & 15) : lane);
   const int c = lane >> 2;   // the lane group's chunk
   for (int u = 0; u < n_mine; ++u) {
     const int st = u % kRStages;
@@ -281,7 +285,7 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
           c0 |= ((wr >> (8 * j)) & 0xFu) << 4;
           c1 |= ((wr >> (8 * j + 4)) & 0xFu) << 4;
         }
-        const float2 l = make_float2(lut_lane[c0 * 32], lut_lane[c1 * 32]);
+        const float2 l = make_float2(lut_lane[c0 * (kFull ? 16 : 32)], lut_lane[c1 * (kFull ? 16 : 32)]);
         xv[j] = __ffma2_rn(__ffma2_rn(l, ds2, mu2), dg2, gm2);
       }
       const int64_t orow = page * kH + row;
