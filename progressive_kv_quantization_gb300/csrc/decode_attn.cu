@@ -642,6 +642,16 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   const float* od = ws + r * kH + d;
   float o = 0.0f;
   int s = 0;
+  for (; s + 32 <= n; s += 32) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = od[(int64_t)(s + k) * kWsPerCta];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float f = s_w[s + k];
+      o = (f != 0.0f) ? fmaf(v[k], f, o) : o;
+    }
+  }
   for (; s + 8 <= n; s += 8) {
     float v[8];
 #pragma unroll
