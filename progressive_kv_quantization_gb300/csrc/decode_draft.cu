@@ -287,7 +287,7 @@ decode_draft_kernel(const DecodeArgs a, const LutTables lut, const __grid_consta
           Bf[k] = __fmul_rn(B, 1.0f / kDFix);
           bmax = fmaxf(bmax, fabsf(Bf[k]));
         }
-        bmax = warp_max(bmax);
+        bmax = warp_max_nonneg(bmax);
         // |q| < 2^eq and |B'| < 2^eb, so |q B' 2^-ek| < 2^15 with ek = eq + eb - 15
         const int eb = (int)((__float_as_uint(bmax) >> 23) & 0xFFu) - 127 + 1;
         ek = min(max(eq + eb - 15, -100), 100);

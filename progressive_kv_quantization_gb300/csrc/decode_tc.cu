@@ -387,7 +387,7 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       }
       int ek = 0;
       if (key) {
-        mx = warp_max(mx);
+        mx = warp_max_nonneg(mx);
         ek = min(max((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 14, -100), 100);
       }
       const float f = __uint_as_float((uint32_t)(127 - ek) << 23);
