@@ -258,7 +258,10 @@ int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* par
  *             (LYNX_OUT_F32).  The float32 value is
  *             fmaf(fmaf(S*l(I_hat), sigma+eps, mu), gamma_scale+eps, gamma_min)
  *             with S*l(I_hat) rounded to float32.
- * Errors as for lynx_encode_pages; INVALID_ARG for an unknown out_dtype. */
+ * Errors as for lynx_encode_pages; INVALID_ARG for an unknown out_dtype.  The
+ * kernel stages pages through shared memory with bounded waits: a wait that
+ * runs out (2 s) sets the device status word that lynx_device_status()
+ * reports, and the affected pages' outputs are unspecified. */
 int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                      int64_t n_pages, const lynx_params_t* params, void* out, int out_dtype,
                      void* stream);
