@@ -216,7 +216,8 @@ int lynx_encode_variant(const void* x_bf16, int64_t n_pages, int variant, const 
  * variants: fmaf(fmaf(v, sigma+eps, mu), gamma_scale+eps, gamma_min) with v the
  * code's signed inverse-compander value rounded to float32 (as
  * lynx_reconstruct); uniform: fmaf(Q, S, min).  Errors as lynx_encode_variant;
- * INVALID_ARG for an unknown out_dtype. */
+ * INVALID_ARG for an unknown out_dtype.  Lynx-INT4 runs lynx_reconstruct's
+ * staged kernel, whose bounded waits set the device status word as there. */
 int lynx_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
                              const lynx_params_t* params, void* out, int out_dtype, void* stream);
 

@@ -614,7 +614,9 @@ int lynx_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_
   const LutTables* lut = nullptr;
   if (variant == LYNX_VARIANT_LYNX_INT8) lut = lut_tables8(params->alpha, params->eps);
   if (variant == LYNX_VARIANT_LYNX_INT4) lut = lut_tables4(params->alpha, params->eps);
-  cudaError_t e = launch_reconstruct_variant(codes, meta, n_pages, variant, out, out_dtype, lut,
+  int* status = device_status_ptr();
+  if (!status) return fail(LYNX_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = launch_reconstruct_variant(codes, meta, n_pages, variant, out, out_dtype, lut, status,
                                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct_variant launch");
   return LYNX_OK;

@@ -117,7 +117,7 @@ cudaError_t launch_encode_variant(const void* x, int64_t n_pages, int variant, u
 // nibbles (token 2j in the low nibble of byte j, 2j + 1 in the high one)
 cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* lo, uint8_t* hi, cudaStream_t s);
 cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
-                                       void* out, int out_dtype, const LutTables* lut, cudaStream_t s);
+                                       void* out, int out_dtype, const LutTables* lut, int* status, cudaStream_t s);
 cudaError_t launch_encode_split(const void* x, int64_t n_pages, int anchor_bits, uint8_t* anchor,
                                 uint8_t* residual, float* meta, const EncodeTables* tab, cudaStream_t s);
 cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,

@@ -1,7 +1,10 @@
 // lynx_reconstruct kernels: the Anchor-phase and Residual-phase dequantisation
-// of the Lynx paper (§4.2; inverse compander of Eq. (4)).
+// of the Lynx paper (§4.2; inverse compander of Eq. (4)).  lynx_reconstruct
+// and the Lynx-INT4 comparator run reconstruct_staged_kernel (whole pages
+// staged by bulk copies, described before it); the Lynx-INT8 comparator's
+// one-byte codes run reconstruct_kernel below.
 //
-// Work mapping.  A CTA of 8 warps takes 16 consecutive channel rows of a page
+// reconstruct_kernel work mapping.  A CTA of 8 warps takes 16 consecutive channel rows of a page
 // (a row group) at a time; warp w owns rows w and w+8, lane L owns tokens 8L .. 8L+7,
 // which are one 32-bit word of each 4-bit plane (coalesced 128-byte warp
 // loads) and 16 bytes of BF16 output (coalesced 512-byte warp stores).  The
@@ -564,15 +567,15 @@ cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* resid
 }
 
 cudaError_t launch_reconstruct_variant(const uint8_t* codes, const float* meta, int64_t n_pages, int variant,
-                                       void* out, int out_dtype, const LutTables* lut, cudaStream_t s) {
+                                       void* out, int out_dtype, const LutTables* lut, int* status, cudaStream_t s) {
   const bool f32 = out_dtype == LYNX_OUT_F32;
   switch (variant) {
     case kVariantLynxInt8:
       return f32 ? launch<2, true>(codes, nullptr, meta, n_pages, out, lut, s)
                  : launch<2, false>(codes, nullptr, meta, n_pages, out, lut, s);
-    case kVariantLynxInt4:
-      return f32 ? launch<0, true>(codes, nullptr, meta, n_pages, out, lut, s)
-                 : launch<0, false>(codes, nullptr, meta, n_pages, out, lut, s);
+    case kVariantLynxInt4:   // the Anchor-plane layout with the 7-level table
+      return f32 ? launch_staged<false, true>(codes, nullptr, meta, n_pages, out, lut, status, s)
+                 : launch_staged<false, false>(codes, nullptr, meta, n_pages, out, lut, status, s);
     case kVariantUniformInt8:
     case kVariantUniformInt4: {
       const int64_t n_rows = n_pages * kH;
