@@ -33,7 +33,10 @@
 //            constants: O = O corr + A psum + B U.  l~ comes from a table of
 //            fp16 head/remainder pairs (two MMAs, ~22 bits); P is fp16, scaled
 //            by 2^10 away from fp16 subnormals (O and the row sums carry the
-//            2^10, removed once at the end).  Slot order of k-step kv: slots
+//            2^10, removed once at the end).  The row sums that normalise the
+//            output and weight A are those of the same fp16 probabilities (a
+//            matrix of ones times P^T), so a dominant key's rounding cancels.
+//            Slot order of k-step kv: slots
 //            2t, 2t+1 hold tokens 8t + 4kv + {0, 1}, slots 2t+8, 2t+9 hold
 //            8t + 4kv + {2, 3}.  With that order the A fragments are packed
 //            bytes as stored (both tokens of a byte in one register; bytes
@@ -147,6 +150,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+constexpr uint32_t kOnes2 = 0x3C003C00u;   // fp16 pair (1, 1)
 
 // UNI: uniform-code metadata (min, scale per channel row) instead of Lynx's
 template <bool FULL, int R, bool UNI>
@@ -287,11 +292,14 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   const int np = max(min(p_begin + a.pages_per_split, n_pages) - p_begin, 0);
   const int32_t* pt_row = a.page_table + ((int64_t)b * a.Hkv + h) * a.max_pages;
 
-  float m_run[NR], l_run[NR];
+  // m_run: rows 8 rh + g; l_run: the fp16 probabilities' row sums of rows
+  // 8 nt + 2t and 8 nt + 2t + 1 (the layout of the V side's U columns)
+  float m_run[NR];
+  float2 l_run[NR];
 #pragma unroll
   for (int rh = 0; rh < NR; ++rh) {
     m_run[rh] = -CUDART_INF_F;
-    l_run[rh] = 0.0f;
+    l_run[rh] = make_float2(0.0f, 0.0f);
   }
   // R = 16: O[mt][nt][c] = channel 16 mt + g + 8c, rows 8 nt + 2t and 8 nt + 2t + 1
   float2 O[kTmem ? 1 : 8][2][2];
@@ -478,37 +486,49 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
       if (L == 0) mbar_arrive(bar_empty + 8 * sK);
 
       // ---- online softmax: row 8 rh + g is accumulator half rh & 1 (S entries
-      // 2 (rh & 1) + hh) of m-tile rh >> 1; token 8t + j, j = 4 hh + k, sits in n-tile k
+      // 2 (rh & 1) + hh) of m-tile rh >> 1; token 8t + j, j = 4 hh + k, sits in n-tile k.
+      // One warp vote tells whether any score of the chunk exceeds its row's
+      // running maximum; only then are the row maxima taken by shuffles and the
+      // output rescaled.  Each probability x 2^10 is one exp2 of a fused
+      // multiply-add, 2^(S sck + 10 - m) <= 2^10, a masked score (-inf) giving 0.
+      // (Letting the maximum lag by up to 2^5 ran 2% faster, but then a
+      // dominant key's fp16 probability is no longer exactly 2^10 and the worst
+      // output error on an outlier channel rose from 3.6e-4 to 1.5e-3.)
       const int pos0 = p * kP + 32 * w + 8 * t;
       const bool all_visible = (p + 1) * kP <= min_vis;
-      float pr[NR][8];   // [rh][j], probabilities x 2^10
-      float corr[NR], psum[NR];
+      float pr[NR][8];   // [rh][j], raw scores, then probabilities x 2^10
+      float smax[NR];    // the lane's largest score of each row (scaled)
 #pragma unroll
       for (int rh = 0; rh < NR; ++rh) {
-        float mloc = -CUDART_INF_F;
+        float mx = -CUDART_INF_F;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float sv = sacc[rh >> 1][j & 3][2 * (rh & 1) + (j >> 2)] * sck;
+          float sv = sacc[rh >> 1][j & 3][2 * (rh & 1) + (j >> 2)];
           if (!all_visible && pos0 + j >= nv[rh]) sv = -CUDART_INF_F;
           pr[rh][j] = sv;
-          mloc = fmaxf(mloc, sv);
+          mx = fmaxf(mx, sv);
         }
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        const float mnew = fmaxf(m_run[rh], mloc);
-        corr[rh] = (mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[rh] - mnew);
-        float ps = 0.0f;
+        smax[rh] = mx * sck;   // sck > 0
+      }
+      bool up = false;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float sv = pr[rh][j];
-          const float pv = (sv == -CUDART_INF_F) ? 0.0f : exp2f(sv - mnew) * 1024.0f;
-          pr[rh][j] = pv;
-          ps += pv;
+      for (int rh = 0; rh < NR; ++rh) up |= smax[rh] > m_run[rh];
+      const bool rescale = __any_sync(0xffffffffu, up);
+      float corr[NR];
+#pragma unroll
+      for (int rh = 0; rh < NR; ++rh) {
+        float mnew = m_run[rh];
+        if (rescale) {
+          float mr = smax[rh];
+          mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 1));
+          mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 2));
+          mnew = fmaxf(m_run[rh], mr);
         }
-        l_run[rh] = l_run[rh] * corr[rh] + ps;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-        psum[rh] = ps;
+        corr[rh] = (!rescale || mnew == -CUDART_INF_F) ? 1.0f : exp2f(m_run[rh] - mnew);
+        // a row with no visible score yet (m = -inf) takes the reference 0
+        const float nref = (mnew == -CUDART_INF_F) ? 0.0f : 10.0f - mnew;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pr[rh][j] = exp2f(__fmaf_rn(pr[rh][j], sck, nref));
         m_run[rh] = mnew;
       }
       // P^T fragments of k-step kv, n-tile nt (rows 8 nt + g): tokens 8t + 4kv + {0,1} and + {2,3}
@@ -520,19 +540,23 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
           pb[kv][nt][0] = h2(pr[nt][4 * kv], pr[nt][4 * kv + 1]);
           pb[kv][nt][1] = h2(pr[nt][4 * kv + 2], pr[nt][4 * kv + 3]);
         }
-      // statistics of U's columns: rows 8 nt + 2t + e live in lane 8t + 4e
+      // statistics of U's columns, rows 8 nt + 2t + e: the corrections from lane
+      // 8t + 4e; the row sums of exactly the fp16 probabilities the V side
+      // multiplies, from a matrix of ones times P^T (so the normaliser and the
+      // A psum term use the same rounded weights as U)
       float2 cr[NR], pss[NR];
 #pragma unroll
       for (int nt = 0; nt < NR; ++nt) {
-        cr[nt] = make_float2(__shfl_sync(0xffffffffu, corr[nt], 8 * t),
-                             __shfl_sync(0xffffffffu, corr[nt], 8 * t + 4));
-        pss[nt] = make_float2(__shfl_sync(0xffffffffu, psum[nt], 8 * t),
-                              __shfl_sync(0xffffffffu, psum[nt], 8 * t + 4));
+        cr[nt] = make_float2(1.0f, 1.0f);
+        if (rescale)
+          cr[nt] = make_float2(__shfl_sync(0xffffffffu, corr[nt], 8 * t),
+                               __shfl_sync(0xffffffffu, corr[nt], 8 * t + 4));
+        float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16(ps4, kOnes2, kOnes2, kOnes2, kOnes2, pb[0][nt][0], pb[0][nt][1]);
+        mma_f16(ps4, kOnes2, kOnes2, kOnes2, kOnes2, pb[1][nt][0], pb[1][nt][1]);
+        pss[nt] = make_float2(ps4[0], ps4[1]);
+        l_run[nt] = __ffma2_rn(l_run[nt], cr[nt], pss[nt]);
       }
-      bool any_corr = false;
-#pragma unroll
-      for (int rh = 0; rh < NR; ++rh) any_corr |= corr[rh] != 1.0f;
-      const bool rescale = __any_sync(0xffffffffu, any_corr);
 
       // ---- V unit: U = l~ P^T per 16-channel m-tile, folded into O
       failed = __any_sync(0xffffffffu, !mbar_wait(bar_full + 8 * sV, (uV / kSt) & 1, a.wait_ns));
@@ -634,12 +658,10 @@ decode_tc_kernel(const DecodeArgs a, const LutTables lut,
   if (ok && warp < kConsumers) {
 #pragma unroll
     for (int rh = 0; rh < NR; ++rh) {
-      float lw = l_run[rh];
-      lw += __shfl_xor_sync(0xffffffffu, lw, 1);
-      lw += __shfl_xor_sync(0xffffffffu, lw, 2);
-      if (t == 0) {
-        mm[warp * R + 8 * rh + g] = m_run[rh];
-        ml[warp * R + 8 * rh + g] = lw;
+      if (t == 0) mm[warp * R + 8 * rh + g] = m_run[rh];
+      if (g == 0) {   // every g holds the row sums of rows 8 rh + 2t, + 1
+        ml[warp * R + 8 * rh + 2 * t] = l_run[rh].x;
+        ml[warp * R + 8 * rh + 2 * t + 1] = l_run[rh].y;
       }
     }
   }
