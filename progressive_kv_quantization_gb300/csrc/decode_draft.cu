@@ -14,13 +14,17 @@
 // low nibble in bits 0..15.  32 copies, one per lane (conflict-free lookups,
 // 4 bytes per byte of plane).
 //
-//   K side  S^T[32 tokens x 8 rows] = K Q^T as TF32 m16n8k8 (two m-tiles of
-//           16 tokens, 16 k-steps of 8 channels).  A value is rebuilt exactly
-//           as a float by one byte permute (u under the exponent of 2^23) and
-//           one subtraction, v = u - 2^14 = rint(l~ F); k = A + (B / F) v
+//   K side  S^T[32 tokens x 8 rows] = K Q^T as fp16 m16n8k16 (two m-tiles of
+//           16 tokens, 8 k-steps of 16 channels).  With k = A + B l~
 //           (A = gamma_min + (gamma_scale + eps) mu, B = (gamma_scale + eps)
-//           (sigma + eps)) is split into its TF32 head and remainder, two MMAs
-//           (~21-bit products).  Row g of m-tile mi holds token 4g + 2mi and
+//           (sigma + eps)) and l~ = (u - 2^14) / F, the chunk's scale is folded
+//           into the queries: Q' = q B / F 2^-ek (ek puts |Q'| below 2^15),
+//           split into an fp16 head and remainder, so that
+//           S = alpha + 2^(ek + 32) sum_c Q'_c u_c 2^-32 with
+//           alpha = sum_c q_c (A - B 2^14 / F).  The table's bytes of u enter
+//           the MMAs as they are (fp16 subnormals u_hi 2^-24, u_lo 2^-24):
+//           u_hi x Q'_head, u_hi x Q'_rem and u_lo x Q'_head 2^-8, three
+//           products in three accumulators (~21-bit products).  Row g of m-tile mi holds token 4g + 2mi and
 //           row g + 8 token 4g + 2mi + 1, the two tokens of one plane byte.
 //   V side  T[128 channels x 8 rows] = sum over the chunk's tokens of
 //           u 2^-32 p as fp16 m16n8k16: the two bytes of u are the fp16
