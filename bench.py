@@ -432,7 +432,7 @@ KERNEL_SOURCES = {
     "decode_anchor_b1": ["decode_draft.cu", "decode_common.cuh", "lynx_internal.cuh"],
     "decode_anchor_b8": ["decode_draft.cu", "decode_common.cuh", "lynx_internal.cuh"],
     "verify_full_t8": ["decode_tc.cu", "decode_common.cuh", "lynx_internal.cuh"],
-    "decode_bf16_b1": ["decode_attn.cu", "lynx_internal.cuh"],
+    "decode_bf16_b1": ["decode_bf16.cu", "decode_common.cuh", "lynx_internal.cuh"],
 }
 
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblynx.so")
 
 SOURCES = ["lynx_api.cu", "encode.cu", "reconstruct.cu", "decode_attn.cu", "decode_quant.cu", "decode_tc.cu",
-           "decode_narrow.cu", "decode_draft.cu",
+           "decode_narrow.cu", "decode_draft.cu", "decode_bf16.cu",
            "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

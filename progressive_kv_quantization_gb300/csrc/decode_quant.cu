@@ -1,7 +1,8 @@
 // Dispatch of the decode / verification attention over Lynx-encoded pages
 // (the attention of the Lynx paper's §2.1 over the KV that the Anchor and
-// Residual phases of §4.2-4.3 deliver) to its two tensor-core kernels, and the
-// TMA tensor maps both use to stream the 4-bit planes.
+// Residual phases of §4.2-4.3 deliver) to its tensor-core kernels, and the
+// TMA tensor maps the decode kernels use to stream the 4-bit planes and the
+// BF16 pages.
 //
 //   fewer than 12 query rows per KV head  decode_draft_kernel over Anchor planes
 //                                          with Lynx metadata (the draft decode at
@@ -60,6 +61,36 @@ bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool) {
   const cuuint32_t box[2] = {128, 128};
   const cuuint32_t estr[2] = {1, 1};
   const bool ok = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (ok) {
+    cache[next] = Entry{pool, n_pool, *m};
+    next = (next + 1) % kEntries;
+  }
+  return ok;
+}
+
+bool bf16_page_map(CUtensorMap* m, const uint16_t* pool, int64_t n_pool) {
+  struct Entry {
+    const uint16_t* pool;
+    int64_t n_pool;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i)
+    if (cache[i].pool == pool && cache[i].n_pool == n_pool && pool != nullptr) {
+      *m = cache[i].map;
+      return true;
+    }
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {kP, (cuuint64_t)n_pool * kH};
+  const cuuint64_t strides[1] = {kP * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const bool ok = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(pool), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   if (ok) {

@@ -192,6 +192,10 @@ cudaError_t launch_decode_narrow(const DecodeArgs& a, bool full, const LutTables
 // the draft decode kernel: Anchor planes with Lynx metadata and a table of
 // values |l~| < 1, fewer than 12 query rows per KV head (8 per CTA)
 cudaError_t launch_decode_draft(const DecodeArgs& a, const LutTables* lut, cudaStream_t s);
+// BF16 pages (the baseline): one CTA takes bf16_rows_per_cta(rows) query rows
+// of a (sequence, KV head), 8 or 16
+int bf16_rows_per_cta(int rows);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode_quant(const DecodeArgs& a, bool full, const LutTables* lut, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int mode, const LutTables* lut, cudaStream_t s);

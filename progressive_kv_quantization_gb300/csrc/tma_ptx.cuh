@@ -14,6 +14,11 @@ namespace lynx {
 // tile per page, 128-byte swizzle); false if the driver refuses it
 bool plane_map(CUtensorMap* m, const uint8_t* pool, int64_t n_pool);
 
+// 2-D tensor map over a pool of BF16 pages [n_pool][128][256] (rows of 512
+// bytes), boxes of 64 tokens x 128 channels (four per page), 128-byte swizzle;
+// false if the driver refuses it
+bool bf16_page_map(CUtensorMap* m, const uint16_t* pool, int64_t n_pool);
+
 // 2-D tensor map over token-major BF16 KV (row t = token t, row_elems valid
 // elements, stride elements between rows), boxes of 64 channels x 256 tokens,
 // no swizzle, zero fill past the last token; false if the driver refuses it
