@@ -326,6 +326,25 @@ def test_thirty_two_row_tiles_ragged(cuda_device, llama_pools, mode, T):
         check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
 
 
+@pytest.mark.parametrize("G,T", [(8, 1), (8, 2), (1, 17), (2, 12)])
+def test_bf16_row_tile_boundaries(cuda_device, llama_pools, G, T):
+    """BF16 pages: 8 query rows per KV head (one full 8-row tile), 16 (one
+    full 16-row tile), 17 (a full 16-row tile and one holding a single row)
+    and 24 (a full tile and a half one); causal and not, contexts of 0 keys,
+    fewer keys than T, a partial page and several pages."""
+    B, Hkv = 4, 2
+    Hq = G * Hkv
+    ctx = np.array([0, max(T - 3, 1), 2500, 5121])
+    table = np.stack([contiguous_table(1, Hkv, 24, 64, offset=5 * b)[0] for b in range(B)])
+    q = inputs.queries_np((B, T, Hq, 128), 500 + 10 * G + T)
+    for causal in (False, True):
+        o, lse = run(llama_pools, "bf16", q, table, ctx, Hkv, causal)
+        ro, rl = reference(llama_pools, "bf16", q, table, ctx, Hkv, causal)
+        empty = np.isnan(ro[..., 0])
+        assert np.all(o[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
+        check_attention(o, lse, np.nan_to_num(ro), rl, mask=~empty)
+
+
 @pytest.mark.parametrize("mode", ["anchor", "full"])
 def test_extreme_row_counts_and_alpha(cuda_device, mode):
     """The largest supported row count per KV head (T = 32, G = 8: 256 rows in 8
