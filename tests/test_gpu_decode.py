@@ -411,6 +411,38 @@ def test_extreme_magnitudes(cuda_device, mode, T):
         check_attention(o, lse, ro, rl)
 
 
+@pytest.mark.parametrize("T", [1, 8])
+def test_bf16_extreme_magnitudes(cuda_device, T):
+    """BF16 pages with queries of magnitude 2^24 and 2^-30 and keys of 2^30 and
+    2^-30 (the softmax scale compensates): BF16 products are exact and sum in
+    float32, so only the float32 range matters.  8-row (T = 1) and 16-row
+    (T = 8: 32 rows per KV head) tiles."""
+    base = Pools(2, 2048, 13, lazy=True)
+    B, Hq, Hkv = 2, 8, 2
+    ctx = np.array([2048, 1500])
+    table = np.stack([contiguous_table(1, Hkv, 8, 8, offset=b)[0] for b in range(B)])
+    pt = torch.from_numpy(table.astype(np.int32)).cuda()
+    cl = torch.from_numpy(ctx.astype(np.int32)).cuda()
+    q0 = lo.bf16_to_f32(inputs.queries_np((B, T, Hq, 128), 960 + T)).astype(np.float64)
+    s0 = 1.0 / math.sqrt(128)
+    # a BF16 value times a power of two (in range) is a BF16 value: keep the top 16 bits
+    scale_bits = lambda x, e: ((x * 2.0 ** e).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    v64 = lo.bf16_to_f32(base.vb).astype(np.float64)
+    for qe, ke in ((24, 0), (-30, 0), (0, 30), (0, -30)):
+        kbits = scale_bits(lo.bf16_to_f32(base.kb).astype(np.float64), ke)
+        qbits = scale_bits(q0, qe)
+        scale = s0 * 2.0 ** (-qe - ke)
+        q = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).cuda()
+        k = torch.from_numpy(kbits.view(np.int16)).view(torch.bfloat16).cuda()
+        o, lse = L.lynx_decode_attn_bf16(q, k, base.dev_bf16["v"], pt, cl, Hkv, sm_scale=scale, causal=True)
+        torch.cuda.synchronize()
+        L.lynx_device_status()
+        k64 = lo.bf16_to_f32(kbits).astype(np.float64)
+        ro, rl = at.decode_attention(lo.bf16_to_f32(qbits).astype(np.float64), lambda ids: (k64[ids], v64[ids]),
+                                     table, ctx, Hkv, scale, True)
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl)
+
+
 @pytest.mark.parametrize("entry", ["anchor", "full_t8", "bf16", "noalloc"])
 def test_decode_replays_in_cuda_graph(cuda_device, llama_pools, entry):
     """A decode call captured in a CUDA graph (after one eager call on the
