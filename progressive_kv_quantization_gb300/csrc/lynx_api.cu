@@ -356,6 +356,12 @@ int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* par
   return LYNX_OK;
 }
 
+namespace {
+// reconstruct and quantised decode calls of this host thread still to run
+// with the wait time-out injected (lynx_test_inject_wait_timeout)
+thread_local int g_inject_calls = 0;
+}  // namespace
+
 int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                      int64_t n_pages, const lynx_params_t* params, void* out, int out_dtype,
                      void* stream) {
@@ -373,17 +379,21 @@ int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float
   const LutTables* lut = lut_tables(params->alpha, params->eps);
   int* status = device_status_ptr();
   if (!status) return fail(LYNX_ERR_CUDA, "cannot resolve the device status word");
-  cudaError_t e = launch_reconstruct(anchor, residual, meta, n_pages, out, out_dtype, lut, status,
-                                     static_cast<cudaStream_t>(stream));
+  unsigned long long wait_ns = kDefaultWaitNs;
+  int skip_unit = -1;
+  if (g_inject_calls > 0) {   // test hook, off unless armed
+    --g_inject_calls;
+    skip_unit = 0;          // the first page of every CTA is never copied
+    wait_ns = 1000000ull;   // and every wait gives up after 1 ms
+  }
+  cudaError_t e = launch_reconstruct(anchor, residual, meta, n_pages, out, out_dtype, lut, status, wait_ns,
+                                     skip_unit, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_reconstruct launch");
   return LYNX_OK;
 }
 
 namespace {
 
-// quantised decode calls of this host thread still to run with the wait
-// time-out injected (lynx_test_inject_wait_timeout)
-thread_local int g_inject_calls = 0;
 
 int check_decode_shape(int B, int T, int Hq, int Hkv, int head_dim, int max_pages) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || max_pages < 1)

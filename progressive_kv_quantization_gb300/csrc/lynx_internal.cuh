@@ -128,9 +128,11 @@ cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, i
                                  cudaStream_t s);
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,
                             cudaStream_t s);
+// wait_ns bounds every wait of the staged kernel; skip_unit >= 0 (test hook
+// only) makes the producer of every CTA never copy its page skip_unit
 cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                                int64_t n_pages, void* out, int out_dtype, const LutTables* lut, int* status,
-                               cudaStream_t s);
+                               unsigned long long wait_ns, int skip_unit, cudaStream_t s);
 
 enum DecodeMode { kModeAnchor = 0, kModeFull = 1, kModeBf16 = 2 };
 

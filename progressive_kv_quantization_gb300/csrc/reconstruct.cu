@@ -189,7 +189,8 @@ template <bool kFull, bool kF32>
 __global__ void __launch_bounds__(kRThreads, 1)
 reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
                           const float* __restrict__ meta, int64_t n_pages, void* __restrict__ out,
-                          const LutTables lut, int* __restrict__ status) {
+                          const LutTables lut, int* __restrict__ status, unsigned long long wait_ns,
+                          int skip_unit) {
   using S = RLayout<kFull>;
   constexpr int kRStages = S::kRStages;
   constexpr int kEntries = kFull ? 256 : 16;
@@ -227,11 +228,12 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
     bool ok = true;
     for (int u = 0; u < n_mine; ++u) {
       const int st = u % kRStages;
-      if (u >= kRStages && !mbar_wait(bar_empty + 8 * st, ((u / kRStages) - 1) & 1)) {
+      if (u >= kRStages && !mbar_wait(bar_empty + 8 * st, ((u / kRStages) - 1) & 1, wait_ns)) {
         ok = false;
         break;
       }
       u_end = u + 1;
+      if (u == skip_unit) continue;   // test hook: this page's copy is never issued
       const int64_t page = first + (int64_t)u * stride;
       const uint32_t dst = base + S::kRing + st * S::kUnit;
       const uint32_t bar = bar_full + 8 * st;
@@ -246,7 +248,7 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
     }
     // every copy this lane issued has landed before the CTA may exit
     for (int u = u_end - 1; u >= 0 && u >= u_end - kRStages; --u)
-      mbar_wait(bar_full + 8 * (u % kRStages), (u / kRStages) & 1);
+      if (u != skip_unit) mbar_wait(bar_full + 8 * (u % kRStages), (u / kRStages) & 1, wait_ns);
     return;
   }
 
@@ -256,7 +258,7 @@ reconstruct_staged_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __r
   const int c = lane >> 2;   // the lane group's chunk
   for (int u = 0; u < n_mine; ++u) {
     const int st = u % kRStages;
-    const bool got = mbar_wait(bar_full + 8 * st, (u / kRStages) & 1);
+    const bool got = mbar_wait(bar_full + 8 * st, (u / kRStages) & 1, wait_ns);
     if (__any_sync(0xffffffffu, !got) || *reinterpret_cast<volatile int*>(s_flag) != 0) {
       if (lane == 0) {
         atomicExch(status, 1);
@@ -511,7 +513,8 @@ cudaError_t launch(const uint8_t* anchor, const uint8_t* residual, const float* 
 // one CTA per SM (each holds kRStages pages), pages taken round robin
 template <bool kFull, bool kF32>
 cudaError_t launch_staged(const uint8_t* anchor, const uint8_t* residual, const float* meta, int64_t n_pages,
-                          void* out, const LutTables* lut, int* status, cudaStream_t s) {
+                          void* out, const LutTables* lut, int* status, cudaStream_t s,
+                          unsigned long long wait_ns = kDefaultWaitNs, int skip_unit = -1) {
   constexpr int kSmem = RLayout<kFull>::kTotal;
   static bool configured[64] = {false};
   int dev = 0;
@@ -525,7 +528,7 @@ cudaError_t launch_staged(const uint8_t* anchor, const uint8_t* residual, const 
   const int64_t sms = device_sm_count();
   const int blocks = (int)(n_pages < sms ? n_pages : sms);
   return launch_programmatic(reconstruct_staged_kernel<kFull, kF32>, dim3(blocks), dim3(kRThreads), kSmem, s,
-                             anchor, residual, meta, n_pages, out, *lut, status);
+                             anchor, residual, meta, n_pages, out, *lut, status, wait_ns, skip_unit);
 }
 
 }  // namespace
@@ -541,15 +544,15 @@ cudaError_t launch_split_nibbles(const uint8_t* codes, int64_t n_rows, uint8_t* 
 
 cudaError_t launch_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                                int64_t n_pages, void* out, int out_dtype, const LutTables* lut, int* status,
-                               cudaStream_t s) {
+                               unsigned long long wait_ns, int skip_unit, cudaStream_t s) {
   const bool full = residual != nullptr;
   const bool f32 = out_dtype == LYNX_OUT_F32;
   if (full) {
-    return f32 ? launch_staged<true, true>(anchor, residual, meta, n_pages, out, lut, status, s)
-               : launch_staged<true, false>(anchor, residual, meta, n_pages, out, lut, status, s);
+    return f32 ? launch_staged<true, true>(anchor, residual, meta, n_pages, out, lut, status, s, wait_ns, skip_unit)
+               : launch_staged<true, false>(anchor, residual, meta, n_pages, out, lut, status, s, wait_ns, skip_unit);
   }
-  return f32 ? launch_staged<false, true>(anchor, residual, meta, n_pages, out, lut, status, s)
-             : launch_staged<false, false>(anchor, residual, meta, n_pages, out, lut, status, s);
+  return f32 ? launch_staged<false, true>(anchor, residual, meta, n_pages, out, lut, status, s, wait_ns, skip_unit)
+             : launch_staged<false, false>(anchor, residual, meta, n_pages, out, lut, status, s, wait_ns, skip_unit);
 }
 
 cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,

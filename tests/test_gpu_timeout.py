@@ -4,9 +4,9 @@ its first V page and shortens every wait to 1 ms.  The call must return, the
 device error word must say that a wait gave up, and the next, normal call must
 give exactly the result it gives without the fault (the kernel drained its
 copies and freed its tensor memory).  Covers the draft kernel (anchor, T = 1),
-the narrow kernel (full codes, T = 1; uniform INT4) and the verification
+the narrow kernel (full codes, T = 1; uniform INT4), the verification
 kernel with 16-row register tiles (T = 4) and 32-row tensor-memory tiles
-(T = 8)."""
+(T = 8), and the staged reconstruction (Anchor only and full codes)."""
 import numpy as np
 import pytest
 import torch
@@ -64,6 +64,30 @@ def test_wait_that_runs_out_is_reported_and_the_context_recovers(pools, mode, T)
         torch.cuda.synchronize()
         L.lynx_device_status()
         assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_reconstruct_wait_that_runs_out_is_reported_and_the_context_recovers(pools, full):
+    """The staged reconstruction: with the hook armed every CTA's producer skips
+    its first page, the consumers' 1 ms waits run out, the error word is set;
+    the next calls are normal and bit-identical to a call before the fault."""
+    ka, kr, km = pools["k"]
+    res = kr if full else None
+    ref = L.lynx_reconstruct(ka, res, km)
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    lib = L.load()
+    assert lib.lynx_test_inject_wait_timeout(1) == 0
+    L.lynx_reconstruct(ka, res, km)
+    torch.cuda.synchronize()
+    with pytest.raises(L.LynxError, match="error word = 1"):
+        L.lynx_device_status()
+    L.lynx_device_status()       # read and cleared
+    for _ in range(2):
+        out = L.lynx_reconstruct(ka, res, km)
+        torch.cuda.synchronize()
+        L.lynx_device_status()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
 def test_hook_rejects_negative_counts(cuda_device):
