@@ -400,8 +400,9 @@ int lynx_attn_merge(const float* o_a, const float* lse_a, const float* o_b, cons
 size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_dim, int max_pages);
 
 /* Test hook (not for production use; off by default): the next n_calls calls
- * of lynx_decode_attn, lynx_decode_attn_int4, lynx_decode_attn_uniform or
- * lynx_reconstruct made from this host thread run with a fault planted on the
+ * of lynx_decode_attn, lynx_decode_attn_bf16, lynx_decode_attn_int4,
+ * lynx_decode_attn_uniform or lynx_reconstruct made from this host thread run
+ * with a fault planted on the
  * host side of the launch: the producer of every CTA never issues the copy of
  * its first V page (decode) or of its first page (reconstruct), and every
  * bounded wait of those kernels gives up after 1 ms instead of 2 s.  The

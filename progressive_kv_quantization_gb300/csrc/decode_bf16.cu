@@ -103,6 +103,7 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uin
 __device__ void produce_bf16(const DecodeArgs& a, const int32_t* pt_row, int p_begin, int np, int first_id,
                              uint32_t s_ring, uint32_t bar_full, uint32_t bar_empty, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, int* s_flag) {
+  const int skip = a.inject_skip - 1;   // -1: no unit is skipped
   int u_end = 0;
   bool ok = true;
   int64_t id = first_id;
@@ -115,6 +116,7 @@ __device__ void produce_bf16(const DecodeArgs& a, const int32_t* pt_row, int p_b
     u_end = u + 1;
     const bool is_v = (u & 1) != 0;
     if (u >= 2 && !is_v) id = pt_row[p_begin + (u >> 1)];
+    if (u == skip) continue;   // test hook: this unit's copy is never issued
     if (id < 0 || id >= a.n_pool) {
       atomicExch(a.status, 2);
       id = 0;
@@ -130,7 +132,7 @@ __device__ void produce_bf16(const DecodeArgs& a, const int32_t* pt_row, int p_b
     *s_flag = 1;
   }
   for (int u = u_end - 1; u >= 0 && u >= u_end - kBStages; --u)
-    mbar_wait(bar_full + 8 * (u % kBStages), (u / kBStages) & 1, a.wait_ns);
+    if (u != skip) mbar_wait(bar_full + 8 * (u % kBStages), (u / kBStages) & 1, a.wait_ns);
 }
 
 template <int NT>

@@ -460,7 +460,7 @@ int decode_common(DecodeArgs& a, int mode, const void* q, int B, int T, int Hq, 
     a.code_max = 1.0f;
   }
   a.wait_ns = kDefaultWaitNs;
-  if (mode != kModeBf16 && g_inject_calls > 0) {   // test hook, off unless armed
+  if (g_inject_calls > 0) {   // test hook, off unless armed
     --g_inject_calls;
     a.inject_skip = 2;       // the first V unit of every split is never copied
     a.wait_ns = 1000000ull;  // and every wait gives up after 1 ms

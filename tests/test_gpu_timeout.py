@@ -6,7 +6,8 @@ give exactly the result it gives without the fault (the kernel drained its
 copies and freed its tensor memory).  Covers the draft kernel (anchor, T = 1),
 the narrow kernel (full codes, T = 1; uniform INT4), the verification
 kernel with 16-row register tiles (T = 4) and 32-row tensor-memory tiles
-(T = 8), and the staged reconstruction (Anchor only and full codes)."""
+(T = 8), the BF16 decode kernel (8- and 16-row tiles) and the staged
+reconstruction (Anchor only and full codes)."""
 import numpy as np
 import pytest
 import torch
@@ -28,7 +29,7 @@ def pools(cuda_device):
     uk, um = L.lynx_encode_variant(k, "uniform_int4")
     uv, uvm = L.lynx_encode_variant(v, "uniform_int4")
     table = torch.arange(Hkv * 16, dtype=torch.int32, device="cuda").view(1, Hkv, 16)
-    return dict(Hkv=Hkv, k=(ka, kr, km), v=(va, vr, vm), u=(uk, um, uv, uvm), table=table,
+    return dict(Hkv=Hkv, k=(ka, kr, km), v=(va, vr, vm), u=(uk, um, uv, uvm), kb=k, vb=v, table=table,
                 ctx=torch.tensor([n_tok], dtype=torch.int32, device="cuda"))
 
 
@@ -37,6 +38,8 @@ def _call(p, mode, T):
     q = inputs.queries_torch((1, T, 4 * Hkv, 128), 73 + T, "cuda")
     ka, kr, km = p["k"]
     va, vr, vm = p["v"]
+    if mode == "bf16":
+        return L.lynx_decode_attn_bf16(q, p["kb"], p["vb"], p["table"], p["ctx"], Hkv, causal=T > 1)
     if mode == "uniform4":
         uk, um, uv, uvm = p["u"]
         return L.lynx_decode_attn_uniform(q, 4, uk.view(-1, 128, 128), None, um, uv.view(-1, 128, 128), None, uvm,
@@ -47,7 +50,7 @@ def _call(p, mode, T):
 
 
 @pytest.mark.parametrize("mode,T", [("anchor", 1), ("full", 1), ("uniform4", 1), ("full", 4), ("full", 8),
-                                    ("anchor", 8)])
+                                    ("anchor", 8), ("bf16", 1), ("bf16", 8)])
 def test_wait_that_runs_out_is_reported_and_the_context_recovers(pools, mode, T):
     o_ref, l_ref = _call(pools, mode, T)
     torch.cuda.synchronize()
