@@ -401,16 +401,18 @@ size_t lynx_decode_attn_workspace_size(int B, int T, int Hq, int Hkv, int head_d
 
 /* Test hook (not for production use; off by default): the next n_calls calls
  * of lynx_decode_attn, lynx_decode_attn_bf16, lynx_decode_attn_int4,
- * lynx_decode_attn_uniform or lynx_reconstruct made from this host thread run
- * with a fault planted on the
- * host side of the launch: the producer of every CTA never issues the copy of
- * its first V page (decode) or of its first page (reconstruct), and every
- * bounded wait of those kernels gives up after 1 ms instead of 2 s.  The
- * consumers' waits for that page then run out, the kernel records device
- * error word 1, drains the copies it did issue, frees its tensor memory and
- * returns; the call's outputs are unspecified.  Used to check that a wait that
- * runs out leaves the context usable.  n_calls = 0 disarms it.  The paper has
- * no counterpart.  Errors: INVALID_ARG (n_calls < 0). */
+ * lynx_decode_attn_uniform, lynx_reconstruct or lynx_encode_tokens made from
+ * this host thread run with a fault planted on the host side of the launch:
+ * every CTA never issues the copy of its first V page (decode), of its first
+ * page (reconstruct) or of its first item (the token encoder's TMA-staged
+ * kernel; an input that admits no tensor map takes the other kernel, which
+ * has no waits, and the call runs normally), and every bounded wait of those
+ * kernels gives up after 1 ms instead of 2 s.  The waits for that copy then run
+ * out, the kernel records device error word 1, drains the copies it did
+ * issue, frees its tensor memory and returns; the call's outputs are
+ * unspecified.  Used to check that a wait that runs out leaves the context
+ * usable.  n_calls = 0 disarms it.  The paper has no counterpart.  Errors:
+ * INVALID_ARG (n_calls < 0). */
 int lynx_test_inject_wait_timeout(int n_calls);
 
 /* Reads and clears the current device's error word, which kernels set when a

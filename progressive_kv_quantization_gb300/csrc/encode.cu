@@ -487,7 +487,8 @@ template <bool PARTIAL>
 __global__ void __launch_bounds__(256, 2)
 encode_tokens_tma_kernel(const __grid_constant__ CUtensorMap tm, int64_t n_tokens, int n_heads, int n_pp,
                          int j_begin, int j_count, uint4* __restrict__ anchor, uint4* __restrict__ residual,
-                         float* __restrict__ meta, const EncodeTables tab, int* __restrict__ status) {
+                         float* __restrict__ meta, const EncodeTables tab, int* __restrict__ status,
+                         unsigned long long wait_ns, bool skip_first) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_thr[129];
   __shared__ float2 s_mn[2][8][32], s_mx[2][8][32];   // [parity][chunk][lane]: channels 2L, 2L + 1
@@ -521,22 +522,23 @@ encode_tokens_tma_kernel(const __grid_constant__ CUtensorMap tm, int64_t n_token
   for (int i = tid; i < 129; i += blockDim.x) s_thr[i] = tab.thr[i];
   __syncthreads();
   if (tid == 0)
-    for (int k = 0; k < kTokSlots; ++k)
-      if (blockIdx.x + (int64_t)k * gridDim.x < n_items) issue(blockIdx.x + (int64_t)k * gridDim.x, k);
+    for (int k = 0; k < kTokSlots; ++k)   // (test hook: skip_first leaves the first item uncopied)
+      if (blockIdx.x + (int64_t)k * gridDim.x < n_items && !(skip_first && k == 0))
+        issue(blockIdx.x + (int64_t)k * gridDim.x, k);
 
   const float eps = tab.eps;
   const QuantConsts qc{f2(tab.alpha), f2(tab.c_lg2), tab.edge};
   int k = 0;
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
     const int slot = k % kTokSlots, par = k & 1;
-    const bool ok = mbar_wait(bars + 8 * slot, (uint32_t)((k / kTokSlots) & 1));
+    const bool ok = mbar_wait(bars + 8 * slot, (uint32_t)((k / kTokSlots) & 1), wait_ns);
     if (__syncthreads_or(!ok)) {
       // a copy never landed: record it, wait (bounded) for the copies in flight, leave
       if (tid == 0) {
         atomicExch(status, 1);
         for (int u = 1; u < kTokSlots; ++u)
           if (item + (int64_t)u * gridDim.x < n_items)
-            mbar_wait(bars + 8 * ((k + u) % kTokSlots), (uint32_t)(((k + u) / kTokSlots) & 1));
+            mbar_wait(bars + 8 * ((k + u) % kTokSlots), (uint32_t)(((k + u) / kTokSlots) & 1), wait_ns);
       }
       return;
     }
@@ -851,7 +853,8 @@ cudaError_t launch_tokens_t(const void* x, int64_t n_tokens, int n_heads, int n_
 template <bool PARTIAL>
 cudaError_t launch_tokens_tma(const CUtensorMap& tm, int64_t n_tokens, int n_heads, int n_pp, int j_begin,
                               int j_count, uint8_t* anchor, uint8_t* residual, float* meta,
-                              const EncodeTables* tab, cudaStream_t s) {
+                              const EncodeTables* tab, unsigned long long wait_ns, bool skip_first,
+                              cudaStream_t s) {
   const int64_t n_items = (int64_t)n_heads * j_count * 2;
   if (n_items == 0) return cudaSuccess;
   static bool configured[64] = {false};
@@ -867,7 +870,7 @@ cudaError_t launch_tokens_tma(const CUtensorMap& tm, int64_t n_tokens, int n_hea
   const int blocks = (int)(n_items < max_blocks ? n_items : max_blocks);
   encode_tokens_tma_kernel<PARTIAL><<<blocks, 256, kTokSmem, s>>>(
       tm, n_tokens, n_heads, n_pp, j_begin, j_count, reinterpret_cast<uint4*>(anchor),
-      reinterpret_cast<uint4*>(residual), meta, *tab, device_status_ptr());
+      reinterpret_cast<uint4*>(residual), meta, *tab, device_status_ptr(), wait_ns, skip_first);
   return cudaGetLastError();
 }
 
@@ -876,15 +879,16 @@ cudaError_t launch_tokens_tma(const CUtensorMap& tm, int64_t n_tokens, int n_hea
 // through the kernel that reads the channels straight from global memory.
 cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
                                  uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
-                                 cudaStream_t s) {
+                                 unsigned long long wait_ns, bool skip_first, cudaStream_t s) {
   const int n_pp = (int)((n_tokens + 255) / 256);
   const int n_full = (int)(n_tokens / 256);
   CUtensorMap tm;
   if (token_map(&tm, x, n_tokens, (int64_t)n_heads * kH, stride)) {
     cudaError_t e = launch_tokens_tma<false>(tm, n_tokens, n_heads, n_pp, 0, n_full, anchor, residual, meta,
-                                            tab, s);
+                                            tab, wait_ns, skip_first, s);
     if (e != cudaSuccess || n_full == n_pp) return e;
-    return launch_tokens_tma<true>(tm, n_tokens, n_heads, n_pp, n_full, 1, anchor, residual, meta, tab, s);
+    return launch_tokens_tma<true>(tm, n_tokens, n_heads, n_pp, n_full, 1, anchor, residual, meta, tab, wait_ns,
+                                   skip_first, s);
   }
   cudaError_t e = launch_tokens_t<false>(x, n_tokens, n_heads, n_pp, 0, n_full, stride, anchor, residual, meta,
                                          tab, s);

@@ -16,6 +16,10 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
+// calls of this host thread still to run with the wait time-out injected
+// (lynx_test_inject_wait_timeout): token encode, reconstruct and decode
+thread_local int g_inject_calls = 0;
+
 int fail(int status, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -335,8 +339,15 @@ int lynx_encode_tokens(const void* x_bf16, int64_t n_tokens, int n_heads, int64_
   if (n_tokens > ((int64_t)1 << 40) || (int64_t)n_heads * ((n_tokens + 255) / 256) > ((int64_t)1 << 40))
     return fail(LYNX_ERR_INVALID_ARG, "too many tokens");
   const EncodeTables* tab = encode_tables(params->alpha, params->eps);
+  unsigned long long wait_ns = kDefaultWaitNs;
+  bool skip_first = false;
+  if (g_inject_calls > 0) {   // test hook, off unless armed
+    --g_inject_calls;
+    skip_first = true;      // the first item of every CTA is never copied
+    wait_ns = 1000000ull;   // and every wait gives up after 1 ms
+  }
   cudaError_t e = launch_encode_tokens(x_bf16, n_tokens, n_heads, token_stride, anchor, residual, meta, tab,
-                                       static_cast<cudaStream_t>(stream));
+                                       wait_ns, skip_first, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lynx_encode_tokens launch");
   return LYNX_OK;
 }
@@ -355,12 +366,6 @@ int lynx_quantize_magnitudes(const float* a, int64_t n, const lynx_params_t* par
   if (e != cudaSuccess) return cuda_fail(e, "lynx_quantize_magnitudes launch");
   return LYNX_OK;
 }
-
-namespace {
-// reconstruct and quantised decode calls of this host thread still to run
-// with the wait time-out injected (lynx_test_inject_wait_timeout)
-thread_local int g_inject_calls = 0;
-}  // namespace
 
 int lynx_reconstruct(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                      int64_t n_pages, const lynx_params_t* params, void* out, int out_dtype,

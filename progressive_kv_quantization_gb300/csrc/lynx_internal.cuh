@@ -123,9 +123,11 @@ cudaError_t launch_encode_split(const void* x, int64_t n_pages, int anchor_bits,
 cudaError_t launch_reconstruct_split(const uint8_t* anchor, const uint8_t* residual, const float* meta,
                                      int64_t n_pages, int anchor_bits, void* out, int out_dtype,
                                      const SplitTables* st, const LutTables* lut8, cudaStream_t s);
+// wait_ns bounds the waits of the TMA-staged kernel; skip_first (test hook
+// only) makes every CTA of it never copy its first item
 cudaError_t launch_encode_tokens(const void* x, int64_t n_tokens, int n_heads, int64_t stride,
                                  uint8_t* anchor, uint8_t* residual, float* meta, const EncodeTables* tab,
-                                 cudaStream_t s);
+                                 unsigned long long wait_ns, bool skip_first, cudaStream_t s);
 cudaError_t launch_quantize(const float* a, int64_t n, uint8_t* codes, const EncodeTables* tab,
                             cudaStream_t s);
 // wait_ns bounds every wait of the staged kernel; skip_unit >= 0 (test hook

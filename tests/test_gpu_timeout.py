@@ -6,8 +6,9 @@ give exactly the result it gives without the fault (the kernel drained its
 copies and freed its tensor memory).  Covers the draft kernel (anchor, T = 1),
 the narrow kernel (full codes, T = 1; uniform INT4), the verification
 kernel with 16-row register tiles (T = 4) and 32-row tensor-memory tiles
-(T = 8), the BF16 decode kernel (8- and 16-row tiles) and the staged
-reconstruction (Anchor only and full codes)."""
+(T = 8), the BF16 decode kernel (8- and 16-row tiles), the staged
+reconstruction (Anchor only and full codes) and the TMA-staged token-major
+encoder."""
 import numpy as np
 import pytest
 import torch
@@ -91,6 +92,30 @@ def test_reconstruct_wait_that_runs_out_is_reported_and_the_context_recovers(poo
         torch.cuda.synchronize()
         L.lynx_device_status()
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_token_encoder_wait_that_runs_out_is_reported_and_the_context_recovers(cuda_device):
+    """The TMA-staged token-major encoder (600 tokens of 3 heads: full pages
+    and a partial last page, two launches): with the hook armed every CTA skips
+    its first item's copy; the error word is set; later calls are exact."""
+    n_heads, n_tok = 3, 600
+    xt = inputs.queries_torch((n_tok, n_heads * 128), 77, "cuda")
+    ref = [t.clone() for t in L.lynx_encode_tokens(xt, n_heads)]
+    torch.cuda.synchronize()
+    L.lynx_device_status()
+    lib = L.load()
+    assert lib.lynx_test_inject_wait_timeout(1) == 0
+    L.lynx_encode_tokens(xt, n_heads)
+    torch.cuda.synchronize()
+    with pytest.raises(L.LynxError, match="error word = 1"):
+        L.lynx_device_status()
+    L.lynx_device_status()       # read and cleared
+    for _ in range(2):
+        got = L.lynx_encode_tokens(xt, n_heads)
+        torch.cuda.synchronize()
+        L.lynx_device_status()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
 
 
 def test_hook_rejects_negative_counts(cuda_device):
