@@ -219,9 +219,11 @@ def test_end_to_end_encode_then_decode(cuda_device):
 @pytest.mark.slow
 def test_qwen235b_layers_full_context_sampled(cuda_device):
     """Qwen3-235B-A22B-shaped layers at the full 131,072-token context (4 KV
-    heads, 16 query heads): GPU encode of the layer's K and V, anchor-only
-    decode over the whole context; two query heads of every KV head are checked
-    against the oracle (which re-encodes the same BF16 pages)."""
+    heads, 16 query heads): GPU encode of the layer's K and V, then the three
+    decode calls of the benchmark step over the whole context -- the Anchor
+    draft (T = 1), the causal T = 8 verification over the full codes (32 rows
+    per KV head) and the BF16 decode (T = 1); four query heads (one per KV head)
+    are checked against the oracle, which re-encodes the same BF16 pages."""
     w = inputs.QWEN235B_CACHE
     outl = inputs.outlier_pairs(w.n_kv_heads, 0)
     Hkv, Hq = w.n_kv_heads, w.n_q_heads
@@ -233,30 +235,44 @@ def test_qwen235b_layers_full_context_sampled(cuda_device):
         npph = w.pages_per_head
         table = contiguous_table(1, Hkv, npph, npph)
         ctx = np.array([w.n_tokens])
-        qb = inputs.queries_np((1, 1, Hq, 128), 500 + layer)
-        q = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).cuda()
-        o, lse = L.lynx_decode_attn(q, ka, None, km, va, None, vm, torch.from_numpy(table).cuda(),
-                                    torch.from_numpy(ctx.astype(np.int32)).cuda(), Hkv)
-        torch.cuda.synchronize()
-        L.lynx_device_status()
+        pt = torch.from_numpy(table).cuda()
+        cl = torch.from_numpy(ctx.astype(np.int32)).cuda()
         kbits = k.view(torch.int16).cpu().numpy().view(np.uint16)
         vbits = v.view(torch.int16).cpu().numpy().view(np.uint16)
         heads = [0, 5, 10, 15]
-        cache = {}
+        sel_h = np.zeros(Hq, dtype=bool)
+        sel_h[heads] = True
+        enc = {}   # the oracle's planes of each KV head's pages (encoded once)
 
-        def fetch(ids):
+        def pages(ids, mode):
+            if mode == "bf16":
+                return (lo.bf16_to_f32(kbits[ids]).astype(np.float64), lo.bf16_to_f32(vbits[ids]).astype(np.float64))
             key = int(ids[0])
-            if key not in cache:
-                oa, _, om = lo.encode_pages(kbits[ids], 100.0, EPS)
-                ova, _, ovm = lo.encode_pages(vbits[ids], 100.0, EPS)
-                cache[key] = (lo.reconstruct(oa, None, om, 100.0, EPS), lo.reconstruct(ova, None, ovm, 100.0, EPS))
-            return cache[key]
-        ro, rl = at.decode_attention(lo.bf16_to_f32(qb).astype(np.float64), fetch, table, ctx, Hkv,
-                                     1 / math.sqrt(128), False, q_heads=heads)
-        sel = np.zeros(o.shape[:3], dtype=bool)
-        sel[:, :, heads] = True
-        check_attention(o.cpu().numpy(), lse.cpu().numpy(), np.nan_to_num(ro), np.nan_to_num(rl, nan=0.0),
-                        mask=sel)
+            if key not in enc:
+                enc[key] = (lo.encode_pages(kbits[ids], 100.0, EPS), lo.encode_pages(vbits[ids], 100.0, EPS))
+            (oa, orr, om), (ova, ovr, ovm) = enc[key]
+            full = mode == "full"
+            return (lo.reconstruct(oa, orr if full else None, om, 100.0, EPS),
+                    lo.reconstruct(ova, ovr if full else None, ovm, 100.0, EPS))
+
+        for mode, T in (("anchor", 1), ("full", 8), ("bf16", 1)):
+            qb = inputs.queries_np((1, T, Hq, 128), 500 + layer + 7 * T)
+            q = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).cuda()
+            causal = T > 1
+            if mode == "bf16":
+                o, lse = L.lynx_decode_attn_bf16(q, k, v, pt, cl, Hkv, causal=causal)
+            else:
+                full = mode == "full"
+                o, lse = L.lynx_decode_attn(q, ka, kr if full else None, km, va, vr if full else None, vm, pt, cl,
+                                            Hkv, causal=causal)
+            torch.cuda.synchronize()
+            L.lynx_device_status()
+            ro, rl = at.decode_attention(lo.bf16_to_f32(qb).astype(np.float64), lambda ids: pages(ids, mode),
+                                         table, ctx, Hkv, 1 / math.sqrt(128), causal, q_heads=heads)
+            sel = np.zeros(o.shape[:3], dtype=bool)
+            sel[:, :, sel_h] = True
+            check_attention(o.cpu().numpy(), lse.cpu().numpy(), np.nan_to_num(ro), np.nan_to_num(rl, nan=0.0),
+                            mask=sel)
         del k, v, ka, kr, km, va, vr, vm
         torch.cuda.empty_cache()
 
